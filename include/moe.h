@@ -1,0 +1,173 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) routed-MoE library.
+ *
+ * One MoE layer's routed branch on one GPU, in three calls:
+ *
+ *   moe_dispatch        x, topk_idx            -> recv [E,R,H], counts [E], src_map [T,K]
+ *   moe_expert_compute  recv, counts, weights  -> out  [E,R,H]
+ *   moe_combine         out, src_map, topk_w   -> y    [T,H]
+ *
+ * The steps follow "SGLang、NCCL 与 MoE EP" (Level 1 §1.1: the routed output
+ * is the weighted sum of the expert outputs; §2.3: receive, compact and the
+ * source map; §3.2: dispatch, compute, combine of one token) and "SGLang
+ * Expert Compute Backend" (§1.1 gated-SiLU expert; §3.5-3.7 block-wise FP8
+ * GEMMs writing each output back at its original slot).  The pages' multi-rank
+ * EP layout is modelled inside one GPU: global expert g belongs to logical rank
+ * g / L as local expert g % L, and the all-to-all exchange becomes the
+ * in-memory scatter of moe_dispatch and gather of moe_combine.
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" are CUDA device memory owned by the caller; the
+ *    library never allocates, frees or retains them.  Tensors are contiguous
+ *    and row-major.  BF16 tensors are passed as void* (IEEE bfloat16, 2 bytes).
+ *    FP8 tensors are e4m3 (OCP "float8_e4m3fn") codes, one byte each.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream): no host synchronisation, no allocation, no host reads of
+ *    device data.  All calls can be captured into a CUDA graph.
+ *  - Host-detectable errors (null pointers, bad sizes, workspace too small,
+ *    unsupported device) return a negative moe_status before anything is
+ *    launched.  MOE_ERR_CUDA means a CUDA runtime call failed; the CUDA error
+ *    is left for the caller's cudaGetLastError().
+ *  - Data-dependent problems are reported in a caller-owned device status
+ *    word `dev_status` (int32[2]): dev_status[0] holds MOE_DEV_* bits and
+ *    dev_status[1] the number of routes dropped for capacity.  moe_dispatch
+ *    resets both words; moe_expert_compute only ORs bits into dev_status[0].
+ *    Read it after your own synchronisation.
+ *  - Sizes: 0 <= T, 1 <= K <= min(E, 32), E <= 1024, 1 <= R, H and I
+ *    multiples of 128, H <= 16384, I <= 16384.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* null pointer, negative or inconsistent size */
+  MOE_ERR_UNSUPPORTED = -2, /* device is not sm_103, or a size outside the limits above */
+  MOE_ERR_WORKSPACE = -3,   /* workspace pointer null or smaller than *_workspace_size() */
+  MOE_ERR_CUDA = -4         /* a CUDA runtime call failed (see cudaGetLastError) */
+} moe_status;
+
+/* Bits of dev_status[0]. */
+#define MOE_DEV_BAD_EXPERT_ID 1    /* a topk_idx entry outside [-1, E): that route was ignored */
+#define MOE_DEV_CAPACITY_DROPPED 2 /* some expert had more than R routes; dev_status[1] = how many dropped */
+#define MOE_DEV_TIMEOUT 4          /* a bounded device-side wait expired; that kernel's outputs are invalid */
+
+/* Version of this ABI (incremented on any signature change). */
+int moe_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+/* ---------------------------------------------------------------------------
+ * Dispatch -- "SGLang、NCCL 与 MoE EP", §2.3.1 (source tensors), §2.3.4
+ * (receive and compact: recv[e, s, :] = payload, s from expert e's counter),
+ * §2.3.6 (expert_counters and the source map, flat row q = e*R + s).
+ *
+ *   x         device, BF16 [T, H]      token activations (read once per token)
+ *   topk_idx  device, int64 [T, K]     global expert ids; -1 = padding route
+ *   topk_w    device, fp32 [T, K]      accepted for interface fidelity, not read
+ *                                      (the pages keep router weights at the source)
+ *   recv      device, BF16 [E, R, H]   out: rows [0, counts[e]) of expert e hold the
+ *                                      payload of its routes; other rows untouched
+ *   counts    device, int32 [E]        out: kept routes per expert (= min(routes, R))
+ *   src_map   device, int32 [T, K]     out: q = e*R + s of route (t, k), or -1 for a
+ *                                      padding, invalid or dropped route
+ *   dev_status device, int32 [2]       out: reset, then MOE_DEV_* bits and drop count
+ *   workspace device, >= moe_dispatch_workspace_size(T, K, E) bytes, 256-byte aligned;
+ *                                      scratch, contents need not be initialised
+ *
+ * Slot order: the slot of a route within its expert is its rank among that
+ * expert's routes in ascending route id i = t*K + k (deterministic; any order
+ * would be a valid compact prefix, the pages leave it to atomic arrival order).
+ * Routes past capacity R are dropped in that order.  T == 0 is legal: counts
+ * are zeroed and nothing else is written.
+ * ------------------------------------------------------------------------- */
+size_t moe_dispatch_workspace_size(int T, int K, int E);
+moe_status moe_dispatch(const void* x, const int64_t* topk_idx, const float* topk_w, int T, int H,
+                        int K, int E, int R, void* recv, int32_t* counts, int32_t* src_map,
+                        int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                        moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Expert compute -- per-token FP8 quantisation of the valid receive rows
+ * ("SGLang、NCCL 与 MoE EP", §2.3.5; rule of "DeepEP 架构与实现笔记", §11), then
+ * the gated-SiLU expert of "SGLang Expert Compute Backend", §1.1 and §3.5-3.7:
+ * G = block-scaled FP8 GEMM of x with W13 (first I output columns gate, last
+ * I up), Z = SiLU(gate) * up re-quantised per row per 128, out = block-scaled
+ * FP8 GEMM of Z with W2, written at the original slot (e, s).
+ *
+ *   recv       device, BF16 [E, R, H]          rows >= counts[e] are never read
+ *   counts     device, int32 [E]               valid rows per expert (values > R act as R)
+ *   w13        device, e4m3 [E, 2I, H]         gate/up weights, output-major
+ *   w13_scale  device, fp32 [E, 2I/128, H/128] one scale per 128x128 block
+ *   w2         device, e4m3 [E, H, I]          down weights, output-major
+ *   w2_scale   device, fp32 [E, H/128, I/128]
+ *   out        device, BF16 [E, R, H]          out: rows [0, counts[e]); others untouched
+ *   dev_status device, int32 [2]               MOE_DEV_TIMEOUT may be ORed in
+ *   workspace  device, >= moe_expert_compute_workspace_size(E, R, H, I) bytes,
+ *              256-byte aligned; holds the FP8 activations and their scales
+ *
+ * Router weights never enter this call ("SGLang、NCCL 与 MoE EP", §1.1: the
+ * weight multiplies the expert output, not its input).
+ * ------------------------------------------------------------------------- */
+size_t moe_expert_compute_workspace_size(int E, int R, int H, int I);
+moe_status moe_expert_compute(const void* recv, const int32_t* counts, int E, int R, int H, int I,
+                              const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                              const float* w2_scale, void* out, int32_t* dev_status,
+                              void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Combine -- "SGLang、NCCL 与 MoE EP", §3.2 (合对): each route's expert output
+ * is multiplied by its router weight exactly once and summed into the token's
+ * own row; "DeepEP 架构与实现笔记", §9.6: the weighted reduce is done inside the
+ * combine kernel.
+ *
+ *   out      device, BF16 [E, R, H]   expert outputs at flat rows q
+ *   src_map  device, int32 [T, K]     from moe_dispatch; -1 entries are skipped
+ *   topk_w   device, fp32 [T, K]      router weights
+ *   y        device, BF16 [T, H]      out: y[t] = bf16( sum over k ascending of
+ *                                     w[t,k] * out[q] ), accumulated in fp32 from 0,
+ *                                     each product and each sum rounded to fp32;
+ *                                     a token with no kept route gets zeros
+ * ------------------------------------------------------------------------- */
+moe_status moe_combine(const void* out, const int32_t* src_map, const float* topk_w, int T, int H,
+                       int K, int E, int R, void* y, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The three steps inside moe_expert_compute, exposed for testing and
+ * profiling.  Scales are stored group-major, [E, G, R] (G = H/128 or I/128),
+ * so the 128 row scales of one GEMM tile and K-group are contiguous; this is
+ * the transpose of the pages' [E, R, G].
+ *
+ * moe_quantize_fp8 -- "DeepEP 架构与实现笔记", §11: per valid row and 128-group,
+ *   amax = max(max|v|, 1e-4); xq = e4m3_rn_satfinite(v * (448/amax)); xs = amax/448,
+ *   all in fp32.  xq device e4m3 [E, R, H]; xs device fp32 [E, H/128, R].
+ * moe_gemm_gateup_silu -- "SGLang Expert Compute Backend", §3.5-3.6: G from xq/xs
+ *   and W13, Z = SiLU(G[:, :I]) * G[:, I:], quantised like moe_quantize_fp8.
+ *   zq device e4m3 [E, R, I]; zs device fp32 [E, I/128, R].
+ * moe_gemm_down -- the same page, §3.6-3.7: out = block-scaled GEMM of zq/zs
+ *   with W2, BF16 [E, R, H], rows [0, counts[e]) only.
+ * Only rows < counts[e] are read or written in every step.
+ * ------------------------------------------------------------------------- */
+moe_status moe_quantize_fp8(const void* recv, const int32_t* counts, int E, int R, int H,
+                            uint8_t* xq, float* xs, moe_stream_t stream);
+moe_status moe_gemm_gateup_silu(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
+                                int R, int H, int I, const uint8_t* w13, const float* w13_scale,
+                                uint8_t* zq, float* zs, int32_t* dev_status, moe_stream_t stream);
+moe_status moe_gemm_down(const uint8_t* zq, const float* zs, const int32_t* counts, int E, int R,
+                         int H, int I, const uint8_t* w2, const float* w2_scale, void* out,
+                         int32_t* dev_status, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,96 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every entry
+point include/moe.h declares, and rejects bad arguments on the host before
+touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from token_dispatch_grouped_topk_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for fn in ("moe_dispatch", "moe_expert_compute", "moe_combine", "moe_dispatch_workspace_size",
+               "moe_expert_compute_workspace_size", "moe_quantize_fp8", "moe_gemm_gateup_silu",
+               "moe_gemm_down", "moe_abi_version", "moe_status_string"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_exports_are_c_symbols():
+    out = os.popen(f"nm -D --defined-only {_lib._build.LIB_PATH}").read()
+    exported = set(re.findall(r"\bT (moe_\w+)$", out, flags=re.M))
+    assert set(declared_functions()) <= exported
+
+
+def test_version_and_status_strings(lib):
+    assert lib.moe_abi_version() == 1
+    for code, name in _lib.STATUS.items():
+        assert lib.moe_status_string(code).decode() == name
+
+
+def test_workspace_sizes(lib):
+    assert lib.moe_dispatch_workspace_size(-1, 2, 8) == 0
+    assert lib.moe_dispatch_workspace_size(0, 2, 8) == 256
+    # one int32 per (expert, block of 8 warps x 32/K tokens)
+    assert lib.moe_dispatch_workspace_size(16384, 8, 256) == 256 * (16384 // 32) * 4
+    ws = lib.moe_expert_compute_workspace_size(2, 128, 256, 128)
+    assert ws == 2 * 128 * 256 + 2 * 2 * 128 * 4 + 2 * 128 * 128 + 2 * 1 * 128 * 4
+    assert lib.moe_expert_compute_workspace_size(2, 128, 200, 128) == 0   # H % 128 != 0
+
+
+FAKE = ctypes.c_void_p(4096)   # aligned, never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("case,expected", [
+    (dict(H=200), -1),                  # H % 128 != 0
+    (dict(K=9), -1),                    # K > E
+    (dict(T=-1), -1),
+    (dict(E=0), -1),
+    (dict(R=0), -1),
+    (dict(counts=None), -1),            # null output
+    (dict(x=None), -1),                 # null input with T > 0
+    (dict(ws_bytes=8), -3),             # workspace too small
+    (dict(ws=None), -3),
+])
+def test_dispatch_rejects_on_host(lib, case, expected):
+    a = dict(x=FAKE, idx=FAKE, T=112, H=256, K=2, E=8, R=128, recv=FAKE, counts=FAKE, src=FAKE,
+             st=FAKE, ws=FAKE, ws_bytes=1 << 20)
+    a.update(case)
+    if "K" in case:
+        a["E"] = 8
+    r = lib.moe_dispatch(a["x"], a["idx"], None, a["T"], a["H"], a["K"], a["E"], a["R"], a["recv"],
+                         a["counts"], a["src"], a["st"], a["ws"], a["ws_bytes"], None)
+    assert r == expected
+
+
+def test_compute_and_combine_reject_on_host(lib):
+    assert lib.moe_expert_compute(FAKE, FAKE, 2, 128, 256, 100, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, 1 << 30, None) == -1           # I % 128
+    assert lib.moe_expert_compute(FAKE, FAKE, 2, 128, 256, 128, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, 16, None) == -3                # workspace too small
+    assert lib.moe_expert_compute(FAKE, FAKE, 2, 128, 256, 128, None, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, 1 << 30, None) == -1           # null weights
+    misaligned = ctypes.c_void_p(4096 + 8)
+    assert lib.moe_expert_compute(FAKE, FAKE, 2, 128, 256, 128, misaligned, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, FAKE, 1 << 30, None) == -1     # TMA needs 16-byte alignment
+    assert lib.moe_combine(None, FAKE, FAKE, 4, 256, 2, 8, 128, FAKE, None) == -1
+    assert lib.moe_combine(FAKE, FAKE, FAKE, 4, 256, 40, 8, 128, FAKE, None) == -1   # K > 32
+    assert lib.moe_gemm_down(FAKE, FAKE, FAKE, 2, 128, 256, 128, FAKE, FAKE, None, FAKE, None) == -1
+    assert lib.moe_quantize_fp8(FAKE, FAKE, 2, 128, 250, FAKE, FAKE, None) == -1

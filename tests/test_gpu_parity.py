@@ -1,0 +1,372 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: dispatch (counts, src_map, the payload rows), the FP8 quantisation
+bytes and scales, and combine (against the fp32 restatement).  Within 2e-2
+max relative error per row (vs the fp64 oracle on the same quantised
+operands): the grouped GEMMs and the whole layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from token_dispatch_grouped_topk_gb300 import api
+from token_dispatch_grouped_topk_gb300 import workloads as W
+
+from helpers import REL_TOL, assert_rows_close, f32, host_weights, oracle_expert_rows, u8
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    api._lib.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def check_dispatch(x, idx, E, R, recv, counts, src_map, status):
+    """Bit-exact dispatch check against the oracle's canonical routing."""
+    rr = O.route(idx.cpu().numpy(), E, R)
+    assert counts.cpu().numpy().tolist() == rr.counts.tolist()
+    assert np.array_equal(src_map.cpu().numpy(), rr.src_map)
+    st = status.cpu().numpy()
+    assert int(st[1]) == rr.dropped
+    assert bool(st[0] & api.DEV_CAPACITY_DROPPED) == (rr.dropped > 0)
+    assert bool(st[0] & api.DEV_BAD_EXPERT_ID) == rr.bad_id
+    # payload: every kept route's row equals its token row, bit for bit
+    sm = torch.from_numpy(rr.src_map).to(x.device).long()
+    tok = torch.arange(x.shape[0], device=x.device)[:, None].expand_as(sm)
+    keep = sm >= 0
+    rows = recv.view(-1, x.shape[1])[sm[keep]]
+    assert torch.equal(rows.view(torch.int16), x[tok[keep]].view(torch.int16))
+    return rr
+
+
+# ---------------------------------------------------------------- dispatch
+
+def test_dispatch_traced_scenario():
+    d = W.make_layer_inputs("traced", seed=0, device=DEV, weights=False)
+    wl = d["wl"]
+    recv, counts, src_map, st = api.moe_dispatch(d["x"], d["topk_idx"], d["topk_w"], wl.E, wl.R)
+    torch.cuda.synchronize()
+    rr = check_dispatch(d["x"], d["topk_idx"], wl.E, wl.R, recv, counts, src_map, st)
+    assert counts.cpu().tolist() == [111, 1, 0, 0, 0, 0, 1, 111]
+    assert src_map[21].cpu().tolist() == [1 * 128, 6 * 128]
+    assert rr.dropped == 0
+
+
+@pytest.mark.parametrize("E,K", [(1, 1), (3, 2), (8, 2), (8, 8), (33, 5), (256, 8), (64, 32)])
+def test_dispatch_random_small(E, K):
+    g = torch.Generator().manual_seed(E * 100 + K)
+    for T in (0, 1, 17, 300):
+        for R in (1, 5, 64):
+            H = 128 if T > 100 else 256
+            idx = torch.randint(-1, E, (T, K), generator=g)
+            if T > 3:
+                idx[3, 0] = E + 4  # invalid id: reported, route ignored
+            x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+            xd, idd = x.to(DEV), idx.to(DEV)
+            recv, counts, src_map, st = api.moe_dispatch(xd, idd, None, E, R)
+            torch.cuda.synchronize()
+            check_dispatch(xd, idd, E, R, recv, counts, src_map, st)
+
+
+def test_dispatch_empty_rank_resets_counts():
+    counts = torch.full((8,), 99, dtype=torch.int32, device=DEV)
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty(0, 2, dtype=torch.int64, device=DEV)
+    _, counts, src_map, st = api.moe_dispatch(x, idx, None, 8, 128, counts=counts)
+    torch.cuda.synchronize()
+    assert counts.cpu().tolist() == [0] * 8 and st.cpu().tolist() == [0, 0]
+    assert src_map.shape == (0, 2)
+
+
+# ------------------------------------------------------------------- quant
+
+def test_quantize_bit_exact_ragged():
+    g = torch.Generator().manual_seed(5)
+    E, R, H = 5, 200, 640
+    counts = torch.tensor([200, 0, 1, 77, 129], dtype=torch.int32)
+    recv = (torch.randn(E, R, H, generator=g) * torch.rand(E, R, 1, generator=g) * 30).to(torch.bfloat16)
+    recv[2, 0, :128] = 0.0                   # floor case
+    recv[3, 5, 128:256] = 2.5                # constant group
+    recv[3, 6, 256:384] = 1e-30              # tiny values below the floor
+    for e in range(E):
+        recv[e, counts[e]:] = float("nan")   # capacity rows must never be read
+    rd, cd = recv.to(DEV), counts.to(DEV)
+    xq0 = torch.full((E, R, H), 0xAB, dtype=torch.uint8, device=DEV)
+    xq, xs = api.moe_quantize_fp8(rd, cd, xq=xq0)
+    torch.cuda.synchronize()
+    xq_h, xs_h = u8(xq), f32(xs)
+    for e in range(E):
+        c = int(counts[e])
+        if c == 0:
+            assert np.all(xq_h[e] == 0xAB)
+            continue
+        codes, scales = O.quantize_rows(f32(recv[e, :c]))
+        assert np.array_equal(xq_h[e, :c], codes)
+        assert np.array_equal(xs_h[e, :, :c].T, scales)
+        assert np.all(xq_h[e, c:] == 0xAB)   # capacity rows untouched
+
+
+# ------------------------------------------------------------------- GEMMs
+
+def _expert_setup(E, R, H, I, counts, seed):
+    g = torch.Generator().manual_seed(seed)
+    recv = torch.randn(E, R, H, generator=g).to(torch.bfloat16)
+    for e in range(E):
+        recv[e, counts[e]:] = float("nan")
+    w13, s13, w2, s2 = W.expert_weights(E, H, I, seed, "cpu")
+    return recv, w13, s13, w2, s2
+
+
+def _check_expert_compute(E, R, H, I, counts, seed):
+    recv, w13, s13, w2, s2 = _expert_setup(E, R, H, I, counts, seed)
+    cd = torch.tensor(counts, dtype=torch.int32, device=DEV)
+    rd = recv.to(DEV)
+    sentinel = torch.full((E, R, H), 3.0, dtype=torch.bfloat16, device=DEV)
+    # step by step through the stage entry points
+    xq, xs = api.moe_quantize_fp8(rd, cd)
+    zq, zs = api.moe_gemm_gateup_silu(xq, xs, cd, w13.to(DEV), s13.to(DEV))
+    out = api.moe_gemm_down(zq, zs, cd, w2.to(DEV), s2.to(DEV), out=sentinel.clone())
+    # and the fused call
+    st = torch.zeros(2, dtype=torch.int32, device=DEV)
+    out2 = api.moe_expert_compute(rd, cd, w13.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV),
+                                  out=sentinel.clone(), dev_status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, 0]
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    zq_h, zs_h, out_h = u8(zq), f32(zs), f32(out)
+    worst = 0.0
+    for e in range(E):
+        c = counts[e]
+        assert np.all(out_h[e, c:] == 3.0), "capacity rows of out were written"
+        if c == 0:
+            continue
+        xqo, sxo = O.quantize_rows(f32(recv[e, :c]))
+        ref, zq_ref, sz_ref, _ = O.expert_forward(xqo, sxo, u8(w13[e]), f32(s13[e]), u8(w2[e]), f32(s2[e]))
+        # Z: scales agree to fp32 rounding noise, codes to within one e4m3 step
+        assert np.allclose(zs_h[e, :, :c].T, sz_ref, rtol=1e-4, atol=0)
+        dz = np.abs(O.e4m3_decode(zq_h[e, :c]) - O.e4m3_decode(zq_ref))
+        step = np.maximum(np.abs(O.e4m3_decode(zq_ref)), 2.0 ** -6) * 2.0 ** -3
+        assert np.all(dz <= step + 1e-12)
+        assert np.mean(zq_h[e, :c] != zq_ref) < 0.01
+        worst = max(worst, assert_rows_close(out_h[e, :c], ref, what=f"expert {e}"))
+    return worst
+
+
+def test_gemm_unit_example():
+    """The pages' [70, 12] example: 2 experts, R=128, H=256, I=128; capacity
+    rows are NaN and must not leak."""
+    _check_expert_compute(2, 128, 256, 128, [70, 12], seed=3)
+
+
+def test_expert_compute_multi_tile_ragged():
+    _check_expert_compute(4, 384, 512, 384, [300, 129, 0, 17], seed=4)
+
+
+def test_expert_compute_bn128_tail():
+    """H = 384 is not a multiple of 256: the down GEMM uses 128-wide tiles."""
+    _check_expert_compute(3, 256, 384, 256, [256, 1, 130], seed=5)
+
+
+def test_expert_compute_capacity_not_multiple_of_tile():
+    _check_expert_compute(3, 200, 256, 128, [200, 199, 64], seed=6)
+
+
+# ------------------------------------------------------------------ combine
+
+def test_combine_bit_exact():
+    g = torch.Generator().manual_seed(7)
+    E, R, H, T, K = 6, 50, 384, 77, 4
+    out = (torch.randn(E, R, H, generator=g) * 3).to(torch.bfloat16)
+    src = torch.randint(-1, E * R, (T, K), generator=g).to(torch.int32)
+    src[5] = -1                               # token with no kept route
+    w = torch.rand(T, K, generator=g)
+    y = api.moe_combine(out.to(DEV), src.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    want = O.combine_f32_sequential(f32(out).reshape(E * R, H), src.numpy(), w.numpy())
+    assert np.array_equal(f32(y), want)
+    assert np.all(f32(y)[5] == 0)
+
+
+def test_identity_experts_return_input():
+    d = W.make_layer_inputs("traced", seed=1, device=DEV, weights=False)
+    wl = d["wl"]
+    recv, counts, src_map, _ = api.moe_dispatch(d["x"], d["topk_idx"], d["topk_w"], wl.E, wl.R)
+    y = api.moe_combine(recv, src_map, d["topk_w"])   # out := recv
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), d["x"].view(torch.int16))
+
+
+# -------------------------------------------------------------- whole layer
+
+def _layer_oracle(d, tokens=None):
+    wl = d["wl"]
+    x = f32(d["x"])
+    idx = d["topk_idx"].cpu().numpy()
+    w = d["topk_w"].cpu().numpy()
+    rr = O.route(idx, wl.E, wl.R)
+    toks = np.arange(wl.T) if tokens is None else np.asarray(tokens)
+    experts = sorted({int(idx[t, k]) for t in toks for k in range(wl.K) if rr.src_map[t, k] >= 0})
+    wts = host_weights(d, experts)
+    y = np.zeros((len(toks), wl.H))
+    route_out = {}
+    for e in experts:
+        sel = [(i, k) for i, t in enumerate(toks) for k in range(wl.K)
+               if idx[t, k] == e and rr.src_map[t, k] >= 0]
+        rows = oracle_expert_rows(x[[toks[i] for i, _ in sel]], wts[e])
+        for (i, k), r in zip(sel, rows):
+            y[i] += float(w[toks[i], k]) * r
+            route_out[(int(toks[i]), k)] = r
+    return y, rr, route_out
+
+
+def test_layer_traced_scenario():
+    d = W.make_layer_inputs("traced", seed=0, device=DEV)
+    wl = d["wl"]
+    buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
+    y = buf.forward(d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
+    torch.cuda.synchronize()
+    y_ref, rr, _ = _layer_oracle(d)
+    assert_rows_close(f32(y), y_ref, what="y")
+    # token 21 = 0.25 * F1(x) + 0.75 * F6(x)
+    assert buf.counts.cpu().tolist() == [111, 1, 0, 0, 0, 0, 1, 111]
+
+
+def test_graph_replay_changes_routes():
+    """Replay of one captured graph reads this round's routes: switching
+    token 21 from [E1, E6] to [E0, E7] moves counts 111/1/1/111 -> 112/0/0/112
+    and the output follows (the pages' replay example)."""
+    d = W.make_layer_inputs("traced", seed=0, device=DEV)
+    wl = d["wl"]
+    buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
+    x, idx, w = d["x"].clone(), d["topk_idx"].clone(), d["topk_w"].clone()
+    args = (d["w13"], d["s13"], d["w2"], d["s2"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        buf.forward(x, idx, w, *args)         # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        buf.forward(x, idx, w, *args)
+    swapped, _ = W.traced_routes(0, swap_token_21=True)
+    idx.copy_(swapped.to(DEV))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert [int(buf.counts[e]) for e in (0, 1, 6, 7)] == [112, 0, 0, 112]
+    d2 = dict(d, topk_idx=idx)
+    y_ref, _, _ = _layer_oracle(d2)
+    assert_rows_close(f32(buf.y), y_ref, what="replayed y")
+    idx.copy_(d["topk_idx"])
+    graph.replay()
+    torch.cuda.synchronize()
+    assert [int(buf.counts[e]) for e in (0, 1, 6, 7)] == [111, 1, 1, 111]
+
+
+def test_layer_decode_config():
+    """Decode-shaped layer, full size (T=256, E=64, top-8, H=4096, I=1536,
+    R=256): dispatch bit-exact, every token's output against the oracle."""
+    d = W.make_layer_inputs("decode", seed=0, device=DEV)
+    wl = d["wl"]
+    buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
+    y = buf.forward(d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
+    torch.cuda.synchronize()
+    check_dispatch(d["x"], d["topk_idx"], wl.E, wl.R, buf.recv, buf.counts, buf.src_map, buf.dev_status)
+    toks = np.arange(0, wl.T, 4)
+    y_ref, _, _ = _layer_oracle(d, toks)
+    assert_rows_close(f32(y)[toks], y_ref, what="decode y")
+
+
+def _sampled_out_check(d, buf, n_routes, seed):
+    """Expert outputs of sampled kept routes, one by one against the oracle."""
+    wl = d["wl"]
+    rng = np.random.default_rng(seed)
+    src = buf.src_map.cpu().numpy()
+    idx = d["topk_idx"].cpu().numpy()
+    kept = np.argwhere(src >= 0)
+    pick = kept[rng.choice(len(kept), size=min(n_routes, len(kept)), replace=False)]
+    experts = sorted({int(idx[t, k]) for t, k in pick})
+    wts = host_weights(d, experts)
+    x = d["x"]
+    out_flat = buf.out.view(-1, wl.H)
+    for e in experts:
+        sel = [(t, k) for t, k in pick if idx[t, k] == e]
+        rows = oracle_expert_rows(f32(x[[t for t, _ in sel]]), wts[e])
+        got = f32(out_flat[[int(src[t, k]) for t, k in sel]])
+        assert_rows_close(got, rows, what=f"expert {e} sampled rows")
+
+
+def test_layer_prefill_config_and_split():
+    """Prefill-shaped Zipf-skewed layer (T=4096, E=128, R=2048): dispatch
+    bit-exact (with capacity drops), sampled expert rows against the oracle,
+    combine against the fp32 restatement, and the two-micro-batch split: rows
+    of tokens whose routes are kept in both runs are bit-identical."""
+    d = W.make_layer_inputs("prefill", seed=0, device=DEV)
+    wl = d["wl"]
+    buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
+    args = (d["w13"], d["s13"], d["w2"], d["s2"])
+    y = buf.forward(d["x"], d["topk_idx"], d["topk_w"], *args).clone()
+    torch.cuda.synchronize()
+    rr = check_dispatch(d["x"], d["topk_idx"], wl.E, wl.R, buf.recv, buf.counts, buf.src_map, buf.dev_status)
+    assert rr.dropped > 0
+    _sampled_out_check(d, buf, 48, seed=1)
+    want = O.combine_f32_sequential(f32(buf.out).reshape(-1, wl.H), buf.src_map.cpu().numpy(),
+                                    d["topk_w"].cpu().numpy())
+    assert np.array_equal(f32(y), want)
+    # split into two lanes of 2048 tokens
+    half = wl.T // 2
+    lanes = [api.MoeLayerBuffers(half, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV)) for _ in range(2)]
+    ys = [lanes[i].forward(d["x"][i * half:(i + 1) * half], d["topk_idx"][i * half:(i + 1) * half],
+                           d["topk_w"][i * half:(i + 1) * half], *args) for i in range(2)]
+    torch.cuda.synchronize()
+    y_split = torch.cat(ys)
+    full_kept = (buf.src_map >= 0) | (d["topk_idx"] < 0)
+    split_map = torch.cat([lane.src_map for lane in lanes])
+    split_kept = (split_map >= 0) | (d["topk_idx"] < 0)
+    same = (full_kept.all(1) & split_kept.all(1))
+    assert int(same.sum()) > wl.T // 4
+    assert torch.equal(y_split[same].view(torch.int16), y[same].view(torch.int16))
+
+
+def test_layer_large_config_sampled():
+    """Large layer (T=16384, E=256, H=7168, I=2048, R=4096, ~11 GB of FP8
+    weights), in the launch configuration the benchmark times: dispatch
+    bit-exact, sampled expert rows against the oracle, combine bit-exact
+    against the fp32 restatement, two graph replays with new routing."""
+    d = W.make_layer_inputs("large", seed=0, device=DEV)
+    wl = d["wl"]
+    buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
+    args = (d["w13"], d["s13"], d["w2"], d["s2"])
+    idx, w = d["topk_idx"].clone(), d["topk_w"].clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        buf.forward(d["x"], idx, w, *args)
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        buf.forward(d["x"], idx, w, *args)
+    for seed in (0, 11):
+        i2, w2_ = W.router(wl.T, wl.E, wl.K, W.router_bias(wl, seed, DEV), seed + 1, DEV)
+        idx.copy_(i2)
+        w.copy_(w2_)
+        graph.replay()
+        torch.cuda.synchronize()
+        check_dispatch(d["x"], idx, wl.E, wl.R, buf.recv, buf.counts, buf.src_map, buf.dev_status)
+        dd = dict(d, topk_idx=idx, topk_w=w)
+        _sampled_out_check(dd, buf, 24, seed=seed)
+        toks = np.random.default_rng(seed).choice(wl.T, 512, replace=False)
+        sm = buf.src_map.cpu().numpy()[toks]
+        uniq, inv = np.unique(sm[sm >= 0], return_inverse=True)
+        compact = np.full_like(sm, -1)
+        compact[sm >= 0] = inv
+        rows = f32(buf.out.view(-1, wl.H)[torch.from_numpy(uniq).to(DEV).long()])
+        want = O.combine_f32_sequential(rows, compact, w.cpu().numpy()[toks])
+        assert np.array_equal(f32(buf.y)[toks], want)

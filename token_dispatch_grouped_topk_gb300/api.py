@@ -1,1 +1,206 @@
+"""Python entry points with the names of the C ABI (``include/moe.h``).
 
+PyTorch supplies device memory, tensors' ``data_ptr()`` and the current CUDA
+stream; every computation runs in the library's sm_103a kernels.  Outputs not
+passed in are allocated with torch on the input's device.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+__all__ = [
+    "MoeError", "dispatch_workspace_size", "expert_compute_workspace_size", "moe_dispatch",
+    "moe_expert_compute", "moe_combine", "moe_quantize_fp8", "moe_gemm_gateup_silu",
+    "moe_gemm_down", "MoeLayerBuffers", "DEV_BAD_EXPERT_ID", "DEV_CAPACITY_DROPPED", "DEV_TIMEOUT",
+]
+
+MoeError = _lib.MoeError
+DEV_BAD_EXPERT_ID = _lib.DEV_BAD_EXPERT_ID
+DEV_CAPACITY_DROPPED = _lib.DEV_CAPACITY_DROPPED
+DEV_TIMEOUT = _lib.DEV_TIMEOUT
+
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def _s(stream):
+    return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+
+
+def _u8(t):
+    return t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def dispatch_workspace_size(T: int, K: int, E: int) -> int:
+    return int(_lib.load().moe_dispatch_workspace_size(T, K, E))
+
+
+def expert_compute_workspace_size(E: int, R: int, H: int, I: int) -> int:
+    return int(_lib.load().moe_expert_compute_workspace_size(E, R, H, I))
+
+
+def _workspace(nbytes, device):
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def moe_dispatch(x, topk_idx, topk_w, E: int, R: int, *, recv=None, counts=None, src_map=None,
+                 dev_status=None, workspace=None, stream=None):
+    """Top-k dispatch into the expert-major receive buffer.  Returns
+    ``(recv [E,R,H] bf16, counts [E] int32, src_map [T,K] int32, dev_status [2] int32)``."""
+    lib = _lib.load()
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    dev = x.device
+    _need(x, torch.bfloat16, "x")
+    _need(topk_idx, torch.int64, "topk_idx")
+    if recv is None:
+        recv = torch.empty(E, R, H, dtype=torch.bfloat16, device=dev)
+    if counts is None:
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+    if src_map is None:
+        src_map = torch.empty(T, K, dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(2, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _workspace(lib.moe_dispatch_workspace_size(T, K, E), dev)
+    st = lib.moe_dispatch(_p(x), _p(topk_idx), _p(topk_w), T, H, K, E, R, _p(recv), _p(counts),
+                          _p(src_map), _p(dev_status), _p(workspace), workspace.numel(), _s(stream))
+    _lib.check("moe_dispatch", st)
+    return recv, counts, src_map, dev_status
+
+
+def moe_expert_compute(recv, counts, w13, w13_scale, w2, w2_scale, *, out=None, dev_status=None,
+                       workspace=None, stream=None):
+    """Quantise the valid rows and run the grouped gated-SiLU FP8 expert MLP.
+    Returns ``out [E,R,H] bf16`` (rows past counts[e] untouched)."""
+    lib = _lib.load()
+    E, R, H = recv.shape
+    w13, w2 = _u8(w13), _u8(w2)
+    I = w13.shape[1] // 2
+    dev = recv.device
+    if out is None:
+        out = torch.empty(E, R, H, dtype=torch.bfloat16, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(2, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _workspace(lib.moe_expert_compute_workspace_size(E, R, H, I), dev)
+    st = lib.moe_expert_compute(_p(recv), _p(counts), E, R, H, I, _p(w13), _p(w13_scale), _p(w2),
+                                _p(w2_scale), _p(out), _p(dev_status), _p(workspace),
+                                workspace.numel(), _s(stream))
+    _lib.check("moe_expert_compute", st)
+    return out
+
+
+def moe_combine(out, src_map, topk_w, *, y=None, stream=None):
+    """Weighted combine back into token order.  Returns ``y [T,H] bf16``."""
+    lib = _lib.load()
+    E, R, H = out.shape
+    T, K = src_map.shape
+    if y is None:
+        y = torch.empty(T, H, dtype=torch.bfloat16, device=out.device)
+    st = lib.moe_combine(_p(out), _p(src_map), _p(topk_w), T, H, K, E, R, _p(y), _s(stream))
+    _lib.check("moe_combine", st)
+    return y
+
+
+def moe_quantize_fp8(recv, counts, *, xq=None, xs=None, stream=None):
+    """Per-token FP8 quantisation of the valid rows: ``xq [E,R,H] uint8`` (e4m3
+    codes) and ``xs [E,H/128,R] fp32``."""
+    lib = _lib.load()
+    E, R, H = recv.shape
+    if xq is None:
+        xq = torch.empty(E, R, H, dtype=torch.uint8, device=recv.device)
+    if xs is None:
+        xs = torch.empty(E, H // 128, R, dtype=torch.float32, device=recv.device)
+    st = lib.moe_quantize_fp8(_p(recv), _p(counts), E, R, H, _p(xq), _p(xs), _s(stream))
+    _lib.check("moe_quantize_fp8", st)
+    return xq, xs
+
+
+def moe_gemm_gateup_silu(xq, xs, counts, w13, w13_scale, *, zq=None, zs=None, dev_status=None,
+                         stream=None):
+    """Gate/up GEMM + SiLU(gate)*up + FP8 requant: ``zq [E,R,I]``, ``zs [E,I/128,R]``."""
+    lib = _lib.load()
+    E, R, H = xq.shape
+    w13 = _u8(w13)
+    I = w13.shape[1] // 2
+    dev = xq.device
+    if zq is None:
+        zq = torch.empty(E, R, I, dtype=torch.uint8, device=dev)
+    if zs is None:
+        zs = torch.empty(E, I // 128, R, dtype=torch.float32, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(2, dtype=torch.int32, device=dev)
+    st = lib.moe_gemm_gateup_silu(_p(_u8(xq)), _p(xs), _p(counts), E, R, H, I, _p(w13),
+                                  _p(w13_scale), _p(zq), _p(zs), _p(dev_status), _s(stream))
+    _lib.check("moe_gemm_gateup_silu", st)
+    return zq, zs
+
+
+def moe_gemm_down(zq, zs, counts, w2, w2_scale, *, out=None, dev_status=None, stream=None):
+    """Down GEMM: ``out [E,R,H] bf16`` for the valid rows."""
+    lib = _lib.load()
+    E, R, I = zq.shape
+    w2 = _u8(w2)
+    H = w2.shape[1]
+    dev = zq.device
+    if out is None:
+        out = torch.empty(E, R, H, dtype=torch.bfloat16, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(2, dtype=torch.int32, device=dev)
+    st = lib.moe_gemm_down(_p(_u8(zq)), _p(zs), _p(counts), E, R, H, I, _p(w2), _p(w2_scale),
+                           _p(out), _p(dev_status), _s(stream))
+    _lib.check("moe_gemm_down", st)
+    return out
+
+
+@dataclass
+class MoeLayerBuffers:
+    """One resource set ("lane") for a routed MoE layer: every buffer the three
+    calls touch, allocated once so the calls can be repeated or captured into a
+    CUDA graph.  Two instances give the two independent lanes a two-micro-batch
+    split needs ("SGLang、NCCL 与 MoE EP", §2.4: each micro-batch owns its own
+    receive, routing and output storage)."""
+
+    T: int
+    E: int
+    K: int
+    H: int
+    I: int
+    R: int
+    device: torch.device
+
+    def __post_init__(self):
+        d, E, R, H, I, T, K = self.device, self.E, self.R, self.H, self.I, self.T, self.K
+        self.recv = torch.empty(E, R, H, dtype=torch.bfloat16, device=d)
+        self.out = torch.empty(E, R, H, dtype=torch.bfloat16, device=d)
+        self.counts = torch.zeros(E, dtype=torch.int32, device=d)
+        self.src_map = torch.empty(T, K, dtype=torch.int32, device=d)
+        self.dev_status = torch.zeros(2, dtype=torch.int32, device=d)
+        self.y = torch.empty(T, H, dtype=torch.bfloat16, device=d)
+        self.ws_dispatch = _workspace(dispatch_workspace_size(T, K, E), d)
+        self.ws_compute = _workspace(expert_compute_workspace_size(E, R, H, I), d)
+
+    def forward(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None):
+        """dispatch -> expert compute -> combine on one stream; returns ``y``."""
+        moe_dispatch(x, topk_idx, topk_w, self.E, self.R, recv=self.recv, counts=self.counts,
+                     src_map=self.src_map, dev_status=self.dev_status, workspace=self.ws_dispatch,
+                     stream=stream)
+        moe_expert_compute(self.recv, self.counts, w13, w13_scale, w2, w2_scale, out=self.out,
+                           dev_status=self.dev_status, workspace=self.ws_compute, stream=stream)
+        moe_combine(self.out, self.src_map, topk_w, y=self.y, stream=stream)
+        return self.y

@@ -1,0 +1,205 @@
+// Dispatch: route validation, per-expert counting, slot assignment and the
+// payload scatter into the expert-major receive buffer.
+//
+// "SGLang、NCCL 与 MoE EP", §2.3.4: every route to expert e takes a row s from
+// e's counter, the payload is written to recv[e, s, :] and the flat row
+// q = e*R + s is recorded for combine (§2.3.6).  On one GPU the per-expert
+// counter is replaced by a deterministic three-kernel scheme so the slot of a
+// route is its rank among e's routes in ascending route id:
+//   1. route_hist    -- each block counts its routes per expert (warp match +
+//                       shared-memory atomics; integer sums are order-free);
+//   2. route_scan    -- one block per expert: exclusive scan of the block
+//                       counts, counts[e] = min(total, R), drops reported;
+//   3. route_scatter -- each block re-derives the in-block rank of its routes
+//                       (warp match + per-warp counts), writes src_map and
+//                       copies each token row once from x to its K rows of
+//                       recv with 16-byte vector accesses.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+// Lane `lane` of global warp `gw` holds route (t, k) with
+// t = gw * (32/K) + lane / K and k = lane % K.
+struct RouteLane {
+  int t, k, e;  // e = expert id, or -1 for padding / invalid id / idle lane
+  bool active;  // the lane maps to a real route (t < T)
+};
+
+__device__ __forceinline__ RouteLane load_route(const int64_t* __restrict__ topk_idx, int T, int K,
+                                                int E, int gw, int lane, int32_t* dev_status) {
+  const int tpw = 32 / K;
+  RouteLane r;
+  r.t = gw * tpw + lane / K;
+  r.k = lane % K;
+  r.active = (lane < tpw * K) && (r.t < T);
+  r.e = -1;
+  if (r.active) {
+    const int64_t id = topk_idx[static_cast<int64_t>(r.t) * K + r.k];
+    if (id >= 0 && id < E) {
+      r.e = static_cast<int>(id);
+    } else if (id != -1 && dev_status != nullptr) {
+      atomicOr(dev_status, kDevBadExpertId);
+    }
+  }
+  return r;
+}
+
+__global__ void __launch_bounds__(kDispatchWarps * 32)
+    route_hist_kernel(const int64_t* __restrict__ topk_idx, int T, int K, int E, int nblocks,
+                      int32_t* __restrict__ hist, int32_t* dev_status) {
+  extern __shared__ int s_hist[];  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const RouteLane r =
+      load_route(topk_idx, T, K, E, blockIdx.x * kDispatchWarps + warp, lane, dev_status);
+  const unsigned peers = __match_any_sync(0xffffffffu, r.e);
+  if (r.e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&s_hist[r.e], __popc(peers));
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    hist[static_cast<size_t>(e) * nblocks + blockIdx.x] = s_hist[e];
+}
+
+constexpr int kScanThreads = 512;
+
+__global__ void __launch_bounds__(kScanThreads)
+    route_scan_kernel(int32_t* __restrict__ hist, int nblocks, int R, int32_t* __restrict__ counts,
+                      int32_t* dev_status) {
+  __shared__ int s_warp[kScanThreads / 32];
+  const int e = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int32_t* h = hist + static_cast<size_t>(e) * nblocks;
+  const int per = (nblocks + kScanThreads - 1) / kScanThreads;
+  const int b0 = threadIdx.x * per;
+  int local = 0;
+  for (int i = 0; i < per; ++i)
+    if (b0 + i < nblocks) local += h[b0 + i];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < kScanThreads / 32 ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (lane < kScanThreads / 32) s_warp[lane] = v;
+  }
+  __syncthreads();
+  int run = (warp > 0 ? s_warp[warp - 1] : 0) + incl - local;
+  for (int i = 0; i < per; ++i) {
+    if (b0 + i < nblocks) {
+      const int v = h[b0 + i];
+      h[b0 + i] = run;
+      run += v;
+    }
+  }
+  if (threadIdx.x == 0) {
+    const int total = s_warp[kScanThreads / 32 - 1];
+    counts[e] = min(total, R);
+    if (total > R) {
+      atomicAdd(dev_status + 1, total - R);
+      atomicOr(dev_status, kDevCapacityDropped);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kDispatchWarps * 32)
+    route_scatter_kernel(const uint4* __restrict__ x, const int64_t* __restrict__ topk_idx, int T,
+                         int H, int K, int E, int R, int nblocks, const int32_t* __restrict__ base,
+                         uint4* __restrict__ recv, int32_t* __restrict__ src_map,
+                         int vec_per_slice) {
+  extern __shared__ int smem[];
+  int* s_cnt = smem;                           // [kDispatchWarps][E]
+  int* s_dest = smem + kDispatchWarps * E;     // [kDispatchWarps][32]
+  for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kDispatchWarps + warp;
+  const RouteLane r = load_route(topk_idx, T, K, E, gw, lane, nullptr);
+  const unsigned peers = __match_any_sync(0xffffffffu, r.e);
+  const int lane_rank = __popc(peers & ((1u << lane) - 1u));
+  if (r.e >= 0 && lane == __ffs(peers) - 1) s_cnt[warp * E + r.e] = __popc(peers);
+  __syncthreads();
+  int q = -1;
+  if (r.e >= 0) {
+    int s = base[static_cast<size_t>(r.e) * nblocks + blockIdx.x] + lane_rank;
+    for (int w = 0; w < warp; ++w) s += s_cnt[w * E + r.e];
+    if (s < R) q = r.e * R + s;
+  }
+  if (blockIdx.y == 0 && r.active) src_map[static_cast<int64_t>(r.t) * K + r.k] = q;
+  s_dest[warp * 32 + lane] = q;
+  __syncwarp();
+
+  // Payload: each token row is read once (this block's slice of it) and
+  // written to every kept destination row.
+  const int tpw = 32 / K;
+  const int nvec = H / 8;
+  const int v0 = blockIdx.y * vec_per_slice;
+  const int v1 = min(nvec, v0 + vec_per_slice);
+  const int* wdest = s_dest + warp * 32;
+  for (int tt = 0; tt < tpw; ++tt) {
+    const int t = gw * tpw + tt;
+    if (t >= T) break;
+    const int* dq = wdest + tt * K;
+    bool any = false;
+    for (int k = 0; k < K; ++k) any |= dq[k] >= 0;
+    if (!any) continue;
+    const uint4* src = x + static_cast<size_t>(t) * nvec;
+    for (int v = v0 + lane; v < v1; v += 32 * 4) {
+      uint4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v + 32 * u < v1) a[u] = ld_stream(src + v + 32 * u);
+      for (int k = 0; k < K; ++k) {
+        const int qq = dq[k];
+        if (qq < 0) continue;
+        uint4* dst = recv + static_cast<size_t>(qq) * nvec;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v + 32 * u < v1) dst[v + 32 * u] = a[u];
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
+                            int R, void* recv, int32_t* counts, int32_t* src_map,
+                            int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s) {
+  cudaError_t err = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
+  if (err != cudaSuccess) return err;
+  const int nblocks = dispatch_blocks(T, K);
+  if (nblocks > 0) {
+    route_hist_kernel<<<nblocks, kDispatchWarps * 32, E * sizeof(int), s>>>(topk_idx, T, K, E,
+                                                                            nblocks, hist, dev_status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  route_scan_kernel<<<E, kScanThreads, 0, s>>>(hist, nblocks, R, counts, dev_status);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (nblocks == 0) return cudaSuccess;
+  // Split each row into column slices when there are too few tokens to keep
+  // enough warps in flight; a slice keeps at least 32 vectors (512 bytes).
+  const int nvec = H / 8;
+  const int target_warps = sm_count * 48;
+  int hsplit = (target_warps + nblocks * kDispatchWarps - 1) / (nblocks * kDispatchWarps);
+  hsplit = max(1, min(hsplit, nvec / 32));
+  const int vec_per_slice = (nvec + hsplit - 1) / hsplit;
+  hsplit = (nvec + vec_per_slice - 1) / vec_per_slice;
+  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32) * sizeof(int);
+  route_scatter_kernel<<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
+      static_cast<const uint4*>(x), topk_idx, T, H, K, E, R, nblocks, hist,
+      static_cast<uint4*>(recv), src_map, vec_per_slice);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

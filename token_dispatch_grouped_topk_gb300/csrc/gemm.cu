@@ -1,0 +1,466 @@
+// Grouped block-scaled FP8 GEMMs of the gated-SiLU expert on tcgen05.
+//
+// "SGLang Expert Compute Backend", §3.5: activations carry one fp32 scale per
+// row per 128 K-elements, weights (stored [E, N, K]) one per 128x128 block, and
+//   G[m, n] = sum_g  sx[m, g] * sw[n/128, g] * sum_{k in g} xq[m, k] * wq[n, k].
+// §2.4: each expert's valid rows are tiled on their own; only tiles that hold
+// valid rows are scheduled.  §3.6: the gate/up output's first I columns are
+// gate and the last I up; Z = SiLU(gate) * up is re-quantised per row per 128
+// for the down GEMM, whose output is written back at the original slot (§3.7).
+//
+// Design (one CTA per SM, persistent):
+//  - tiles are 128 rows x BN columns of one expert; the tile list is derived on
+//    the device from counts (prefix of ceil(count/128) * n_tiles per expert),
+//    walked by all CTAs with a stride of gridDim.x.  Within an expert the M
+//    blocks of one N slice are adjacent so concurrently running CTAs share the
+//    same weight slice in L2;
+//  - warp 0 (one thread) streams A and B tiles with TMA (128-byte swizzle) into
+//    a 4-stage shared-memory ring guarded by full/empty mbarriers;
+//  - warp 1 (one thread) issues tcgen05.mma kind::f8f6f4 (M=128, N=BN, K=32,
+//    fp32 accumulate) -- one 128-wide K group per TMEM buffer, two buffers, so
+//    the tensor core fills one while the epilogue drains the other;
+//  - warp 2 owns the TMEM allocation;
+//  - warps 4-11 promote each K group's partial product: acc += sx * sw * P in
+//    registers (the fp32 scales are not of a form the hardware block-scaled
+//    MMA accepts), then run the fused epilogue: SiLU(gate) * up and the
+//    per-row FP8 requantisation of Z for the gate/up GEMM, BF16 rows for the
+//    down GEMM.  Only rows below counts[e] are stored.
+// Every wait is bounded; on expiry the kernel raises MOE_DEV_TIMEOUT in the
+// status word, drains its own copies and MMAs, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 128;
+constexpr int kStages = 4;
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiThreads = 256;
+constexpr int kMaxExperts = 1024;
+
+struct GemmArgs {
+  const int32_t* counts;
+  const float* a_scale;  // [E, nkb, R]
+  const float* w_scale;  // [E, Ndim/128, nkb]
+  int E, R, nkb, n_tiles;
+  int I, H;
+  uint8_t* zq;           // gate/up: [E, R, I]
+  float* zs;             // gate/up: [E, I/128, R]
+  __nv_bfloat16* out;    // down: [E, R, H]
+  int32_t* dev_status;
+};
+
+struct Control {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint64_t amax_bar;
+  uint32_t tmem_base;
+  int abort;
+  int tile_start[kMaxExperts + 1];
+  int cnt[kMaxExperts];
+  float amax[2][2][kBM];  // [tile parity][column half][row]
+};
+
+template <int BN>
+struct Layout {
+  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Control);
+};
+
+struct Tile {
+  int e, m_blk, n_blk, rows;
+};
+
+__device__ __forceinline__ Tile decode_tile(const Control* ctl, int E, int n_tiles, int t) {
+  Tile r;
+  r.e = find_expert(ctl->tile_start, E, t);
+  const int local = t - ctl->tile_start[r.e];
+  const int mt = (ctl->tile_start[r.e + 1] - ctl->tile_start[r.e]) / n_tiles;
+  r.n_blk = local / mt;
+  r.m_blk = local - r.n_blk * mt;
+  r.rows = min(kBM, ctl->cnt[r.e] - r.m_blk * kBM);
+  return r;
+}
+
+// Bounded wait used while draining after an abort (ignores the abort flag).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  int dummy = 0;
+  mbar_wait(bar, parity, &dummy);
+}
+
+template <int BN, bool kGateUp>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+  using L = Layout<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  Control* ctl = reinterpret_cast<Control*>(smem + kStages * L::kStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&ctl->full[i], 1);
+      mbar_init(&ctl->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->tfull[i], 1);
+      mbar_init(&ctl->tempty[i], kEpiThreads / 32);
+    }
+    mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->amax_bar, kEpiThreads);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 2) {
+    tmem_alloc(&ctl->tmem_base, L::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  // Tile prefix per expert (ends with __syncthreads, which also publishes the
+  // barrier initialisation and the TMEM address).
+  expert_prefix(args.counts, args.E, args.R, kBM, args.n_tiles, ctl->tile_start, ctl->cnt);
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const int total = ctl->tile_start[args.E];
+  volatile int* abort_flag = &ctl->abort;
+  const int nkb = args.nkb;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile(ctl, args.E, args.n_tiles, t);
+        const int a_row = tl.e * args.R + tl.m_blk * kBM;
+        int b_row0, b_row1;
+        if (kGateUp) {
+          b_row0 = tl.e * 2 * args.I + tl.n_blk * 128;
+          b_row1 = b_row0 + args.I;
+        } else {
+          b_row0 = tl.e * args.H + tl.n_blk * BN;
+          b_row1 = b_row0 + 128;
+        }
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int stage = issued % kStages;
+          const uint32_t phase = (issued / kStages) & 1;
+          if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * L::kStageBytes;
+          uint8_t* sb = sa + L::kABytes;
+          mbar_arrive_expect_tx(&ctl->full[stage], L::kStageBytes);
+          tma_load_2d(sa, &tmA, &ctl->full[stage], kb * kBK, a_row);
+          tma_load_2d(sb, &tmB, &ctl->full[stage], kb * kBK, b_row0);
+          if (BN == 256) tma_load_2d(sb + 128 * kBK, &tmB, &ctl->full[stage], kb * kBK, b_row1);
+          ++issued;
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      // No copy may land after the block exits: wait for the last loads.
+      for (int i = 0; i < min(issued, kStages); ++i) {
+        const int n = issued - 1 - i;
+        drain_wait(&ctl->full[n % kStages], (n / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
+      int consumed = 0, kcount = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int stage = consumed % kStages;
+          const uint32_t phase = (consumed / kStages) & 1;
+          const int acc = kcount & 1;
+          const uint32_t acc_phase = (kcount >> 1) & 1;
+          if (!mbar_wait(&ctl->tempty[acc], acc_phase ^ 1, abort_flag) ||
+              !mbar_wait(&ctl->full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * L::kStageBytes);
+          const uint64_t adesc = smem_desc_kmajor_sw128(sa);
+          const uint64_t bdesc = smem_desc_kmajor_sw128(sa + L::kABytes);
+          const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k)  // 32 e4m3 = 32 bytes = 2 descriptor units
+            mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
+          mma_commit(&ctl->empty[stage]);
+          mma_commit(&ctl->tfull[acc]);
+          ++consumed;
+          ++kcount;
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      if (kcount > 0) {
+        mma_commit(&ctl->drain);
+        drain_wait(&ctl->drain, 0);
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------------------ epilogue
+    constexpr int kCols = BN / 2;  // columns of the tile this thread owns
+    const int ew = warp - kEpiWarp0;
+    const int lq = warp & 3;       // TMEM lane quarter accessible to this warp
+    const int ch = ew >> 2;        // which half of the tile's columns
+    const int row = lq * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(lq * 32) << 16);
+    int kcount = 0, iter = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++iter) {
+      const Tile tl = decode_tile(ctl, args.E, args.n_tiles, t);
+      const int m = tl.m_blk * kBM + row;
+      const bool in_cap = m < args.R;
+      const float* asc = args.a_scale + static_cast<size_t>(tl.e) * nkb * args.R + m;
+      const float* wsc0;
+      const float* wsc1;
+      if (kGateUp) {
+        const int nb = 2 * args.I / 128;
+        wsc0 = args.w_scale + (static_cast<size_t>(tl.e) * nb + tl.n_blk) * nkb;
+        wsc1 = args.w_scale + (static_cast<size_t>(tl.e) * nb + args.I / 128 + tl.n_blk) * nkb;
+      } else {
+        const int nb = args.H / 128;
+        const int cb = (tl.n_blk * BN + ch * kCols) / 128;
+        wsc0 = args.w_scale + (static_cast<size_t>(tl.e) * nb + cb) * nkb;
+        wsc1 = wsc0;
+      }
+      float accv[kCols];
+#pragma unroll
+      for (int i = 0; i < kCols; ++i) accv[i] = 0.f;
+      float sa_next = in_cap ? __ldg(asc) : 0.f;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const float sa = sa_next;
+        if (kb + 1 < nkb) sa_next = in_cap ? __ldg(asc + static_cast<size_t>(kb + 1) * args.R) : 0.f;
+        const float s0 = sa * __ldg(wsc0 + kb);
+        const float s1 = kGateUp ? sa * __ldg(wsc1 + kb) : s0;
+        const int acc = kcount & 1;
+        const uint32_t acc_phase = (kcount >> 1) & 1;
+        if (!mbar_wait(&ctl->tfull[acc], acc_phase, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t base = t_lane + static_cast<uint32_t>(acc * BN);
+        float buf[32];
+        if (kGateUp) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            tmem_load32_sync(base + ch * 64 + 32 * j, buf);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) accv[32 * j + i] = fmaf(s0, buf[i], accv[32 * j + i]);
+          }
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            tmem_load32_sync(base + 128 + ch * 64 + 32 * j, buf);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              accv[64 + 32 * j + i] = fmaf(s1, buf[i], accv[64 + 32 * j + i]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kCols / 32; ++j) {
+            tmem_load32_sync(base + ch * kCols + 32 * j, buf);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) accv[32 * j + i] = fmaf(s0, buf[i], accv[32 * j + i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
+        ++kcount;
+      }
+      if (!ok) break;
+      const bool valid = row < tl.rows;
+      if (kGateUp) {
+        // Z = SiLU(gate) * up for this thread's 64 columns, then the row amax
+        // over the 128 columns shared with the partner warp (other half).
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float g = accv[i];
+          const float z = (g / (1.0f + expf(-g))) * accv[64 + i];
+          accv[i] = z;
+          amax = fmaxf(amax, fabsf(z));
+        }
+        const int par = iter & 1;
+        ctl->amax[par][ch][row] = amax;
+        mbar_arrive(&ctl->amax_bar);
+        if (!mbar_wait(&ctl->amax_bar, par, abort_flag)) {
+          ok = false;
+          break;
+        }
+        amax = fmaxf(ctl->amax[par][0][row], ctl->amax[par][1][row]);
+        float mult, scale;
+        fp8_group_scale(amax, &mult, &scale);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(
+              args.zq + (static_cast<size_t>(tl.e) * args.R + m) * args.I + tl.n_blk * 128 + ch * 64);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int c = 16 * j + 4 * i;
+              w[i] = static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(accv[c], mult), __fmul_rn(accv[c + 1], mult))) |
+                     (static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(accv[c + 2], mult),
+                                                        __fmul_rn(accv[c + 3], mult)))
+                      << 16);
+            }
+            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          if (ch == 0)
+            args.zs[(static_cast<size_t>(tl.e) * (args.I / 128) + tl.n_blk) * args.R + m] = scale;
+        }
+      } else if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(
+            args.out + (static_cast<size_t>(tl.e) * args.R + m) * args.H + tl.n_blk * BN + ch * kCols);
+#pragma unroll
+        for (int j = 0; j < kCols / 8; ++j) {
+          uint4 o;
+          o.x = pack_bf16x2_rn(accv[8 * j + 0], accv[8 * j + 1]);
+          o.y = pack_bf16x2_rn(accv[8 * j + 2], accv[8 * j + 3]);
+          o.z = pack_bf16x2_rn(accv[8 * j + 4], accv[8 * j + 5]);
+          o.w = pack_bf16x2_rn(accv[8 * j + 6], accv[8 * j + 7]);
+          dst[j] = o;
+        }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  }
+
+  // --------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+  if (threadIdx.x == 0 && ctl->abort) atomicOr(args.dev_status, kDevTimeout);
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 2D map over a row-major byte matrix [rows, cols] with 128 x 128 boxes and
+// the 128-byte swizzle the MMA descriptors expect.
+cudaError_t make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BN, bool kGateUp>
+cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+                        int sm_count, cudaStream_t s) {
+  using L = Layout<BN>;
+  const long long ub = static_cast<long long>(a.E) * ((a.R + kBM - 1) / kBM) * a.n_tiles;
+  const int grid = static_cast<int>(std::min<long long>(ub, sm_count));
+  if (grid <= 0) return cudaSuccess;
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BN, kGateUp>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L::kSmem));
+  if (err != cudaSuccess) return err;
+  grouped_gemm_kernel<BN, kGateUp><<<grid, kThreads, L::kSmem, s>>>(ta, tb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
+                               int R, int H, int I, const uint8_t* w13, const float* w13_scale,
+                               uint8_t* zq, float* zs, int32_t* dev_status, int sm_count,
+                               cudaStream_t s) {
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  cudaError_t err = make_map_u8(&ta, xq, H, static_cast<uint64_t>(E) * R);
+  if (err == cudaSuccess) err = make_map_u8(&tb, w13, H, static_cast<uint64_t>(E) * 2 * I);
+  if (err != cudaSuccess) return err;
+  GemmArgs a{};
+  a.counts = counts;
+  a.a_scale = xs;
+  a.w_scale = w13_scale;
+  a.E = E;
+  a.R = R;
+  a.nkb = H / kBK;
+  a.n_tiles = I / 128;
+  a.I = I;
+  a.H = H;
+  a.zq = zq;
+  a.zs = zs;
+  a.dev_status = dev_status;
+  return launch_impl<256, true>(ta, tb, a, sm_count, s);
+}
+
+cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* counts, int E,
+                             int R, int H, int I, const uint8_t* w2, const float* w2_scale,
+                             void* out, int32_t* dev_status, int sm_count, cudaStream_t s) {
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  cudaError_t err = make_map_u8(&ta, zq, I, static_cast<uint64_t>(E) * R);
+  if (err == cudaSuccess) err = make_map_u8(&tb, w2, I, static_cast<uint64_t>(E) * H);
+  if (err != cudaSuccess) return err;
+  GemmArgs a{};
+  a.counts = counts;
+  a.a_scale = zs;
+  a.w_scale = w2_scale;
+  a.E = E;
+  a.R = R;
+  a.nkb = I / kBK;
+  a.I = I;
+  a.H = H;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.dev_status = dev_status;
+  if (H % 256 == 0) {
+    a.n_tiles = H / 256;
+    return launch_impl<256, false>(ta, tb, a, sm_count, s);
+  }
+  a.n_tiles = H / 128;
+  return launch_impl<128, false>(ta, tb, a, sm_count, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,51 @@
+// Internal launch wrappers of the sm_103a kernels (host side).  The C ABI in
+// include/moe.h validates arguments and then calls these.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct DeviceInfo {
+  int sm_count;
+  int cc_major;
+  int cc_minor;
+  size_t smem_optin;
+};
+// Cached properties of the current device; nullptr if the query fails.
+const DeviceInfo* current_device_info();
+
+// ----- dispatch (route validation, histogram, scan, stable scatter)
+constexpr int kDispatchWarps = 8;
+inline int dispatch_tokens_per_warp(int K) { return 32 / K; }
+inline int dispatch_tokens_per_block(int K) { return kDispatchWarps * (32 / K); }
+inline int dispatch_blocks(int T, int K) {
+  const int tpb = dispatch_tokens_per_block(K);
+  return (T + tpb - 1) / tpb;
+}
+cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
+                            int R, void* recv, int32_t* counts, int32_t* src_map,
+                            int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s);
+
+// ----- per-token FP8 quantisation of the valid rows; xs is [E, H/128, R]
+cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, int R, int H,
+                            uint8_t* xq, float* xs, int sm_count, cudaStream_t s);
+
+// ----- grouped block-scaled FP8 GEMMs on tcgen05
+cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
+                               int R, int H, int I, const uint8_t* w13, const float* w13_scale,
+                               uint8_t* zq, float* zs, int32_t* dev_status, int sm_count,
+                               cudaStream_t s);
+cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* counts, int E,
+                             int R, int H, int I, const uint8_t* w2, const float* w2_scale,
+                             void* out, int32_t* dev_status, int sm_count, cudaStream_t s);
+
+// ----- weighted combine
+// rows = E * R, the number of rows of `out`; a src_map entry outside
+// [0, rows) is treated like -1.
+cudaError_t launch_combine(const void* out, const int32_t* src_map, const float* topk_w, int T,
+                           int H, int K, int64_t rows, void* y, int sm_count, cudaStream_t s);
+
+}  // namespace moe

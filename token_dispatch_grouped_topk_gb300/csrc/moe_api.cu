@@ -1,0 +1,221 @@
+// The C ABI of include/moe.h: argument validation, workspace carving and the
+// launch sequence of each call.  No call allocates, synchronises or reads
+// device memory on the host.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_info_mu;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ok[kMaxDevices];
+
+constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+const DeviceInfo* current_device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_info_mu);
+  if (!g_info_ok[dev]) {
+    DeviceInfo d{};
+    int smem = 0;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return nullptr;
+    d.smem_optin = static_cast<size_t>(smem);
+    g_info[dev] = d;
+    g_info_ok[dev] = true;
+  }
+  return &g_info[dev];
+}
+
+namespace {
+
+// The kernels are built for sm_103a only.
+moe_status check_device(const DeviceInfo** out) {
+  const DeviceInfo* d = current_device_info();
+  if (d == nullptr) return MOE_ERR_CUDA;
+  if (d->cc_major != 10 || d->cc_minor != 3) return MOE_ERR_UNSUPPORTED;
+  *out = d;
+  return MOE_OK;
+}
+
+bool valid_hidden(int H) { return H > 0 && H % 128 == 0 && H <= 16384; }
+bool valid_experts(int E, int R) {
+  return E >= 1 && E <= 1024 && R >= 1 && static_cast<int64_t>(E) * R <= (int64_t{1} << 30);
+}
+
+struct ComputeWorkspace {
+  size_t xq, xs, zq, zs, total;
+};
+
+ComputeWorkspace compute_workspace(int E, int R, int H, int I) {
+  ComputeWorkspace w{};
+  const size_t rows = static_cast<size_t>(E) * R;
+  size_t off = 0;
+  w.xq = off;
+  off = align_up(off + rows * H, 256);
+  w.xs = off;
+  off = align_up(off + rows * (H / 128) * sizeof(float), 256);
+  w.zq = off;
+  off = align_up(off + rows * I, 256);
+  w.zs = off;
+  off = align_up(off + rows * (I / 128) * sizeof(float), 256);
+  w.total = off;
+  return w;
+}
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return 1; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+size_t moe_dispatch_workspace_size(int T, int K, int E) {
+  if (T < 0 || K < 1 || K > 32 || E < 1) return 0;
+  const size_t nb = static_cast<size_t>(dispatch_blocks(T, K));
+  return align_up(std::max<size_t>(nb * E * sizeof(int32_t), 1), 256);
+}
+
+moe_status moe_dispatch(const void* x, const int64_t* topk_idx, const float* topk_w, int T, int H,
+                        int K, int E, int R, void* recv, int32_t* counts, int32_t* src_map,
+                        int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                        moe_stream_t stream) {
+  (void)topk_w;  // router weights stay at the source; combine reads them
+  if (T < 0 || !valid_hidden(H) || !valid_experts(E, R) || K < 1 || K > 32 || K > E)
+    return MOE_ERR_INVALID_ARG;
+  if (counts == nullptr || dev_status == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || topk_idx == nullptr || recv == nullptr || src_map == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(x) || !aligned16(recv))) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * K > (int64_t{1} << 31) - 1) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_dispatch_workspace_size(T, K, E);
+  if (workspace == nullptr || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_dispatch(x, topk_idx, T, H, K, E, R, recv, counts, src_map, dev_status,
+                                   static_cast<int32_t*>(workspace), dev->sm_count,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_expert_compute_workspace_size(int E, int R, int H, int I) {
+  if (!valid_experts(E, R) || !valid_hidden(H) || !valid_hidden(I)) return 0;
+  return compute_workspace(E, R, H, I).total;
+}
+
+moe_status moe_quantize_fp8(const void* recv, const int32_t* counts, int E, int R, int H,
+                            uint8_t* xq, float* xs, moe_stream_t stream) {
+  if (!valid_experts(E, R) || !valid_hidden(H)) return MOE_ERR_INVALID_ARG;
+  if (recv == nullptr || counts == nullptr || xq == nullptr || xs == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(recv) || (reinterpret_cast<uintptr_t>(xq) & 7u) != 0) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_quantize(recv, counts, E, R, H, xq, xs, dev->sm_count,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_gemm_gateup_silu(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
+                                int R, int H, int I, const uint8_t* w13, const float* w13_scale,
+                                uint8_t* zq, float* zs, int32_t* dev_status, moe_stream_t stream) {
+  if (!valid_experts(E, R) || !valid_hidden(H) || !valid_hidden(I)) return MOE_ERR_INVALID_ARG;
+  if (xq == nullptr || xs == nullptr || counts == nullptr || w13 == nullptr ||
+      w13_scale == nullptr || zq == nullptr || zs == nullptr || dev_status == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xq) || !aligned16(w13) || !aligned16(zq)) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_gemm_gateup(xq, xs, counts, E, R, H, I, w13, w13_scale, zq, zs,
+                                      dev_status, dev->sm_count,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_gemm_down(const uint8_t* zq, const float* zs, const int32_t* counts, int E, int R,
+                         int H, int I, const uint8_t* w2, const float* w2_scale, void* out,
+                         int32_t* dev_status, moe_stream_t stream) {
+  if (!valid_experts(E, R) || !valid_hidden(H) || !valid_hidden(I)) return MOE_ERR_INVALID_ARG;
+  if (zq == nullptr || zs == nullptr || counts == nullptr || w2 == nullptr ||
+      w2_scale == nullptr || out == nullptr || dev_status == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(zq) || !aligned16(w2) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_gemm_down(zq, zs, counts, E, R, H, I, w2, w2_scale, out, dev_status,
+                                    dev->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_compute(const void* recv, const int32_t* counts, int E, int R, int H, int I,
+                              const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                              const float* w2_scale, void* out, int32_t* dev_status,
+                              void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (!valid_experts(E, R) || !valid_hidden(H) || !valid_hidden(I)) return MOE_ERR_INVALID_ARG;
+  if (recv == nullptr || counts == nullptr || w13 == nullptr || w13_scale == nullptr ||
+      w2 == nullptr || w2_scale == nullptr || out == nullptr || dev_status == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(recv) || !aligned16(w13) || !aligned16(w2) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  const ComputeWorkspace w = compute_workspace(E, R, H, I);
+  if (workspace == nullptr || workspace_bytes < w.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  auto* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* xq = ws + w.xq;
+  float* xs = reinterpret_cast<float*>(ws + w.xs);
+  uint8_t* zq = ws + w.zq;
+  float* zs = reinterpret_cast<float*>(ws + w.zs);
+  auto s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err = launch_quantize(recv, counts, E, R, H, xq, xs, dev->sm_count, s);
+  if (err == cudaSuccess)
+    err = launch_gemm_gateup(xq, xs, counts, E, R, H, I, w13, w13_scale, zq, zs, dev_status,
+                             dev->sm_count, s);
+  if (err == cudaSuccess)
+    err = launch_gemm_down(zq, zs, counts, E, R, H, I, w2, w2_scale, out, dev_status,
+                           dev->sm_count, s);
+  return from_cuda(err);
+}
+
+moe_status moe_combine(const void* out, const int32_t* src_map, const float* topk_w, int T, int H,
+                       int K, int E, int R, void* y, moe_stream_t stream) {
+  if (T < 0 || !valid_hidden(H) || !valid_experts(E, R) || K < 1 || K > 32 || K > E)
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (out == nullptr || src_map == nullptr || topk_w == nullptr || y == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(out) || !aligned16(y))) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_combine(out, src_map, topk_w, T, H, K, static_cast<int64_t>(E) * R, y,
+                                  dev->sm_count,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

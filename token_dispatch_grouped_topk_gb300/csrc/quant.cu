@@ -1,0 +1,107 @@
+// Per-token FP8 quantisation of the valid receive rows.
+//
+// "SGLang、NCCL 与 MoE EP", §2.3.5: after receive, the valid rows of recv
+// [L, M, H] are quantised to FP8 with one fp32 scale per row per 128 hidden
+// elements; rows past counts[e] are never touched.  The rule is the one of
+// "DeepEP 架构与实现笔记", §11: amax = max(max|v|, 1e-4), codes =
+// e4m3(v * (448 / amax)), scale = amax / 448, computed here in fp32 with IEEE
+// division and a round-to-nearest-even, saturating e4m3 conversion.
+//
+// Work is split into row blocks of 32 valid rows of one expert.  A persistent
+// grid walks the row blocks; each warp takes whole rows, each half-warp one
+// 128-element group (16 lanes x 8 BF16 = one 16-byte load per lane), so the
+// group amax is a 4-step shuffle reduction.  Scales are staged in shared
+// memory and written group-major ([E, H/128, R]) as 128-byte runs.
+#include "common.cuh"
+#include "kernels.h"
+
+#include <algorithm>
+
+namespace moe {
+namespace {
+
+constexpr int kQuantWarps = 8;
+constexpr int kRowsPerBlock = 32;
+
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    quantize_kernel(const uint4* __restrict__ recv, const int32_t* __restrict__ counts, int E,
+                    int R, int H, uint2* __restrict__ xq, float* __restrict__ xs) {
+  extern __shared__ int smem[];
+  int* s_start = smem;               // [E + 1] prefix of row blocks
+  int* s_cnt = smem + E + 1;         // [E]
+  float* s_scale = reinterpret_cast<float*>(smem + 2 * E + 1);  // [G][32]
+  expert_prefix(counts, E, R, kRowsPerBlock, 1, s_start, s_cnt);
+  const int G = H / kGroup;
+  const int nvec = H / 8;
+  const int total = s_start[E];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
+  for (int b = blockIdx.x; b < total; b += gridDim.x) {
+    const int e = find_expert(s_start, E, b);
+    const int row0 = (b - s_start[e]) * kRowsPerBlock;
+    const int nrows = min(kRowsPerBlock, s_cnt[e] - row0);
+    for (int r = warp; r < nrows; r += kQuantWarps) {
+      const size_t row = static_cast<size_t>(e) * R + row0 + r;
+      const uint4* src = recv + row * nvec;
+      uint2* dst = xq + row * (H / 8);
+      for (int g0 = 0; g0 < G; g0 += 2) {
+        const int g = g0 + half;
+        const bool on = g < G;
+        float f[8];
+        float amax = 0.f;
+        if (on) {
+          const uint4 v = ld_stream(src + g * 16 + hl);
+          bf16x8_to_f32(v, f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        }
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (on) {
+          float mult, scale;
+          fp8_group_scale(amax, &mult, &scale);
+          uint32_t lo = 0, hi = 0;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            lo |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[2 * i], mult),
+                                                    __fmul_rn(f[2 * i + 1], mult)))
+                  << (16 * i);
+            hi |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[4 + 2 * i], mult),
+                                                    __fmul_rn(f[5 + 2 * i], mult)))
+                  << (16 * i);
+          }
+          dst[g * 16 + hl] = make_uint2(lo, hi);
+          if (hl == 0) s_scale[g * kRowsPerBlock + r] = scale;
+        }
+      }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < G * kRowsPerBlock; i += blockDim.x) {
+      const int g = i / kRowsPerBlock, r = i % kRowsPerBlock;
+      if (r < nrows) xs[(static_cast<size_t>(e) * G + g) * R + row0 + r] = s_scale[i];
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, int R, int H,
+                            uint8_t* xq, float* xs, int sm_count, cudaStream_t s) {
+  const int G = H / kGroup;
+  const size_t smem = (2 * E + 1) * sizeof(int) + G * kRowsPerBlock * sizeof(float);
+  // Upper bound of row blocks; the kernel walks the true count read from device memory.
+  const long long max_blocks = static_cast<long long>(E) * ((R + kRowsPerBlock - 1) / kRowsPerBlock);
+  const int grid = static_cast<int>(std::min<long long>(max_blocks, sm_count * 8LL));
+  if (grid <= 0) return cudaSuccess;
+  if (smem > 48 * 1024) {
+    cudaError_t err = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+  }
+  quantize_kernel<<<grid, kQuantWarps * 32, smem, s>>>(static_cast<const uint4*>(recv), counts, E, R,
+                                                        H, reinterpret_cast<uint2*>(xq), xs);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
