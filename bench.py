@@ -113,7 +113,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -399,7 +399,7 @@ def workload_config(wl, extra=None) -> dict:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large", choices=["large", "prefill", "decode", "traced"])
@@ -429,7 +429,7 @@ def main():
             "kernels": res["kernels"], "roofline": res["roofline"], "e2e": res["e2e"],
             "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
         }
-        sample = cpu_oracle_sample(wl, n_experts=4, rows_per_expert=64)
+        sample = cpu_oracle_sample(wl, n_experts=8, rows_per_expert=128)
         line["cpu_baseline"] = {"value": sample["value"], "unit": UNIT, "cores": sample["cores"],
                                 "kind": "oracle", "sample": sample["sample"]}
         print(json.dumps(line), flush=True)

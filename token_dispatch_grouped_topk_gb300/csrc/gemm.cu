@@ -22,9 +22,16 @@
 //  - warp 2 owns the TMEM allocation;
 //  - warps 4-11 promote each K group's partial product: acc += sx * sw * P in
 //    registers (the fp32 scales are not of a form the hardware block-scaled
-//    MMA accepts), then run the fused epilogue: SiLU(gate) * up and the
-//    per-row FP8 requantisation of Z for the gate/up GEMM, BF16 rows for the
-//    down GEMM.  Only rows below counts[e] are stored.
+//    MMA accepts).  Warp w reads TMEM lanes 32*(w%4).. (its lane quarter) and
+//    one half of the tile's columns: 128 accumulators per thread, filled by
+//    64-column TMEM loads and updated with packed two-lane fp32 FMAs.  The
+//    register file is re-split per warpgroup (setmaxnreg): the producer/MMA
+//    warpgroup drops to 40 (24) registers, the two epilogue warpgroups rise to
+//    232 (240) in the gate/up (down) GEMM.
+//    After the last K group they run the fused epilogue: SiLU(gate) * up and
+//    the per-row FP8 requantisation of Z for the gate/up GEMM; for the down
+//    GEMM BF16 rows staged through shared memory so each store instruction
+//    writes 64-byte row segments.  Only rows below counts[e] are stored.
 // Every wait is bounded; on expiry the kernel raises MOE_DEV_TIMEOUT in the
 // status word, drains its own copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -40,9 +47,25 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 128;
 constexpr int kStages = 4;
-constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
-constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+// Register split: launched at kLaunchRegs per thread (the __launch_bounds__
+// maximum for 384 threads); warpgroup 0 gives back to CtrlRegs, warpgroups 1-2
+// take EpiRegs, with 4*32*CtrlRegs + 8*32*EpiRegs == 12*32*kLaunchRegs.  The
+// down GEMM's epilogue holds more live state, so it takes a larger share.
+constexpr int kLaunchRegs = 168;
+template <bool kGateUp>
+struct RegSplit {
+  static constexpr int kCtrl = kGateUp ? 40 : 24;
+  static constexpr int kEpi = kGateUp ? 232 : 240;
+  static_assert(4 * kCtrl + 8 * kEpi == 12 * kLaunchRegs, "register split must fit the launch");
+};
+// Down-GEMM output staging: per epilogue warp 32 rows x 32 BF16 columns, rows
+// padded to 80 bytes.
+constexpr int kStageRowBytes = 80;
+constexpr int kStageWarpBytes = 32 * kStageRowBytes;
 constexpr int kMaxExperts = 1024;
 
 struct GemmArgs {
@@ -71,13 +94,15 @@ struct Control {
   float amax[2][2][kBM];  // [tile parity][column half][row]
 };
 
-template <int BN>
+template <int BN, bool kGateUp>
 struct Layout {
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr size_t kSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Control);
+  static constexpr int kOutStage = kGateUp ? 0 : kEpiWarps * kStageWarpBytes;
+  static constexpr size_t kSmem =
+      1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Control) + kOutStage;
 };
 
 struct Tile {
@@ -105,11 +130,12 @@ template <int BN, bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
-  using L = Layout<BN>;
+  using L = Layout<BN, kGateUp>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   Control* ctl = reinterpret_cast<Control*>(smem + kStages * L::kStageBytes);
+  uint8_t* out_stage = smem + kStages * L::kStageBytes + sizeof(Control);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -146,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    warpgroup_reg_dealloc<RegSplit<kGateUp>::kCtrl>();
     if (lane == 0) {
       int issued = 0;
       bool ok = true;
@@ -185,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
+    warpgroup_reg_dealloc<RegSplit<kGateUp>::kCtrl>();
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
       int consumed = 0, kcount = 0;
@@ -220,12 +248,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(&ctl->drain, 0);
       }
     }
-  } else if (warp >= kEpiWarp0) {
+  } else if (warp < kEpiWarp0) {
+    warpgroup_reg_dealloc<RegSplit<kGateUp>::kCtrl>();   // warps 2-3: TMEM owner and spare
+  } else {
     // ------------------------------------------------------------ epilogue
-    constexpr int kCols = BN / 2;  // columns of the tile this thread owns
+    warpgroup_reg_alloc<RegSplit<kGateUp>::kEpi>();
+    constexpr int kCols = BN / 2;   // columns of the tile this thread owns
+    constexpr int kPairs = kCols / 2;
     const int ew = warp - kEpiWarp0;
-    const int lq = warp & 3;       // TMEM lane quarter accessible to this warp
-    const int ch = ew >> 2;        // which half of the tile's columns
+    const int lq = warp & 3;        // TMEM lane quarter accessible to this warp
+    const int ch = ew >> 2;         // which half of the tile's columns
     const int row = lq * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(lq * 32) << 16);
     int kcount = 0, iter = 0;
@@ -235,6 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = tl.m_blk * kBM + row;
       const bool in_cap = m < args.R;
       const float* asc = args.a_scale + static_cast<size_t>(tl.e) * nkb * args.R + m;
+      // gate/up: gate columns [64ch, 64ch+64) and up columns [128+64ch, ..+64);
+      // down:    columns [kCols*ch, kCols*ch + kCols), inside one 128-column
+      //          weight-scale block.
       const float* wsc0;
       const float* wsc1;
       if (kGateUp) {
@@ -247,15 +282,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         wsc0 = args.w_scale + (static_cast<size_t>(tl.e) * nb + cb) * nkb;
         wsc1 = wsc0;
       }
-      float accv[kCols];
+      uint64_t acc2[kPairs];
 #pragma unroll
-      for (int i = 0; i < kCols; ++i) accv[i] = 0.f;
-      float sa_next = in_cap ? __ldg(asc) : 0.f;
+      for (int i = 0; i < kPairs; ++i) acc2[i] = 0;
+      // Scales of K groups kb+1 and kb+2 are in flight while group kb is promoted.
+      float sa1 = in_cap ? __ldg(asc) : 0.f;
+      float w01 = __ldg(wsc0), w11 = __ldg(wsc1);
+      float sa2 = 0.f, w02 = 0.f, w12 = 0.f;
+      if (nkb > 1) {
+        sa2 = in_cap ? __ldg(asc + args.R) : 0.f;
+        w02 = __ldg(wsc0 + 1);
+        w12 = __ldg(wsc1 + 1);
+      }
       for (int kb = 0; kb < nkb; ++kb) {
-        const float sa = sa_next;
-        if (kb + 1 < nkb) sa_next = in_cap ? __ldg(asc + static_cast<size_t>(kb + 1) * args.R) : 0.f;
-        const float s0 = sa * __ldg(wsc0 + kb);
-        const float s1 = kGateUp ? sa * __ldg(wsc1 + kb) : s0;
+        const float s0 = sa1 * w01;
+        const float s1 = sa1 * w11;
+        sa1 = sa2;
+        w01 = w02;
+        w11 = w12;
+        if (kb + 2 < nkb) {
+          sa2 = in_cap ? __ldg(asc + static_cast<size_t>(kb + 2) * args.R) : 0.f;
+          w02 = __ldg(wsc0 + kb + 2);
+          w12 = __ldg(wsc1 + kb + 2);
+        }
         const int acc = kcount & 1;
         const uint32_t acc_phase = (kcount >> 1) & 1;
         if (!mbar_wait(&ctl->tfull[acc], acc_phase, abort_flag)) {
@@ -264,28 +313,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t base = t_lane + static_cast<uint32_t>(acc * BN);
-        float buf[32];
-        if (kGateUp) {
+        const uint64_t s0x2 = f32x2_pack(s0, s0);
+        const uint64_t s1x2 = f32x2_pack(s1, s1);
+        // Chunk j of 32 columns: gate/up j = 0, 1 gate and 2, 3 up; down j =
+        // 0.. kCols/32-1.  Load j+1 is in flight while chunk j is promoted.
+        auto chunk_col = [&](int j) -> uint32_t {
+          return kGateUp ? static_cast<uint32_t>((j >= 2 ? 128 : 0) + ch * 64 + 32 * (j & 1))
+                         : static_cast<uint32_t>(ch * kCols + 32 * j);
+        };
+        uint32_t bufa[32], bufb[32];
+        tmem_load32_issue(base + chunk_col(0), bufa);
+        tmem_load_wait(bufa);
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            tmem_load32_sync(base + ch * 64 + 32 * j, buf);
+        for (int j = 0; j < kCols / 32; ++j) {
+          uint32_t* cur = (j & 1) ? bufb : bufa;
+          uint32_t* nxt = (j & 1) ? bufa : bufb;
+          if (j + 1 < kCols / 32) tmem_load32_issue(base + chunk_col(j + 1), nxt);
+          const uint64_t sx2 = (kGateUp && j >= 2) ? s1x2 : s0x2;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) accv[32 * j + i] = fmaf(s0, buf[i], accv[32 * j + i]);
-          }
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            tmem_load32_sync(base + 128 + ch * 64 + 32 * j, buf);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              accv[64 + 32 * j + i] = fmaf(s1, buf[i], accv[64 + 32 * j + i]);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < kCols / 32; ++j) {
-            tmem_load32_sync(base + ch * kCols + 32 * j, buf);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) accv[32 * j + i] = fmaf(s0, buf[i], accv[32 * j + i]);
-          }
+          for (int i = 0; i < 16; ++i) ffma2_acc(acc2[16 * j + i], sx2, cur[2 * i], cur[2 * i + 1]);
+          if (j + 1 < kCols / 32) tmem_load_wait(nxt);
         }
         tc_fence_before();
         __syncwarp();
@@ -295,15 +342,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const bool valid = row < tl.rows;
       if (kGateUp) {
-        // Z = SiLU(gate) * up for this thread's 64 columns, then the row amax
-        // over the 128 columns shared with the partner warp (other half).
+        // Z = SiLU(gate) * up on this thread's 64 columns (written over the
+        // gate half of acc2), then the row amax over the tile's 128 Z columns
+        // shared with the partner warp holding the other half.
         float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float g = accv[i];
-          const float z = (g / (1.0f + expf(-g))) * accv[64 + i];
-          accv[i] = z;
-          amax = fmaxf(amax, fabsf(z));
+        for (int i = 0; i < 32; ++i) {
+          const float g0 = f32x2_lo(acc2[i]), g1 = f32x2_hi(acc2[i]);
+          const float u0 = f32x2_lo(acc2[32 + i]), u1 = f32x2_hi(acc2[32 + i]);
+          const float z0 = (g0 / (1.0f + expf(-g0))) * u0;
+          const float z1 = (g1 / (1.0f + expf(-g1))) * u1;
+          acc2[i] = f32x2_pack(z0, z1);
+          amax = fmaxf(amax, fmaxf(fabsf(z0), fabsf(z1)));
         }
         const int par = iter & 1;
         ctl->amax[par][ch][row] = amax;
@@ -323,10 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const int c = 16 * j + 4 * i;
-              w[i] = static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(accv[c], mult), __fmul_rn(accv[c + 1], mult))) |
-                     (static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(accv[c + 2], mult),
-                                                        __fmul_rn(accv[c + 3], mult)))
+              const uint64_t za = acc2[8 * j + 2 * i], zb = acc2[8 * j + 2 * i + 1];
+              w[i] = static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f32x2_lo(za), mult),
+                                                       __fmul_rn(f32x2_hi(za), mult))) |
+                     (static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f32x2_lo(zb), mult),
+                                                        __fmul_rn(f32x2_hi(zb), mult)))
                       << 16);
             }
             dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -334,17 +385,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ch == 0)
             args.zs[(static_cast<size_t>(tl.e) * (args.I / 128) + tl.n_blk) * args.R + m] = scale;
         }
-      } else if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(
-            args.out + (static_cast<size_t>(tl.e) * args.R + m) * args.H + tl.n_blk * BN + ch * kCols);
+      } else {
+        // BF16 rows through a per-warp shared-memory stage: each round the
+        // 32 threads deposit 32 columns of their rows, then the warp writes
+        // 8 rows x 64 bytes per store instruction.
+        uint8_t* stage = out_stage + ew * kStageWarpBytes;
+        const int row0 = tl.m_blk * kBM + lq * 32;             // first row of this warp
+        const int nvalid = min(32, ctl->cnt[tl.e] - row0);     // rows of this warp to store
+        __nv_bfloat16* gbase = args.out + (static_cast<size_t>(tl.e) * args.R + row0) * args.H +
+                               tl.n_blk * BN + ch * kCols;
+        // lane -> (row 8i + lane/4, 16-byte chunk lane%4) of each store instruction i
+        const int c = lane & 3;
+        const uint32_t goff = static_cast<uint32_t>((lane >> 2) * args.H + 8 * c);
+        const uint32_t sidx = static_cast<uint32_t>((lane >> 2) * kStageRowBytes + 16 * c);
+        const uint32_t gstep = static_cast<uint32_t>(8 * args.H);
 #pragma unroll
-        for (int j = 0; j < kCols / 8; ++j) {
-          uint4 o;
-          o.x = pack_bf16x2_rn(accv[8 * j + 0], accv[8 * j + 1]);
-          o.y = pack_bf16x2_rn(accv[8 * j + 2], accv[8 * j + 3]);
-          o.z = pack_bf16x2_rn(accv[8 * j + 4], accv[8 * j + 5]);
-          o.w = pack_bf16x2_rn(accv[8 * j + 6], accv[8 * j + 7]);
-          dst[j] = o;
+        for (int r = 0; r < kCols / 32; ++r) {
+          uint4* srow = reinterpret_cast<uint4*>(stage + lane * kStageRowBytes);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int p = 16 * r + 4 * j;
+            uint4 o;
+            o.x = pack_bf16x2_rn(f32x2_lo(acc2[p + 0]), f32x2_hi(acc2[p + 0]));
+            o.y = pack_bf16x2_rn(f32x2_lo(acc2[p + 1]), f32x2_hi(acc2[p + 1]));
+            o.z = pack_bf16x2_rn(f32x2_lo(acc2[p + 2]), f32x2_hi(acc2[p + 2]));
+            o.w = pack_bf16x2_rn(f32x2_lo(acc2[p + 3]), f32x2_hi(acc2[p + 3]));
+            srow[j] = o;
+          }
+          __syncwarp();
+#pragma unroll 1
+          for (int i = 0; i < 4; ++i) {
+            if (8 * i + (lane >> 2) < nvalid) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stage + sidx + i * 8 * kStageRowBytes);
+              *reinterpret_cast<uint4*>(gbase + goff + i * gstep + 32 * r) = v;
+            }
+          }
+          __syncwarp();
         }
       }
     }
@@ -397,7 +473,17 @@ cudaError_t make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_
 template <int BN, bool kGateUp>
 cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
                         int sm_count, cudaStream_t s) {
-  using L = Layout<BN>;
+  using L = Layout<BN, kGateUp>;
+  // The setmaxnreg split assumes the kernel was compiled to exactly
+  // kLaunchRegs registers per thread; any other count could leave the
+  // epilogue's register increase waiting forever, so refuse to launch.
+  static const int compiled_regs = [] {
+    cudaFuncAttributes attr{};
+    return cudaFuncGetAttributes(&attr, grouped_gemm_kernel<BN, kGateUp>) == cudaSuccess
+               ? attr.numRegs
+               : -1;
+  }();
+  if (compiled_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   const long long ub = static_cast<long long>(a.E) * ((a.R + kBM - 1) / kBM) * a.n_tiles;
   const int grid = static_cast<int>(std::min<long long>(ub, sm_count));
   if (grid <= 0) return cudaSuccess;
