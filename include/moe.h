@@ -98,6 +98,30 @@ moe_status moe_dispatch(const void* x, const int64_t* topk_idx, const float* top
                         moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_dispatch_noalloc -- the pages have no counterpart; this is a convenience
+ * of this library.  The same dispatch as moe_dispatch, for callers that cannot
+ * allocate device memory: code running while a CUDA graph is captured (where
+ * cudaMalloc is not allowed), runtimes that forbid device allocation after
+ * start-up or hand this library no allocator, and latency-critical loops that
+ * cannot afford cudaMalloc's implicit device synchronisation.
+ *
+ * Arguments and outputs are those of moe_dispatch, minus the workspace: the
+ * scratch is a 1 MiB array inside the library (held by every GPU that loads
+ * the library until the process exits), which limits the problem to
+ * moe_dispatch_workspace_size(T, K, E) <= 1 MiB, i.e. E * ceil(T / (8*(32/K)))
+ * <= 262144; larger problems return MOE_ERR_WORKSPACE without launching.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array, and nothing in it needs to start
+ * at zero (each call writes every entry it reads); calls whose kernels overlap
+ * on the GPU (different streams without ordering) race on it and must not be
+ * issued.
+ * ------------------------------------------------------------------------- */
+moe_status moe_dispatch_noalloc(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
+                                int H, int K, int E, int R, void* recv, int32_t* counts,
+                                int32_t* src_map, int32_t* dev_status, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Expert compute -- per-token FP8 quantisation of the valid receive rows
  * ("SGLang、NCCL 与 MoE EP", §2.3.5; rule of "DeepEP 架构与实现笔记", §11), then
  * the gated-SiLU expert of "SGLang Expert Compute Backend", §1.1 and §3.5-3.7:
