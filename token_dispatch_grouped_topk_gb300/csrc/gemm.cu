@@ -24,7 +24,9 @@
 //    registers (the fp32 scales are not of a form the hardware block-scaled
 //    MMA accepts).  Warp w reads TMEM lanes 32*(w%4).. (its lane quarter) and
 //    one half of the tile's columns: 128 accumulators per thread, filled by
-//    64-column TMEM loads and updated with packed two-lane fp32 FMAs.  The
+//    64-column TMEM loads (a load takes ~150 clocks, so 8 KB per warp must be
+//    in flight for eight warps to drain 128x256 fp32 per K group in time) and
+//    updated with packed two-lane fp32 FMAs.  The
 //    register file is re-split per warpgroup (setmaxnreg): the producer/MMA
 //    warpgroup drops to 40 (24) registers, the two epilogue warpgroups rise to
 //    232 (240) in the gate/up (down) GEMM.
@@ -315,24 +317,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t base = t_lane + static_cast<uint32_t>(acc * BN);
         const uint64_t s0x2 = f32x2_pack(s0, s0);
         const uint64_t s1x2 = f32x2_pack(s1, s1);
-        // Chunk j of 32 columns: gate/up j = 0, 1 gate and 2, 3 up; down j =
-        // 0.. kCols/32-1.  Load j+1 is in flight while chunk j is promoted.
-        auto chunk_col = [&](int j) -> uint32_t {
-          return kGateUp ? static_cast<uint32_t>((j >= 2 ? 128 : 0) + ch * 64 + 32 * (j & 1))
-                         : static_cast<uint32_t>(ch * kCols + 32 * j);
-        };
-        uint32_t bufa[32], bufb[32];
-        tmem_load32_issue(base + chunk_col(0), bufa);
-        tmem_load_wait(bufa);
+        // Chunk j of 64 columns (one TMEM load, 8 KB per warp in flight):
+        // gate/up j = 0 gate, j = 1 up; down j = 0 .. kCols/64-1.
+        uint32_t buf[64];
 #pragma unroll
-        for (int j = 0; j < kCols / 32; ++j) {
-          uint32_t* cur = (j & 1) ? bufb : bufa;
-          uint32_t* nxt = (j & 1) ? bufa : bufb;
-          if (j + 1 < kCols / 32) tmem_load32_issue(base + chunk_col(j + 1), nxt);
-          const uint64_t sx2 = (kGateUp && j >= 2) ? s1x2 : s0x2;
+        for (int j = 0; j < kCols / 64; ++j) {
+          const uint32_t col = kGateUp ? static_cast<uint32_t>((j ? 128 : 0) + ch * 64)
+                                       : static_cast<uint32_t>(ch * kCols + 64 * j);
+          const uint64_t sx2 = (kGateUp && j) ? s1x2 : s0x2;
+          tmem_load64_sync(base + col, buf);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) ffma2_acc(acc2[16 * j + i], sx2, cur[2 * i], cur[2 * i + 1]);
-          if (j + 1 < kCols / 32) tmem_load_wait(nxt);
+          for (int i = 0; i < 32; ++i) ffma2_acc(acc2[32 * j + i], sx2, buf[2 * i], buf[2 * i + 1]);
         }
         tc_fence_before();
         __syncwarp();
