@@ -247,11 +247,11 @@ def run_ours(args, rank, local, world):
     G, GI = H // 128, I // 128
     xq = ws[: E * R * H].view(E, R, H)
     off = (E * R * H + 255) // 256 * 256
-    xs = ws[off: off + E * G * R * 4].view(torch.float32).view(E, G, R)
+    xs = ws[off: off + E * G * R * 4].view(torch.float32).view(E, R, G)
     off = (off + E * G * R * 4 + 255) // 256 * 256
     zq = ws[off: off + E * R * I].view(E, R, I)
     off = (off + E * R * I + 255) // 256 * 256
-    zs = ws[off: off + E * GI * R * 4].view(torch.float32).view(E, GI, R)
+    zs = ws[off: off + E * GI * R * 4].view(torch.float32).view(E, R, GI)
     stream = torch.cuda.current_stream()
 
     n_valid, n_active = [], []

@@ -122,6 +122,25 @@ moe_status moe_dispatch_noalloc(const void* x, const int64_t* topk_idx, const fl
                                 int32_t* src_map, int32_t* dev_status, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_dispatch_quant -- dispatch fused with the per-token FP8 quantisation,
+ * the "quantise while packing" candidate of "SGLang Expert Compute Backend",
+ * §4.4.  Every kept route's row is written to the receive layout already as
+ * e4m3 codes plus fp32 scales; the BF16 receive buffer is never formed.  Each
+ * token row is quantised once (the rule of moe_quantize_fp8, which is per row,
+ * so all K copies are identical).  Outputs equal moe_quantize_fp8 applied to
+ * moe_dispatch's recv, bit for bit; counts, src_map and dev_status are those of
+ * moe_dispatch.  Feed xq/xs to moe_gemm_gateup_silu.
+ *
+ *   xq  device, e4m3 [E, R, H]       out: rows [0, counts[e]) written
+ *   xs  device, fp32 [E, R, H/128]   out: scales of those rows
+ *   other arguments and the workspace as for moe_dispatch
+ * ------------------------------------------------------------------------- */
+moe_status moe_dispatch_quant(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
+                              int H, int K, int E, int R, uint8_t* xq, float* xs, int32_t* counts,
+                              int32_t* src_map, int32_t* dev_status, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Expert compute -- per-token FP8 quantisation of the valid receive rows
  * ("SGLang、NCCL 与 MoE EP", §2.3.5; rule of "DeepEP 架构与实现笔记", §11), then
  * the gated-SiLU expert of "SGLang Expert Compute Backend", §1.1 and §3.5-3.7:
@@ -168,16 +187,15 @@ moe_status moe_combine(const void* out, const int32_t* src_map, const float* top
 
 /* ---------------------------------------------------------------------------
  * The three steps inside moe_expert_compute, exposed for testing and
- * profiling.  Scales are stored group-major, [E, G, R] (G = H/128 or I/128),
- * so the 128 row scales of one GEMM tile and K-group are contiguous; this is
- * the transpose of the pages' [E, R, G].
+ * profiling.  Scales are stored row-major per row, [E, R, G] (G = H/128 or
+ * I/128), the pages' layout.
  *
  * moe_quantize_fp8 -- "DeepEP 架构与实现笔记", §11: per valid row and 128-group,
  *   amax = max(max|v|, 1e-4); xq = e4m3_rn_satfinite(v * (448/amax)); xs = amax/448,
- *   all in fp32.  xq device e4m3 [E, R, H]; xs device fp32 [E, H/128, R].
+ *   all in fp32.  xq device e4m3 [E, R, H]; xs device fp32 [E, R, H/128].
  * moe_gemm_gateup_silu -- "SGLang Expert Compute Backend", §3.5-3.6: G from xq/xs
  *   and W13, Z = SiLU(G[:, :I]) * G[:, I:], quantised like moe_quantize_fp8.
- *   zq device e4m3 [E, R, I]; zs device fp32 [E, I/128, R].
+ *   zq device e4m3 [E, R, I]; zs device fp32 [E, R, I/128].
  * moe_gemm_down -- the same page, §3.6-3.7: out = block-scaled GEMM of zq/zs
  *   with W2, BF16 [E, R, H], rows [0, counts[e]) only.
  * Only rows < counts[e] are read or written in every step.

@@ -14,6 +14,7 @@ from . import _lib
 
 __all__ = [
     "MoeError", "dispatch_workspace_size", "expert_compute_workspace_size", "moe_dispatch",
+    "moe_dispatch_quant",
     "moe_expert_compute", "moe_combine", "moe_quantize_fp8", "moe_gemm_gateup_silu",
     "moe_gemm_down", "MoeLayerBuffers", "DEV_BAD_EXPERT_ID", "DEV_CAPACITY_DROPPED", "DEV_TIMEOUT",
 ]
@@ -83,6 +84,35 @@ def moe_dispatch(x, topk_idx, topk_w, E: int, R: int, *, recv=None, counts=None,
     return recv, counts, src_map, dev_status
 
 
+def moe_dispatch_quant(x, topk_idx, topk_w, E: int, R: int, *, xq=None, xs=None, counts=None,
+                       src_map=None, dev_status=None, workspace=None, stream=None):
+    """Dispatch fused with the per-token FP8 quantisation.  Returns
+    ``(xq [E,R,H] uint8, xs [E,R,H/128] fp32, counts, src_map, dev_status)``."""
+    lib = _lib.load()
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    dev = x.device
+    _need(x, torch.bfloat16, "x")
+    _need(topk_idx, torch.int64, "topk_idx")
+    if xq is None:
+        xq = torch.empty(E, R, H, dtype=torch.uint8, device=dev)
+    if xs is None:
+        xs = torch.empty(E, R, H // 128, dtype=torch.float32, device=dev)
+    if counts is None:
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+    if src_map is None:
+        src_map = torch.empty(T, K, dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(2, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _workspace(lib.moe_dispatch_workspace_size(T, K, E), dev)
+    st = lib.moe_dispatch_quant(_p(x), _p(topk_idx), _p(topk_w), T, H, K, E, R, _p(xq), _p(xs),
+                                _p(counts), _p(src_map), _p(dev_status), _p(workspace),
+                                workspace.numel(), _s(stream))
+    _lib.check("moe_dispatch_quant", st)
+    return xq, xs, counts, src_map, dev_status
+
+
 def moe_expert_compute(recv, counts, w13, w13_scale, w2, w2_scale, *, out=None, dev_status=None,
                        workspace=None, stream=None):
     """Quantise the valid rows and run the grouped gated-SiLU FP8 expert MLP.
@@ -119,13 +149,13 @@ def moe_combine(out, src_map, topk_w, *, y=None, stream=None):
 
 def moe_quantize_fp8(recv, counts, *, xq=None, xs=None, stream=None):
     """Per-token FP8 quantisation of the valid rows: ``xq [E,R,H] uint8`` (e4m3
-    codes) and ``xs [E,H/128,R] fp32``."""
+    codes) and ``xs [E,R,H/128] fp32``."""
     lib = _lib.load()
     E, R, H = recv.shape
     if xq is None:
         xq = torch.empty(E, R, H, dtype=torch.uint8, device=recv.device)
     if xs is None:
-        xs = torch.empty(E, H // 128, R, dtype=torch.float32, device=recv.device)
+        xs = torch.empty(E, R, H // 128, dtype=torch.float32, device=recv.device)
     st = lib.moe_quantize_fp8(_p(recv), _p(counts), E, R, H, _p(xq), _p(xs), _s(stream))
     _lib.check("moe_quantize_fp8", st)
     return xq, xs
@@ -133,7 +163,7 @@ def moe_quantize_fp8(recv, counts, *, xq=None, xs=None, stream=None):
 
 def moe_gemm_gateup_silu(xq, xs, counts, w13, w13_scale, *, zq=None, zs=None, dev_status=None,
                          stream=None):
-    """Gate/up GEMM + SiLU(gate)*up + FP8 requant: ``zq [E,R,I]``, ``zs [E,I/128,R]``."""
+    """Gate/up GEMM + SiLU(gate)*up + FP8 requant: ``zq [E,R,I]``, ``zs [E,R,I/128]``."""
     lib = _lib.load()
     E, R, H = xq.shape
     w13 = _u8(w13)
@@ -142,7 +172,7 @@ def moe_gemm_gateup_silu(xq, xs, counts, w13, w13_scale, *, zq=None, zs=None, de
     if zq is None:
         zq = torch.empty(E, R, I, dtype=torch.uint8, device=dev)
     if zs is None:
-        zs = torch.empty(E, I // 128, R, dtype=torch.float32, device=dev)
+        zs = torch.empty(E, R, I // 128, dtype=torch.float32, device=dev)
     if dev_status is None:
         dev_status = torch.zeros(2, dtype=torch.int32, device=dev)
     st = lib.moe_gemm_gateup_silu(_p(_u8(xq)), _p(xs), _p(counts), E, R, H, I, _p(w13),
@@ -194,6 +224,37 @@ class MoeLayerBuffers:
         self.y = torch.empty(T, H, dtype=torch.bfloat16, device=d)
         self.ws_dispatch = _workspace(dispatch_workspace_size(T, K, E), d)
         self.ws_compute = _workspace(expert_compute_workspace_size(E, R, H, I), d)
+
+    def workspace_views(self):
+        """(xq, xs, zq, zs): the FP8 activations and scales inside the expert
+        compute workspace, in the layout moe_expert_compute uses."""
+        E, R, H, I = self.E, self.R, self.H, self.I
+        G, GI = H // 128, I // 128
+        ws = self.ws_compute
+        al = lambda v: (v + 255) // 256 * 256
+        o1 = al(E * R * H)
+        o2 = al(o1 + E * R * G * 4)
+        o3 = al(o2 + E * R * I)
+        xq = ws[:E * R * H].view(E, R, H)
+        xs = ws[o1:o1 + E * R * G * 4].view(torch.float32).view(E, R, G)
+        zq = ws[o2:o2 + E * R * I].view(E, R, I)
+        zs = ws[o3:o3 + E * R * GI * 4].view(torch.float32).view(E, R, GI)
+        return xq, xs, zq, zs
+
+    def forward_fused(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None):
+        """The same layer with dispatch and quantisation fused (moe_dispatch_quant
+        -> gate/up GEMM -> down GEMM -> combine); the BF16 receive buffer is not
+        used.  Returns ``y`` (bit-identical to ``forward``)."""
+        xq, xs, zq, zs = self.workspace_views()
+        moe_dispatch_quant(x, topk_idx, topk_w, self.E, self.R, xq=xq, xs=xs, counts=self.counts,
+                           src_map=self.src_map, dev_status=self.dev_status,
+                           workspace=self.ws_dispatch, stream=stream)
+        moe_gemm_gateup_silu(xq, xs, self.counts, w13, w13_scale, zq=zq, zs=zs,
+                             dev_status=self.dev_status, stream=stream)
+        moe_gemm_down(zq, zs, self.counts, w2, w2_scale, out=self.out, dev_status=self.dev_status,
+                      stream=stream)
+        moe_combine(self.out, self.src_map, topk_w, y=self.y, stream=stream)
+        return self.y
 
     def forward(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None):
         """dispatch -> expert compute -> combine on one stream; returns ``y``."""

@@ -171,6 +171,110 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   }
 }
 
+// Dispatch fused with the per-token FP8 quantisation ("SGLang Expert Compute
+// Backend", §4.4: quantise while packing instead of materialising BF16 rows).
+// Every route of a token carries the same row, and the quantisation is per row
+// and per 128-group, so each token row is quantised once and its e4m3 codes and
+// fp32 scales are written to every kept destination row; the BF16 receive
+// buffer is never formed.  Rank derivation is the one of route_scatter_kernel.
+// Each block takes a slice of whole 128-groups of its tokens' rows.
+__global__ void __launch_bounds__(kDispatchWarps * 32)
+    route_scatter_fp8_kernel(const uint4* __restrict__ x, const int64_t* __restrict__ topk_idx,
+                             int T, int H, int K, int E, int R, int nblocks,
+                             const int32_t* __restrict__ base, uint2* __restrict__ xq,
+                             float* __restrict__ xs, int32_t* __restrict__ src_map,
+                             int groups_per_slice) {
+  extern __shared__ int smem[];
+  int* s_cnt = smem;                                               // [kDispatchWarps][E]
+  int* s_dest = smem + kDispatchWarps * E;                         // [kDispatchWarps][32]
+  float* s_sc = reinterpret_cast<float*>(s_dest + kDispatchWarps * 32);  // [warps][groups_per_slice]
+  for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = lane >> 4, hl = lane & 15;
+  const int gw = blockIdx.x * kDispatchWarps + warp;
+  const RouteLane r = load_route(topk_idx, T, K, E, gw, lane, nullptr);
+  const unsigned peers = __match_any_sync(0xffffffffu, r.e);
+  const int lane_rank = __popc(peers & ((1u << lane) - 1u));
+  if (r.e >= 0 && lane == __ffs(peers) - 1) s_cnt[warp * E + r.e] = __popc(peers);
+  __syncthreads();
+  int q = -1;
+  if (r.e >= 0) {
+    int sl = base[static_cast<size_t>(r.e) * nblocks + blockIdx.x] + lane_rank;
+    for (int w = 0; w < warp; ++w) sl += s_cnt[w * E + r.e];
+    if (sl < R) q = r.e * R + sl;
+  }
+  if (blockIdx.y == 0 && r.active) src_map[static_cast<int64_t>(r.t) * K + r.k] = q;
+  s_dest[warp * 32 + lane] = q;
+  __syncwarp();
+
+  const int tpw = 32 / K;
+  const int G = H / kGroup;
+  const int g0 = blockIdx.y * groups_per_slice;
+  const int g1 = min(G, g0 + groups_per_slice);
+  const int* wdest = s_dest + warp * 32;
+  float* wsc = s_sc + warp * groups_per_slice;
+  for (int tt = 0; tt < tpw; ++tt) {
+    const int t = gw * tpw + tt;
+    if (t >= T) break;
+    const int* dq = wdest + tt * K;
+    bool any = false;
+    for (int k = 0; k < K; ++k) any |= dq[k] >= 0;
+    if (!any) continue;
+    const uint4* src = x + static_cast<size_t>(t) * (H / 8);
+    // eight groups per pass: half-warp `half` takes groups gg + 2u + half
+    for (int gg = g0; gg < g1; gg += 8) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int g = gg + 2 * u + half;
+        if (g < g1) v[u] = ld_stream(src + g * 16 + hl);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int g = gg + 2 * u + half;
+        const bool on = g < g1;
+        float f[8];
+        float amax = 0.f;
+        if (on) {
+          bf16x8_to_f32(v[u], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        }
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (on) {
+          float mult, scale;
+          fp8_group_scale(amax, &mult, &scale);
+          uint32_t lo = 0, hi = 0;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            lo |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[2 * i], mult),
+                                                    __fmul_rn(f[2 * i + 1], mult)))
+                  << (16 * i);
+            hi |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[4 + 2 * i], mult),
+                                                    __fmul_rn(f[5 + 2 * i], mult)))
+                  << (16 * i);
+          }
+          const uint2 codes = make_uint2(lo, hi);
+          for (int k = 0; k < K; ++k) {
+            const int qq = dq[k];
+            if (qq >= 0) xq[static_cast<size_t>(qq) * (H / 8) + g * 16 + hl] = codes;
+          }
+          if (hl == 0) wsc[g - g0] = scale;
+        }
+      }
+    }
+    __syncwarp();
+    for (int k = 0; k < K; ++k) {
+      const int qq = dq[k];
+      if (qq < 0) continue;
+      for (int g = g0 + lane; g < g1; g += 32) xs[static_cast<size_t>(qq) * G + g] = wsc[g - g0];
+    }
+    __syncwarp();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
@@ -199,6 +303,39 @@ cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H
   route_scatter_kernel<<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
       static_cast<const uint4*>(x), topk_idx, T, H, K, E, R, nblocks, hist,
       static_cast<uint4*>(recv), src_map, vec_per_slice);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
+
+namespace moe {
+
+cudaError_t launch_dispatch_quant(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
+                                  int R, uint8_t* xq, float* xs, int32_t* counts, int32_t* src_map,
+                                  int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s) {
+  cudaError_t err = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
+  if (err != cudaSuccess) return err;
+  const int nblocks = dispatch_blocks(T, K);
+  if (nblocks > 0) {
+    route_hist_kernel<<<nblocks, kDispatchWarps * 32, E * sizeof(int), s>>>(topk_idx, T, K, E,
+                                                                            nblocks, hist, dev_status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  route_scan_kernel<<<E, kScanThreads, 0, s>>>(hist, nblocks, R, counts, dev_status);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (nblocks == 0) return cudaSuccess;
+  // Slices of whole 128-groups when there are too few tokens to fill the GPU.
+  const int G = H / kGroup;
+  const int target_warps = sm_count * 48;
+  int hsplit = (target_warps + nblocks * kDispatchWarps - 1) / (nblocks * kDispatchWarps);
+  hsplit = max(1, min(hsplit, G / 4));
+  const int gps = (G + hsplit - 1) / hsplit;
+  hsplit = (G + gps - 1) / gps;
+  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32) * sizeof(int) +
+                      kDispatchWarps * gps * sizeof(float);
+  route_scatter_fp8_kernel<<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
+      static_cast<const uint4*>(x), topk_idx, T, H, K, E, R, nblocks, hist,
+      reinterpret_cast<uint2*>(xq), xs, src_map, gps);
   return cudaGetLastError();
 }
 

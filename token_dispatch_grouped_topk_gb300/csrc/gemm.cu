@@ -72,12 +72,12 @@ constexpr int kMaxExperts = 1024;
 
 struct GemmArgs {
   const int32_t* counts;
-  const float* a_scale;  // [E, nkb, R]
+  const float* a_scale;  // [E, R, nkb], one row's scales contiguous
   const float* w_scale;  // [E, Ndim/128, nkb]
   int E, R, nkb, n_tiles;
   int I, H;
   uint8_t* zq;           // gate/up: [E, R, I]
-  float* zs;             // gate/up: [E, I/128, R]
+  float* zs;             // gate/up: [E, R, I/128]
   __nv_bfloat16* out;    // down: [E, R, H]
   int32_t* dev_status;
 };
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile tl = decode_tile(ctl, args.E, args.n_tiles, t);
       const int m = tl.m_blk * kBM + row;
       const bool in_cap = m < args.R;
-      const float* asc = args.a_scale + static_cast<size_t>(tl.e) * nkb * args.R + m;
+      const float* asc = args.a_scale + (static_cast<size_t>(tl.e) * args.R + m) * nkb;
       // gate/up: gate columns [64ch, 64ch+64) and up columns [128+64ch, ..+64);
       // down:    columns [kCols*ch, kCols*ch + kCols), inside one 128-column
       //          weight-scale block.
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float w01 = __ldg(wsc0), w11 = __ldg(wsc1);
       float sa2 = 0.f, w02 = 0.f, w12 = 0.f;
       if (nkb > 1) {
-        sa2 = in_cap ? __ldg(asc + args.R) : 0.f;
+        sa2 = in_cap ? __ldg(asc + 1) : 0.f;
         w02 = __ldg(wsc0 + 1);
         w12 = __ldg(wsc1 + 1);
       }
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         w01 = w02;
         w11 = w12;
         if (kb + 2 < nkb) {
-          sa2 = in_cap ? __ldg(asc + static_cast<size_t>(kb + 2) * args.R) : 0.f;
+          sa2 = in_cap ? __ldg(asc + kb + 2) : 0.f;
           w02 = __ldg(wsc0 + kb + 2);
           w12 = __ldg(wsc1 + kb + 2);
         }
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
           }
           if (ch == 0)
-            args.zs[(static_cast<size_t>(tl.e) * (args.I / 128) + tl.n_blk) * args.R + m] = scale;
+            args.zs[(static_cast<size_t>(tl.e) * args.R + m) * (args.I / 128) + tl.n_blk] = scale;
         }
       } else {
         // BF16 rows through a per-warp shared-memory stage: each round the

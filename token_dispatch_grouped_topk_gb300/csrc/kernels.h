@@ -29,7 +29,13 @@ cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H
                             int R, void* recv, int32_t* counts, int32_t* src_map,
                             int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s);
 
-// ----- per-token FP8 quantisation of the valid rows; xs is [E, H/128, R]
+// ----- dispatch fused with the per-token FP8 quantisation: xq [E, R, H]
+// e4m3 and xs [E, R, H/128] instead of the BF16 receive buffer
+cudaError_t launch_dispatch_quant(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
+                                  int R, uint8_t* xq, float* xs, int32_t* counts, int32_t* src_map,
+                                  int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s);
+
+// ----- per-token FP8 quantisation of the valid rows; xs is [E, R, H/128]
 cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, int R, int H,
                             uint8_t* xq, float* xs, int sm_count, cudaStream_t s);
 

@@ -126,6 +126,29 @@ moe_status moe_dispatch(const void* x, const int64_t* topk_idx, const float* top
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_dispatch_quant(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
+                              int H, int K, int E, int R, uint8_t* xq, float* xs, int32_t* counts,
+                              int32_t* src_map, int32_t* dev_status, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream) {
+  (void)topk_w;
+  if (T < 0 || !valid_hidden(H) || !valid_experts(E, R) || K < 1 || K > 32 || K > E)
+    return MOE_ERR_INVALID_ARG;
+  if (counts == nullptr || dev_status == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || topk_idx == nullptr || xq == nullptr || xs == nullptr ||
+                src_map == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(x) || (reinterpret_cast<uintptr_t>(xq) & 7u) != 0))
+    return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * K > (int64_t{1} << 31) - 1) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_dispatch_workspace_size(T, K, E);
+  if (workspace == nullptr || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_dispatch_quant(x, topk_idx, T, H, K, E, R, xq, xs, counts, src_map,
+                                         dev_status, static_cast<int32_t*>(workspace),
+                                         dev->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_expert_compute_workspace_size(int E, int R, int H, int I) {
   if (!valid_experts(E, R) || !valid_hidden(H) || !valid_hidden(I)) return 0;
   return compute_workspace(E, R, H, I).total;

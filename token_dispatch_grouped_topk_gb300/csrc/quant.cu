@@ -11,7 +11,8 @@
 // grid walks the row blocks; each warp takes whole rows, each half-warp one
 // 128-element group (16 lanes x 8 BF16 = one 16-byte load per lane), so the
 // group amax is a 4-step shuffle reduction.  Scales are staged in shared
-// memory and written group-major ([E, H/128, R]) as 128-byte runs.
+// memory and written row-major ([E, R, H/128], as on the pages), the block's
+// rows as one contiguous run.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -44,41 +45,52 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       const size_t row = static_cast<size_t>(e) * R + row0 + r;
       const uint4* src = recv + row * nvec;
       uint2* dst = xq + row * (H / 8);
-      for (int g0 = 0; g0 < G; g0 += 2) {
-        const int g = g0 + half;
-        const bool on = g < G;
-        float f[8];
-        float amax = 0.f;
-        if (on) {
-          const uint4 v = ld_stream(src + g * 16 + hl);
-          bf16x8_to_f32(v, f);
+      // Four pairs of groups per pass: every lane has four 16-byte loads in
+      // flight before the reductions.
+      for (int g0 = 0; g0 < G; g0 += 8) {
+        uint4 v[4];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        for (int u = 0; u < 4; ++u) {
+          const int g = g0 + 2 * u + half;
+          if (g < G) v[u] = ld_stream(src + g * 16 + hl);
         }
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (on) {
-          float mult, scale;
-          fp8_group_scale(amax, &mult, &scale);
-          uint32_t lo = 0, hi = 0;
+        for (int u = 0; u < 4; ++u) {
+          const int g = g0 + 2 * u + half;
+          const bool on = g < G;
+          float f[8];
+          float amax = 0.f;
+          if (on) {
+            bf16x8_to_f32(v[u], f);
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            lo |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[2 * i], mult),
-                                                    __fmul_rn(f[2 * i + 1], mult)))
-                  << (16 * i);
-            hi |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[4 + 2 * i], mult),
-                                                    __fmul_rn(f[5 + 2 * i], mult)))
-                  << (16 * i);
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
           }
-          dst[g * 16 + hl] = make_uint2(lo, hi);
-          if (hl == 0) s_scale[g * kRowsPerBlock + r] = scale;
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          if (on) {
+            float mult, scale;
+            fp8_group_scale(amax, &mult, &scale);
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              lo |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[2 * i], mult),
+                                                      __fmul_rn(f[2 * i + 1], mult)))
+                    << (16 * i);
+              hi |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[4 + 2 * i], mult),
+                                                      __fmul_rn(f[5 + 2 * i], mult)))
+                    << (16 * i);
+            }
+            dst[g * 16 + hl] = make_uint2(lo, hi);
+            if (hl == 0) s_scale[g * kRowsPerBlock + r] = scale;
+          }
         }
       }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < G * kRowsPerBlock; i += blockDim.x) {
-      const int g = i / kRowsPerBlock, r = i % kRowsPerBlock;
-      if (r < nrows) xs[(static_cast<size_t>(e) * G + g) * R + row0 + r] = s_scale[i];
+    // scales are stored [E, R, G]: the block's rows are one contiguous run
+    for (int i = threadIdx.x; i < G * nrows; i += blockDim.x) {
+      const int r = i / G, g = i % G;
+      xs[(static_cast<size_t>(e) * R + row0) * G + i] = s_scale[g * kRowsPerBlock + r];
     }
     __syncthreads();
   }
