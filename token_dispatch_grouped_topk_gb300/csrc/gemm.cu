@@ -131,6 +131,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 template <int BN, bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmA64,
+                        const __grid_constant__ CUtensorMap tmA32,
                         const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
   using L = Layout<BN, kGateUp>;
   extern __shared__ uint8_t smem_raw[];
@@ -156,6 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmA64);
+    tma_prefetch_desc(&tmA32);
     tma_prefetch_desc(&tmB);
   }
   if (warp == 2) {
@@ -198,8 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + stage * L::kStageBytes;
           uint8_t* sb = sa + L::kABytes;
-          mbar_arrive_expect_tx(&ctl->full[stage], L::kStageBytes);
-          tma_load_2d(sa, &tmA, &ctl->full[stage], kb * kBK, a_row);
+          // Only the tile's valid activation rows are fetched (32, 64 or 128):
+          // the rest of the A tile keeps stale bytes, which reach only output
+          // rows that are never stored.
+          const int a_box = tl.rows <= 32 ? 32 : (tl.rows <= 64 ? 64 : kBM);
+          mbar_arrive_expect_tx(&ctl->full[stage], L::kBBytes + a_box * kBK);
+          tma_load_2d(sa, a_box == kBM ? &tmA : (a_box == 64 ? &tmA64 : &tmA32), &ctl->full[stage],
+                      kb * kBK, a_row);
           tma_load_2d(sb, &tmB, &ctl->full[stage], kb * kBK, b_row0);
           if (BN == 256) tma_load_2d(sb + 128 * kBK, &tmB, &ctl->full[stage], kb * kBK, b_row1);
           ++issued;
@@ -450,14 +459,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2D map over a row-major byte matrix [rows, cols] with 128 x 128 boxes and
-// the 128-byte swizzle the MMA descriptors expect.
-cudaError_t make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+// 2D map over a row-major byte matrix [rows, cols] with boxes of 128 bytes x
+// box_rows and the 128-byte swizzle the MMA descriptors expect.
+cudaError_t make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                        uint32_t box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t box[2] = {128, box_rows};
   const cuuint32_t es[2] = {1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                          box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -465,8 +475,16 @@ cudaError_t make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Activation maps with 128-, 64- and 32-row boxes.
+cudaError_t make_activation_maps(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  cudaError_t err = make_map_u8(&m[0], base, cols, rows, kBM);
+  if (err == cudaSuccess) err = make_map_u8(&m[1], base, cols, rows, 64);
+  if (err == cudaSuccess) err = make_map_u8(&m[2], base, cols, rows, 32);
+  return err;
+}
+
 template <int BN, bool kGateUp>
-cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a,
+cudaError_t launch_impl(const CUtensorMap* ta, const CUtensorMap& tb, const GemmArgs& a,
                         int sm_count, cudaStream_t s) {
   using L = Layout<BN, kGateUp>;
   // The setmaxnreg split assumes the kernel was compiled to exactly
@@ -486,7 +504,7 @@ cudaError_t launch_impl(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::kSmem));
   if (err != cudaSuccess) return err;
-  grouped_gemm_kernel<BN, kGateUp><<<grid, kThreads, L::kSmem, s>>>(ta, tb, a);
+  grouped_gemm_kernel<BN, kGateUp><<<grid, kThreads, L::kSmem, s>>>(ta[0], ta[1], ta[2], tb, a);
   return cudaGetLastError();
 }
 
@@ -497,9 +515,9 @@ cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t
                                uint8_t* zq, float* zs, int32_t* dev_status, int sm_count,
                                cudaStream_t s) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
-  CUtensorMap ta, tb;
-  cudaError_t err = make_map_u8(&ta, xq, H, static_cast<uint64_t>(E) * R);
-  if (err == cudaSuccess) err = make_map_u8(&tb, w13, H, static_cast<uint64_t>(E) * 2 * I);
+  CUtensorMap ta[3], tb;
+  cudaError_t err = make_activation_maps(ta, xq, H, static_cast<uint64_t>(E) * R);
+  if (err == cudaSuccess) err = make_map_u8(&tb, w13, H, static_cast<uint64_t>(E) * 2 * I, kBM);
   if (err != cudaSuccess) return err;
   GemmArgs a{};
   a.counts = counts;
@@ -521,9 +539,9 @@ cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* 
                              int R, int H, int I, const uint8_t* w2, const float* w2_scale,
                              void* out, int32_t* dev_status, int sm_count, cudaStream_t s) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
-  CUtensorMap ta, tb;
-  cudaError_t err = make_map_u8(&ta, zq, I, static_cast<uint64_t>(E) * R);
-  if (err == cudaSuccess) err = make_map_u8(&tb, w2, I, static_cast<uint64_t>(E) * H);
+  CUtensorMap ta[3], tb;
+  cudaError_t err = make_activation_maps(ta, zq, I, static_cast<uint64_t>(E) * R);
+  if (err == cudaSuccess) err = make_map_u8(&tb, w2, I, static_cast<uint64_t>(E) * H, kBM);
   if (err != cudaSuccess) return err;
   GemmArgs a{};
   a.counts = counts;
