@@ -335,6 +335,29 @@ def run_ours(args, rank, local, world):
     rows_total = reduce_sum(rows_local, world, dev)
     value = rows_total / (max_ms / 1e3)
 
+    # ---- two micro-batches: serial split and overlapped on two streams
+    tbo = api.TwoBatchOverlap(wl.T, E, wl.K, H, I, R, dev)
+    tbo_steps = max(3, min(args.steps, 20))
+
+    def tbo_ms(overlap):
+        for i in range(args.warmup):
+            idx, w = routings[i % N_ROUTINGS]
+            tbo.forward(x, idx, w, w13, s13, w2, s2, overlap=overlap)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(tbo_steps):
+            idx, w = routings[(args.warmup + i) % N_ROUTINGS]
+            tbo.forward(x, idx, w, w13, s13, w2, s2, overlap=overlap)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / tbo_steps
+
+    split_serial_ms = tbo_ms(False)
+    split_overlap_ms = tbo_ms(True)
+    del tbo
+    torch.cuda.empty_cache()
+
     # ---- end to end through the public API with host buffers
     x_h = x.cpu().pin_memory()
     r_h = [(i.cpu().pin_memory(), w.cpu().pin_memory()) for i, w in routings]
@@ -390,6 +413,15 @@ def run_ours(args, rank, local, world):
         "combine": {"ms": stage_ms["combine"], "GB/s": gbs(acct["combine_bytes"], stage_ms["combine"]),
                     "frac_hbm": gbs(acct["combine_bytes"], stage_ms["combine"]) / peaks["hbm_gbs"]},
     }
+    mean_rows = rows_total / args.steps / world
+    tbo_res = {
+        "modes_ms_per_step": {"no_split": max_ms / args.steps, "serial_split": split_serial_ms,
+                              "overlapped_split": split_overlap_ms},
+        "rows_per_s": {"no_split": value, "serial_split": mean_rows / (split_serial_ms / 1e3),
+                       "overlapped_split": mean_rows / (split_overlap_ms / 1e3)},
+        "note": "two token halves, one buffer lane each; overlapped = B's dispatch beside A's expert "
+                "compute and B's expert compute beside A's combine on two streams",
+    }
     fused = {
         "value": rows_total / (fused_ms / 1e3), "unit": UNIT, "ms_per_step": fused_ms / args.steps,
         "note": "moe_dispatch_quant (each token row quantised once, FP8 scattered) replaces dispatch + quant",
@@ -419,7 +451,7 @@ def run_ours(args, rank, local, world):
         "value": value, "ms_per_step": max_ms / args.steps, "kernels": kernels, "roofline": roof,
         "e2e": {"value": e2e_rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps},
-        "gpu_launches": 7 * args.steps, "clocks": clk.summary(), "fused": fused,
+        "gpu_launches": 7 * args.steps, "clocks": clk.summary(), "fused": fused, "tbo": tbo_res,
         "rows_per_step": nv, "dropped_routes_last_routing": dropped, "wl": wl,
     }
 
@@ -466,6 +498,7 @@ def main():
             "kernels": res["kernels"], "roofline": res["roofline"], "e2e": res["e2e"],
             "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
             "fused_dispatch_quant": res["fused"],
+            "two_batch_overlap": res["tbo"],
         }
         sample = cpu_oracle_sample(wl, n_experts=8, rows_per_expert=128)
         line["cpu_baseline"] = {"value": sample["value"], "unit": UNIT, "cores": sample["cores"],

@@ -379,6 +379,29 @@ def test_layer_prefill_config_and_split():
     assert torch.equal(y_split[same].view(torch.int16), y[same].view(torch.int16))
 
 
+def test_two_batch_overlap_equals_serial_split():
+    """The overlapped two-micro-batch schedule (two lanes, two streams) writes
+    exactly what the serial split writes, and equals the unsplit layer on every
+    token whose routes are kept in both."""
+    d = W.make_layer_inputs("prefill", seed=4, device=DEV)
+    wl = d["wl"]
+    args = (d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
+    tbo = api.TwoBatchOverlap(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
+    y_serial = tbo.forward(*args, overlap=False).clone()
+    y_over = tbo.forward(*args, overlap=True).clone()
+    full = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
+    y_full = full.forward(*args)
+    torch.cuda.synchronize()
+    assert torch.equal(y_serial.view(torch.int16), y_over.view(torch.int16))
+    kept_full = ((full.src_map >= 0) | (d["topk_idx"] < 0)).all(1)
+    split_map = torch.cat([lane.src_map for lane in tbo.lanes])
+    kept_split = ((split_map >= 0) | (d["topk_idx"] < 0)).all(1)
+    same = kept_full & kept_split
+    assert torch.equal(y_over[same].view(torch.int16), y_full[same].view(torch.int16))
+    for lane in tbo.lanes:
+        assert lane.dev_status[0].item() & api.DEV_TIMEOUT == 0
+
+
 def test_layer_large_config_sampled():
     """Large layer (T=16384, E=256, H=7168, I=2048, R=4096, ~11 GB of FP8
     weights), in the launch configuration the benchmark times: dispatch

@@ -16,7 +16,8 @@ __all__ = [
     "MoeError", "dispatch_workspace_size", "expert_compute_workspace_size", "moe_dispatch",
     "moe_dispatch_quant",
     "moe_expert_compute", "moe_combine", "moe_quantize_fp8", "moe_gemm_gateup_silu",
-    "moe_gemm_down", "MoeLayerBuffers", "DEV_BAD_EXPERT_ID", "DEV_CAPACITY_DROPPED", "DEV_TIMEOUT",
+    "moe_gemm_down", "MoeLayerBuffers", "TwoBatchOverlap", "DEV_BAD_EXPERT_ID",
+    "DEV_CAPACITY_DROPPED", "DEV_TIMEOUT",
 ]
 
 MoeError = _lib.MoeError
@@ -264,4 +265,69 @@ class MoeLayerBuffers:
         moe_expert_compute(self.recv, self.counts, w13, w13_scale, w2, w2_scale, out=self.out,
                            dev_status=self.dev_status, workspace=self.ws_compute, stream=stream)
         moe_combine(self.out, self.src_map, topk_w, y=self.y, stream=stream)
+        return self.y
+
+
+class TwoBatchOverlap:
+    """A layer split into two micro-batches (token halves), each with its own
+    buffer lane, on two CUDA streams: micro-batch B's dispatch runs beside A's
+    expert compute and B's expert compute beside A's combine ("SGLang、NCCL 与
+    MoE EP", §2.4 and §5.4: two-batch overlap needs one resource set per
+    micro-batch; the overlap can at best hide min(D, S) of the two stages).
+    ``forward(..., overlap=False)`` runs the same two halves back to back on
+    one stream (the "serial split" of "SGLang Expert Compute Backend", §5.6).
+    Both produce the same bytes."""
+
+    def __init__(self, T: int, E: int, K: int, H: int, I: int, R: int, device):
+        self.half = T // 2
+        self.sizes = (self.half, T - self.half)
+        self.lanes = [MoeLayerBuffers(n, E, K, H, I, R, device) for n in self.sizes]
+        self.streams = [torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)]
+        self.y = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+        # each lane's combine writes straight into its half of y
+        self.lanes[0].y = self.y[: self.half]
+        self.lanes[1].y = self.y[self.half:]
+        self.ev = [torch.cuda.Event() for _ in range(2)]
+
+    def _views(self, x, topk_idx, topk_w):
+        h = self.half
+        return [(x[:h], topk_idx[:h], topk_w[:h]), (x[h:], topk_idx[h:], topk_w[h:])]
+
+    def _stage(self, lane, name, inp, weights, stream):
+        x, idx, w = inp
+        if name == "dispatch":
+            moe_dispatch(x, idx, w, lane.E, lane.R, recv=lane.recv, counts=lane.counts,
+                         src_map=lane.src_map, dev_status=lane.dev_status,
+                         workspace=lane.ws_dispatch, stream=stream)
+        elif name == "compute":
+            moe_expert_compute(lane.recv, lane.counts, *weights, out=lane.out,
+                               dev_status=lane.dev_status, workspace=lane.ws_compute, stream=stream)
+        else:
+            moe_combine(lane.out, lane.src_map, w, y=lane.y, stream=stream)
+
+    def forward(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, overlap: bool = True):
+        weights = (w13, w13_scale, w2, w2_scale)
+        views = self._views(x, topk_idx, topk_w)
+        cur = torch.cuda.current_stream()
+        a, b = self.lanes
+        if not overlap:
+            for lane, v in zip(self.lanes, views):
+                for name in ("dispatch", "compute", "combine"):
+                    self._stage(lane, name, v, weights, cur)
+        else:
+            sa, sb = self.streams
+            sa.wait_stream(cur)
+            sb.wait_stream(cur)
+            self._stage(a, "dispatch", views[0], weights, sa)
+            self.ev[0].record(sa)
+            self._stage(a, "compute", views[0], weights, sa)
+            self.ev[1].record(sa)
+            sb.wait_event(self.ev[0])            # B's dispatch beside A's expert compute
+            self._stage(b, "dispatch", views[1], weights, sb)
+            self._stage(a, "combine", views[0], weights, sa)
+            sb.wait_event(self.ev[1])            # B's expert compute beside A's combine
+            self._stage(b, "compute", views[1], weights, sb)
+            self._stage(b, "combine", views[1], weights, sb)
+            cur.wait_stream(sa)
+            cur.wait_stream(sb)
         return self.y
