@@ -209,6 +209,15 @@ moe_status moe_gemm_down(const uint8_t* zq, const float* zs, const int32_t* coun
                          int H, int I, const uint8_t* w2, const float* w2_scale, void* out,
                          int32_t* dev_status, moe_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * moe_selftest_bounded_wait -- exercises the device-side failure path: one
+ * thread runs the kernels' bounded mbarrier wait on a barrier that nothing
+ * completes; after the wait limit (about 2 s) it sets MOE_DEV_TIMEOUT in
+ * dev_status[0] and the kernel returns normally.  For tests of failure
+ * handling; no GPU fault is involved.
+ * ------------------------------------------------------------------------- */
+moe_status moe_selftest_bounded_wait(int32_t* dev_status, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,6 +17,7 @@ c_int, c_size_t, c_void_p, c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_vo
 # name -> (restype, argtypes), mirroring include/moe.h
 SIGNATURES = {
     "moe_abi_version": (c_int, []),
+    "moe_selftest_bounded_wait": (c_int, [c_void_p, c_void_p]),
     "moe_status_string": (c_char_p, [c_int]),
     "moe_dispatch_workspace_size": (c_size_t, [c_int, c_int, c_int]),
     "moe_dispatch": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
