@@ -223,6 +223,16 @@ def test_expert_compute_capacity_not_multiple_of_tile():
     _check_expert_compute(3, 200, 256, 128, [200, 199, 64], seed=6)
 
 
+@pytest.mark.parametrize("H", [512, 384])
+def test_expert_compute_narrow_tile_boundaries(H):
+    """Blocks of 1..64 valid rows run with swapped operands (weights on M,
+    tokens on N), 65..128 as wide tiles: both sides of each boundary, alone
+    and after full blocks, with 256-wide (H=512) and 128-wide (H=384) down
+    tiles."""
+    counts = [1, 31, 32, 33, 63, 64, 65, 127, 129, 192, 193, 256, 0]
+    _check_expert_compute(len(counts), 256, H, 256, counts, seed=11)
+
+
 # ------------------------------------------------------------------ combine
 
 def test_combine_bit_exact():

@@ -252,6 +252,13 @@ __device__ __forceinline__ void ffma2_acc(uint64_t& acc, uint64_t s2, uint32_t b
       : "l"(s2), "r"(b0), "r"(b1));
 }
 
+// Packed two-lane fp32 product, each lane rounded to nearest even.
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Named barrier over a subset of the block's warps.
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
