@@ -48,6 +48,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstddef>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -80,12 +81,15 @@ constexpr int kStageWarpBytes = 32 * kStageRowBytes;
 constexpr int kMaxExperts = 1024;
 // Tiles with at most this many valid rows take the swapped (narrow) form.
 constexpr int kNarrowRows = 64;
+// Experts per chunk of the tile walk (see decode_tile).
+constexpr int kExpertChunk = 8;
 
 struct GemmArgs {
   const int32_t* counts;
   const float* a_scale;  // [E, R, nkb], one row's scales contiguous
   const float* w_scale;  // [E, Ndim/128, nkb]
   int E, R, nkb, n_tiles;
+  int chunk;             // experts per chunk of the tile walk
   int I, H;
   uint8_t* zq;           // gate/up: [E, R, I]
   float* zs;             // gate/up: [E, R, I/128]
@@ -105,7 +109,11 @@ struct Control {
   int tile_start[kMaxExperts + 1];
   int cnt[kMaxExperts];
   float amax[2][2][kBM];  // [tile parity][column half][row]
+  // Narrow tiles: per epilogue warp, the K group's scale products of its 32
+  // tokens -- [0, 32) with the first half's weight scale, [32, 64) the second's.
+  alignas(16) float nscale[kEpiWarps][64];
 };
+static_assert(offsetof(Control, nscale) % 16 == 0, "narrow scale strips are read as float4");
 
 template <int BN, bool kGateUp>
 struct Layout {
@@ -122,13 +130,26 @@ struct Tile {
   int e, m_blk, n_blk, rows;
 };
 
-__device__ __forceinline__ Tile decode_tile(const Control* ctl, int E, int n_tiles, int t) {
+// Tile order: experts are taken in chunks of `chunk`; inside a chunk the walk
+// is N-slice major -- for each N slice, every M block of every expert of the
+// chunk -- so one weight slice's M blocks stay adjacent (they share it in L2)
+// while the tiles running at any moment mix lightly and heavily loaded
+// experts (weight-streaming and compute-heavy work), and a chunk's activation
+// rows stay in L2 across its N slices.  tile_start[e] = n_tiles * (M blocks
+// of experts < e), so a chunk's tiles occupy the same range as in an
+// expert-major walk.
+__device__ __forceinline__ Tile decode_tile(const Control* ctl, int E, int n_tiles, int chunk,
+                                            int t) {
   Tile r;
-  r.e = find_expert(ctl->tile_start, E, t);
-  const int local = t - ctl->tile_start[r.e];
-  const int mt = (ctl->tile_start[r.e + 1] - ctl->tile_start[r.e]) / n_tiles;
-  r.n_blk = local / mt;
-  r.m_blk = local - r.n_blk * mt;
+  const int c0 = (find_expert(ctl->tile_start, E, t) / chunk) * chunk;
+  const int c1 = min(c0 + chunk, E);
+  const int t0 = ctl->tile_start[c0];
+  const int nb = (ctl->tile_start[c1] - t0) / n_tiles;  // M blocks in the chunk
+  const int local = t - t0;
+  r.n_blk = local / nb;
+  const int b = t0 / n_tiles + (local - r.n_blk * nb);  // M block index over all experts
+  r.e = find_expert(ctl->tile_start, E, b * n_tiles);
+  r.m_blk = b - ctl->tile_start[r.e] / n_tiles;
   r.rows = min(kBM, ctl->cnt[r.e] - r.m_blk * kBM);
   return r;
 }
@@ -142,8 +163,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // Epilogue of a narrow tile.  TMEM lane = weight row within a 128-row half,
 // column = token; this thread owns weight row lq*32 + lane of every half and
 // tokens [32*ch, 32*ch + 32).  Each lane fetches the scale of one of those
-// tokens per K group and the warp broadcasts them with shuffles; the product
-// of token and weight scale is formed per lane exactly as in the wide tile.
+// tokens per K group and forms its products with the halves' weight scales
+// (the same fp32 product as in the wide tile); the warp stages them in shared
+// memory and reads them back as broadcasts.
 // Returns false when a wait expired.
 template <int BN, bool kGateUp>
 __device__ __forceinline__ bool narrow_epilogue(Control* ctl, const GemmArgs& args, const Tile& tl,
@@ -169,23 +191,34 @@ __device__ __forceinline__ bool narrow_epilogue(Control* ctl, const GemmArgs& ar
   uint64_t accA[16], accB[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) accA[i] = accB[i] = 0;
-  float x1 = tok_ok ? __ldg(asc) : 0.f, a1 = __ldg(wsA), b1 = __ldg(wsB);
-  float x2 = 0.f, a2 = 0.f, b2 = 0.f;
-  if (nkb > 1) {
-    x2 = tok_ok ? __ldg(asc + 1) : 0.f;
-    a2 = __ldg(wsA + 1);
-    b2 = __ldg(wsB + 1);
+  // Scales are fetched kPrefetch K groups ahead and rotate through registers,
+  // so no register copy waits on a load issued less than three groups ago.
+  constexpr int kPrefetch = 4;
+  float xr[kPrefetch], ar[kPrefetch], br[kPrefetch];
+#pragma unroll
+  for (int j = 0; j < kPrefetch; ++j) {
+    const bool in = j < nkb;
+    xr[j] = (in && tok_ok) ? __ldg(asc + j) : 0.f;
+    ar[j] = in ? __ldg(wsA + j) : 0.f;
+    br[j] = in ? __ldg(wsB + j) : 0.f;
   }
+  float* prod = ctl->nscale[ch * 4 + lq];
   for (int kb = 0; kb < nkb; ++kb) {
-    const float x = x1, wa = a1, wb = b1;
-    x1 = x2;
-    a1 = a2;
-    b1 = b2;
-    if (kb + 2 < nkb) {
-      x2 = tok_ok ? __ldg(asc + kb + 2) : 0.f;
-      a2 = __ldg(wsA + kb + 2);
-      b2 = __ldg(wsB + kb + 2);
+    const float x = xr[0], wa = ar[0], wb = br[0];
+#pragma unroll
+    for (int j = 0; j + 1 < kPrefetch; ++j) {
+      xr[j] = xr[j + 1];
+      ar[j] = ar[j + 1];
+      br[j] = br[j + 1];
     }
+    if (kb + kPrefetch < nkb) {
+      xr[kPrefetch - 1] = tok_ok ? __ldg(asc + kb + kPrefetch) : 0.f;
+      ar[kPrefetch - 1] = __ldg(wsA + kb + kPrefetch);
+      br[kPrefetch - 1] = __ldg(wsB + kb + kPrefetch);
+    }
+    // This lane's token: its scale times each half's weight scale.
+    prod[lane] = x * wa;
+    prod[32 + lane] = x * wb;
     const int acc = kcount & 1;
     const uint32_t acc_phase = (kcount >> 1) & 1;
     if (!mbar_wait(&ctl->tfull[acc], acc_phase, abort_flag)) return false;
@@ -201,14 +234,20 @@ __device__ __forceinline__ bool narrow_epilogue(Control* ctl, const GemmArgs& ar
     __syncwarp();
     if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
     ++kcount;
-    const uint64_t wa2 = f32x2_pack(wa, wa), wb2 = f32x2_pack(wb, wb);
+    // Token scale products come back as broadcasts, four tokens per load.
+    const float4* pg = reinterpret_cast<const float4*>(prod);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint64_t xs2 = f32x2_pack(__shfl_sync(0xffffffffu, x, 2 * i),
-                                      __shfl_sync(0xffffffffu, x, 2 * i + 1));
-      ffma2_acc(accA[i], fmul2(xs2, wa2), pa[2 * i], pa[2 * i + 1]);
-      if (kHalves == 2) ffma2_acc(accB[i], fmul2(xs2, wb2), pb[2 * i], pb[2 * i + 1]);
+    for (int q = 0; q < 8; ++q) {
+      const float4 g = pg[q];
+      ffma2_acc(accA[2 * q], f32x2_pack(g.x, g.y), pa[4 * q], pa[4 * q + 1]);
+      ffma2_acc(accA[2 * q + 1], f32x2_pack(g.z, g.w), pa[4 * q + 2], pa[4 * q + 3]);
+      if (kHalves == 2) {
+        const float4 u = pg[8 + q];
+        ffma2_acc(accB[2 * q], f32x2_pack(u.x, u.y), pb[4 * q], pb[4 * q + 1]);
+        ffma2_acc(accB[2 * q + 1], f32x2_pack(u.z, u.w), pb[4 * q + 2], pb[4 * q + 3]);
+      }
     }
+    __syncwarp();  // every lane has read this group's products before the next overwrite
   }
   const int nt = min(32, tl.rows - 32 * ch);  // valid tokens of this thread (may be <= 0)
   if (kGateUp) {
@@ -327,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile(ctl, args.E, args.n_tiles, t);
+        const Tile tl = decode_tile(ctl, args.E, args.n_tiles, args.chunk, t);
         const int a_row = tl.e * args.R + tl.m_blk * kBM;
         int b_row0, b_row1;
         if (kGateUp) {
@@ -374,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int consumed = 0, kcount = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const bool narrow = decode_tile(ctl, args.E, args.n_tiles, t).rows <= kNarrowRows;
+        const bool narrow = decode_tile(ctl, args.E, args.n_tiles, args.chunk, t).rows <= kNarrowRows;
         for (int kb = 0; kb < nkb; ++kb) {
           const int stage = consumed % kStages;
           const uint32_t phase = (consumed / kStages) & 1;
@@ -433,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kcount = 0, iter = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++iter) {
-      const Tile tl = decode_tile(ctl, args.E, args.n_tiles, t);
+      const Tile tl = decode_tile(ctl, args.E, args.n_tiles, args.chunk, t);
       if (tl.rows <= kNarrowRows) {
         ok = narrow_epilogue<BN, kGateUp>(ctl, args, tl, t_lane, lq, ch, lane, kcount, iter,
                                            abort_flag);
@@ -691,6 +730,7 @@ cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t
   a.R = R;
   a.nkb = H / kBK;
   a.n_tiles = I / 128;
+  a.chunk = kExpertChunk;
   a.I = I;
   a.H = H;
   a.zq = zq;
@@ -714,6 +754,7 @@ cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* 
   a.E = E;
   a.R = R;
   a.nkb = I / kBK;
+  a.chunk = kExpertChunk;
   a.I = I;
   a.H = H;
   a.out = static_cast<__nv_bfloat16*>(out);
