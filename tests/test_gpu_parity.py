@@ -234,9 +234,9 @@ def test_expert_compute_narrow_tile_boundaries(H):
 
 
 @pytest.mark.parametrize("H", [512, 384])
-def test_expert_compute_all_narrow_four_slots(H):
-    """No expert above 64 rows: every tile is narrow and the accumulator
-    memory is split into four slots; many K groups per CTA rotate through them."""
+def test_expert_compute_all_narrow(H):
+    """No expert above 64 rows: every tile is narrow, several per CTA, with
+    K groups rotating through both accumulator buffers."""
     counts = [1, 64, 33, 0, 17, 64, 2, 40, 63, 5, 64, 31]
     _check_expert_compute(len(counts), 64, H, 512, counts, seed=12)
 
