@@ -346,6 +346,36 @@ def test_layer_decode_config():
     assert_rows_close(f32(y)[toks], y_ref, what="decode y")
 
 
+def test_host_pipeline_matches_forward():
+    """api.HostPipeline (pinned host in/out, copies of neighbouring steps
+    overlapped with compute, two device slots) returns, for every step, the
+    bytes a plain forward on device inputs returns; five steps reuse each slot
+    at least twice, with a different routing per step."""
+    d = W.make_layer_inputs("decode", seed=0, device=DEV)
+    wl = d["wl"]
+    dev = torch.device(DEV)
+    buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
+    steps = []
+    for i in range(5):
+        idx, w = W.router(wl.T, wl.E, wl.K, W.router_bias(wl, 10 + i, "cpu"), 20 + i, "cpu")
+        x = W.activations(wl.T, wl.H, 30 + i, "cpu")
+        steps.append((x, idx, w))
+    want = []
+    for x, idx, w in steps:
+        y = buf.forward(x.to(dev), idx.to(dev), w.to(dev), d["w13"], d["s13"], d["w2"], d["s2"])
+        want.append(y.cpu())
+    pipe = api.HostPipeline(buf)
+    outs = [torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory() for _ in steps]
+    pinned = [(x.pin_memory(), idx.pin_memory(), w.pin_memory()) for x, idx, w in steps]
+    for (x, idx, w), y_h in zip(pinned, outs):
+        pipe.submit(x, idx, w, y_h, d["w13"], d["s13"], d["w2"], d["s2"])
+    pipe.synchronize()
+    for i, (got, ref) in enumerate(zip(outs, want)):
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), f"step {i}"
+    with pytest.raises(ValueError):
+        pipe.submit(steps[0][0], *pinned[0][1:], outs[0], d["w13"], d["s13"], d["w2"], d["s2"])
+
+
 def _sampled_out_check(d, buf, n_routes, seed):
     """Expert outputs of sampled kept routes, one by one against the oracle."""
     wl = d["wl"]

@@ -16,7 +16,7 @@ __all__ = [
     "MoeError", "dispatch_workspace_size", "expert_compute_workspace_size", "moe_dispatch",
     "moe_dispatch_quant",
     "moe_expert_compute", "moe_combine", "moe_quantize_fp8", "moe_gemm_gateup_silu",
-    "moe_gemm_down", "MoeLayerBuffers", "TwoBatchOverlap", "DEV_BAD_EXPERT_ID",
+    "moe_gemm_down", "MoeLayerBuffers", "HostPipeline", "TwoBatchOverlap", "DEV_BAD_EXPERT_ID",
     "DEV_CAPACITY_DROPPED", "DEV_TIMEOUT",
 ]
 
@@ -257,15 +257,75 @@ class MoeLayerBuffers:
         moe_combine(self.out, self.src_map, topk_w, y=self.y, stream=stream)
         return self.y
 
-    def forward(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None):
-        """dispatch -> expert compute -> combine on one stream; returns ``y``."""
+    def forward(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None, y=None):
+        """dispatch -> expert compute -> combine on one stream; returns ``y``
+        (the lane's own output buffer unless ``y`` [T, H] BF16 is given)."""
         moe_dispatch(x, topk_idx, topk_w, self.E, self.R, recv=self.recv, counts=self.counts,
                      src_map=self.src_map, dev_status=self.dev_status, workspace=self.ws_dispatch,
                      stream=stream)
         moe_expert_compute(self.recv, self.counts, w13, w13_scale, w2, w2_scale, out=self.out,
                            dev_status=self.dev_status, workspace=self.ws_compute, stream=stream)
-        moe_combine(self.out, self.src_map, topk_w, y=self.y, stream=stream)
-        return self.y
+        y = self.y if y is None else y
+        moe_combine(self.out, self.src_map, topk_w, y=y, stream=stream)
+        return y
+
+
+class HostPipeline:
+    """Layer invocations fed from pinned host memory and returned to it, with
+    the copies of neighbouring steps overlapped with compute: while step i
+    computes on the caller's stream, step i+1's inputs are copied in on one
+    copy stream and step i-1's output is copied out on another.  Inputs and
+    outputs have two device slots each; events order every reuse of a slot
+    (a slot is refilled only after the compute that read it, and an output
+    slot is rewritten only after its copy to the host).  The layer itself runs
+    on one buffer lane, in submission order.  Host tensors must be pinned and
+    must not be touched until ``synchronize()`` (or a later step's completion)
+    has returned."""
+
+    def __init__(self, lane: "MoeLayerBuffers"):
+        self.lane = lane
+        d, T, H, K = lane.device, lane.T, lane.H, lane.K
+        self.x = [torch.empty(T, H, dtype=torch.bfloat16, device=d) for _ in range(2)]
+        self.idx = [torch.empty(T, K, dtype=torch.int64, device=d) for _ in range(2)]
+        self.w = [torch.empty(T, K, dtype=torch.float32, device=d) for _ in range(2)]
+        self.y = [torch.empty(T, H, dtype=torch.bfloat16, device=d) for _ in range(2)]
+        self.s_in = torch.cuda.Stream(d)
+        self.s_out = torch.cuda.Stream(d)
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.in_ready, self.in_free, self.y_ready, self.y_free = ev(), ev(), ev(), ev()
+        self.n = 0
+
+    def submit(self, x_h, idx_h, w_h, y_h, w13, w13_scale, w2, w2_scale, stream=None):
+        """Queue one layer step: x_h [T, H] BF16, idx_h [T, K] int64 and w_h
+        [T, K] fp32 (pinned host) in, y_h [T, H] BF16 (pinned host) out."""
+        for t in (x_h, idx_h, w_h, y_h):
+            if t.is_cuda or not t.is_pinned():
+                raise ValueError("HostPipeline takes pinned host tensors")
+        k = self.n % 2
+        cs = stream if stream is not None else torch.cuda.current_stream(self.lane.device)
+        if self.n >= 2:
+            self.s_in.wait_event(self.in_free[k])
+        with torch.cuda.stream(self.s_in):
+            self.x[k].copy_(x_h, non_blocking=True)
+            self.idx[k].copy_(idx_h, non_blocking=True)
+            self.w[k].copy_(w_h, non_blocking=True)
+        self.in_ready[k].record(self.s_in)
+        cs.wait_event(self.in_ready[k])
+        if self.n >= 2:
+            cs.wait_event(self.y_free[k])
+        self.lane.forward(self.x[k], self.idx[k], self.w[k], w13, w13_scale, w2, w2_scale,
+                          stream=cs, y=self.y[k])
+        self.in_free[k].record(cs)
+        self.y_ready[k].record(cs)
+        self.s_out.wait_event(self.y_ready[k])
+        with torch.cuda.stream(self.s_out):
+            y_h.copy_(self.y[k], non_blocking=True)
+        self.y_free[k].record(self.s_out)
+        self.n += 1
+
+    def synchronize(self):
+        """Wait until every submitted step's output is in host memory."""
+        self.s_out.synchronize()
 
 
 class TwoBatchOverlap:

@@ -538,12 +538,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        : static_cast<uint32_t>(ch * kCols + 64 * j);
           const uint64_t sx2 = (kGateUp && j) ? s1x2 : s0x2;
           tmem_load64_sync(base + col, buf);
+          if (j == kCols / 64 - 1) {
+            // Last chunk is in registers: the buffer goes back to the MMA
+            // before its FMAs.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
+          }
 #pragma unroll
           for (int i = 0; i < 32; ++i) ffma2_acc(acc2[32 * j + i], sx2, buf[2 * i], buf[2 * i + 1]);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
         ++kcount;
       }
       if (!ok) break;
