@@ -42,18 +42,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// Potentially blocking test of a phase: the thread may be suspended until the
-// phase completes or the hinted time (ns) passes, which keeps waiting warps
-// from spinning through the issue slots.
-constexpr uint32_t kSuspendHintNs = 100000;
+// Potentially blocking test of a phase: the thread may wait for a short,
+// hardware-defined time before the test returns false.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendHintNs)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -250,13 +248,6 @@ __device__ __forceinline__ void ffma2_acc(uint64_t& acc, uint64_t s2, uint32_t b
   asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%2, %3};\n\tfma.rn.f32x2 %0, %1, t, %0;\n\t}"
       : "+l"(acc)
       : "l"(s2), "r"(b0), "r"(b1));
-}
-
-// Packed two-lane fp32 product, each lane rounded to nearest even.
-__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
 }
 
 // Named barrier over a subset of the block's warps.

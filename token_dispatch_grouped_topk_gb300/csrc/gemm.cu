@@ -34,21 +34,11 @@
 //    the per-row FP8 requantisation of Z for the gate/up GEMM; for the down
 //    GEMM BF16 rows staged through shared memory so each store instruction
 //    writes 64-byte row segments.  Only rows below counts[e] are stored.
-//  - a tile with at most 64 valid rows (an expert's remainder, or every tile
-//    of a lightly loaded expert) runs with the operands swapped: the 256
-//    weight rows of the B slot go on the MMA's M side as two M=128 halves and
-//    the tile's tokens (the 64-row activation box already in the A slot) on
-//    N=64.  The tensor work per K group halves and the epilogue reads 64 x 128
-//    accumulators instead of 128 x 256; token scales then vary along TMEM
-//    columns, so each lane fetches one token's scale and the warp broadcasts
-//    them with shuffles.  Z's per-token amax becomes a reduction across lanes
-//    (and the four lane-quarter warps), and outputs are stored column-wise.
 // Every wait is bounded; on expiry the kernel raises MOE_DEV_TIMEOUT in the
 // status word, drains its own copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <cstddef>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -79,17 +69,12 @@ struct RegSplit {
 constexpr int kStageRowBytes = 80;
 constexpr int kStageWarpBytes = 32 * kStageRowBytes;
 constexpr int kMaxExperts = 1024;
-// Tiles with at most this many valid rows take the swapped (narrow) form.
-constexpr int kNarrowRows = 64;
-// Experts per chunk of the tile walk (see decode_tile).
-constexpr int kExpertChunk = 8;
 
 struct GemmArgs {
   const int32_t* counts;
   const float* a_scale;  // [E, R, nkb], one row's scales contiguous
   const float* w_scale;  // [E, Ndim/128, nkb]
   int E, R, nkb, n_tiles;
-  int chunk;             // experts per chunk of the tile walk
   int I, H;
   uint8_t* zq;           // gate/up: [E, R, I]
   float* zs;             // gate/up: [E, R, I/128]
@@ -109,11 +94,7 @@ struct Control {
   int tile_start[kMaxExperts + 1];
   int cnt[kMaxExperts];
   float amax[2][2][kBM];  // [tile parity][column half][row]
-  // Narrow tiles: per epilogue warp, the K group's scale products of its 32
-  // tokens -- [0, 32) with the first half's weight scale, [32, 64) the second's.
-  alignas(16) float nscale[kEpiWarps][64];
 };
-static_assert(offsetof(Control, nscale) % 16 == 0, "narrow scale strips are read as float4");
 
 template <int BN, bool kGateUp>
 struct Layout {
@@ -130,26 +111,13 @@ struct Tile {
   int e, m_blk, n_blk, rows;
 };
 
-// Tile order: experts are taken in chunks of `chunk`; inside a chunk the walk
-// is N-slice major -- for each N slice, every M block of every expert of the
-// chunk -- so one weight slice's M blocks stay adjacent (they share it in L2)
-// while the tiles running at any moment mix lightly and heavily loaded
-// experts (weight-streaming and compute-heavy work), and a chunk's activation
-// rows stay in L2 across its N slices.  tile_start[e] = n_tiles * (M blocks
-// of experts < e), so a chunk's tiles occupy the same range as in an
-// expert-major walk.
-__device__ __forceinline__ Tile decode_tile(const Control* ctl, int E, int n_tiles, int chunk,
-                                            int t) {
+__device__ __forceinline__ Tile decode_tile(const Control* ctl, int E, int n_tiles, int t) {
   Tile r;
-  const int c0 = (find_expert(ctl->tile_start, E, t) / chunk) * chunk;
-  const int c1 = min(c0 + chunk, E);
-  const int t0 = ctl->tile_start[c0];
-  const int nb = (ctl->tile_start[c1] - t0) / n_tiles;  // M blocks in the chunk
-  const int local = t - t0;
-  r.n_blk = local / nb;
-  const int b = t0 / n_tiles + (local - r.n_blk * nb);  // M block index over all experts
-  r.e = find_expert(ctl->tile_start, E, b * n_tiles);
-  r.m_blk = b - ctl->tile_start[r.e] / n_tiles;
+  r.e = find_expert(ctl->tile_start, E, t);
+  const int local = t - ctl->tile_start[r.e];
+  const int mt = (ctl->tile_start[r.e + 1] - ctl->tile_start[r.e]) / n_tiles;
+  r.n_blk = local / mt;
+  r.m_blk = local - r.n_blk * mt;
   r.rows = min(kBM, ctl->cnt[r.e] - r.m_blk * kBM);
   return r;
 }
@@ -158,157 +126,6 @@ __device__ __forceinline__ Tile decode_tile(const Control* ctl, int E, int n_til
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   int dummy = 0;
   mbar_wait(bar, parity, &dummy);
-}
-
-// Epilogue of a narrow tile.  TMEM lane = weight row within a 128-row half,
-// column = token; this thread owns weight row lq*32 + lane of every half and
-// tokens [32*ch, 32*ch + 32).  Each lane fetches the scale of one of those
-// tokens per K group and forms its products with the halves' weight scales
-// (the same fp32 product as in the wide tile); the warp stages them in shared
-// memory and reads them back as broadcasts.
-// Returns false when a wait expired.
-template <int BN, bool kGateUp>
-__device__ __forceinline__ bool narrow_epilogue(Control* ctl, const GemmArgs& args, const Tile& tl,
-                                                uint32_t t_lane, int lq, int ch, int lane,
-                                                int& kcount, int iter, volatile int* abort_flag) {
-  constexpr int kHalves = BN / 128;  // gate|up, or two 128-column blocks of H (one when BN = 128)
-  const int nkb = args.nkb;
-  const int tok = 32 * ch + lane;    // token whose scales this lane fetches
-  const bool tok_ok = tok < tl.rows;
-  const size_t slot0 = static_cast<size_t>(tl.e) * args.R + tl.m_blk * kBM;  // tile's first slot
-  const float* asc = args.a_scale + (slot0 + (tok_ok ? tok : 0)) * nkb;
-  const float* wsA;
-  const float* wsB;
-  if (kGateUp) {
-    const int nb = 2 * args.I / 128;
-    wsA = args.w_scale + (static_cast<size_t>(tl.e) * nb + tl.n_blk) * nkb;
-    wsB = args.w_scale + (static_cast<size_t>(tl.e) * nb + args.I / 128 + tl.n_blk) * nkb;
-  } else {
-    const int nb = args.H / 128;
-    wsA = args.w_scale + (static_cast<size_t>(tl.e) * nb + tl.n_blk * kHalves) * nkb;
-    wsB = kHalves == 2 ? wsA + nkb : wsA;
-  }
-  uint64_t accA[16], accB[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) accA[i] = accB[i] = 0;
-  // Scales are fetched kPrefetch K groups ahead and rotate through registers,
-  // so no register copy waits on a load issued less than three groups ago.
-  constexpr int kPrefetch = 4;
-  float xr[kPrefetch], ar[kPrefetch], br[kPrefetch];
-#pragma unroll
-  for (int j = 0; j < kPrefetch; ++j) {
-    const bool in = j < nkb;
-    xr[j] = (in && tok_ok) ? __ldg(asc + j) : 0.f;
-    ar[j] = in ? __ldg(wsA + j) : 0.f;
-    br[j] = in ? __ldg(wsB + j) : 0.f;
-  }
-  float* prod = ctl->nscale[ch * 4 + lq];
-  for (int kb = 0; kb < nkb; ++kb) {
-    const float x = xr[0], wa = ar[0], wb = br[0];
-#pragma unroll
-    for (int j = 0; j + 1 < kPrefetch; ++j) {
-      xr[j] = xr[j + 1];
-      ar[j] = ar[j + 1];
-      br[j] = br[j + 1];
-    }
-    if (kb + kPrefetch < nkb) {
-      xr[kPrefetch - 1] = tok_ok ? __ldg(asc + kb + kPrefetch) : 0.f;
-      ar[kPrefetch - 1] = __ldg(wsA + kb + kPrefetch);
-      br[kPrefetch - 1] = __ldg(wsB + kb + kPrefetch);
-    }
-    // This lane's token: its scale times each half's weight scale.
-    prod[lane] = x * wa;
-    prod[32 + lane] = x * wb;
-    const int acc = kcount & 1;
-    const uint32_t acc_phase = (kcount >> 1) & 1;
-    if (!mbar_wait(&ctl->tfull[acc], acc_phase, abort_flag)) return false;
-    tc_fence_after();
-    const uint32_t base = t_lane + static_cast<uint32_t>(acc * BN + 32 * ch);
-    uint32_t pa[32], pb[32];
-    tmem_load32_issue(base, pa);
-    if (kHalves == 2) tmem_load32_issue(base + kNarrowRows, pb);
-    tmem_load_wait(pa);
-    if (kHalves == 2) tmem_load_wait(pb);
-    // The partial products are in registers: hand the buffer back at once.
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
-    ++kcount;
-    // Token scale products come back as broadcasts, four tokens per load.
-    const float4* pg = reinterpret_cast<const float4*>(prod);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const float4 g = pg[q];
-      ffma2_acc(accA[2 * q], f32x2_pack(g.x, g.y), pa[4 * q], pa[4 * q + 1]);
-      ffma2_acc(accA[2 * q + 1], f32x2_pack(g.z, g.w), pa[4 * q + 2], pa[4 * q + 3]);
-      if (kHalves == 2) {
-        const float4 u = pg[8 + q];
-        ffma2_acc(accB[2 * q], f32x2_pack(u.x, u.y), pb[4 * q], pb[4 * q + 1]);
-        ffma2_acc(accB[2 * q + 1], f32x2_pack(u.z, u.w), pb[4 * q + 2], pb[4 * q + 3]);
-      }
-    }
-    __syncwarp();  // every lane has read this group's products before the next overwrite
-  }
-  const int nt = min(32, tl.rows - 32 * ch);  // valid tokens of this thread (may be <= 0)
-  if (kGateUp) {
-    // Z = SiLU(gate) * up for weight row f = lq*32 + lane and 32 tokens.
-    float z[32], v[32];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float g0 = f32x2_lo(accA[i]), g1 = f32x2_hi(accA[i]);
-      const float u0 = f32x2_lo(accB[i]), u1 = f32x2_hi(accB[i]);
-      z[2 * i] = (g0 / (1.0f + expf(-g0))) * u0;
-      z[2 * i + 1] = (g1 / (1.0f + expf(-g1))) * u1;
-      v[2 * i] = fabsf(z[2 * i]);
-      v[2 * i + 1] = fabsf(z[2 * i + 1]);
-    }
-    // Per-token max over the warp's 32 rows, halving the set each step: after
-    // the step of offset o a lane keeps the tokens whose bit o matches its own,
-    // so lane j ends with token 32*ch + j.
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const bool upper = (lane & o) != 0;
-#pragma unroll
-      for (int i = 0; i < o; ++i) {
-        const float send = upper ? v[i] : v[i + o];
-        const float keep = upper ? v[i + o] : v[i];
-        v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
-      }
-    }
-    // Across the four lane-quarter warps: [lane quarter][64 tokens] per parity.
-    float* tamax = &ctl->amax[iter & 1][0][0];
-    tamax[lq * kNarrowRows + tok] = v[0];
-    mbar_arrive(&ctl->amax_bar);
-    if (!mbar_wait(&ctl->amax_bar, iter & 1, abort_flag)) return false;
-    const float am = fmaxf(fmaxf(tamax[tok], tamax[kNarrowRows + tok]),
-                           fmaxf(tamax[2 * kNarrowRows + tok], tamax[3 * kNarrowRows + tok]));
-    float mult, scale;
-    fp8_group_scale(am, &mult, &scale);
-    if (lq == 0 && tok_ok) args.zs[(slot0 + tok) * (args.I / 128) + tl.n_blk] = scale;
-    uint8_t* zcol = args.zq + (slot0 + 32 * ch) * args.I + tl.n_blk * 128 + lq * 32 + lane;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float mi = __shfl_sync(0xffffffffu, mult, i);
-      if (i < nt)
-        zcol[static_cast<size_t>(i) * args.I] =
-            static_cast<uint8_t>(pack_e4m3x2(__fmul_rn(z[i], mi), 0.f) & 0xFFu);
-    }
-  } else {
-    __nv_bfloat16* ocol = args.out + (slot0 + 32 * ch) * args.H + tl.n_blk * BN + lq * 32 + lane;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int ti = 2 * i + h;
-        if (ti < nt) {
-          __nv_bfloat16* o = ocol + static_cast<size_t>(ti) * args.H;
-          o[0] = __float2bfloat16_rn(h ? f32x2_hi(accA[i]) : f32x2_lo(accA[i]));
-          if (kHalves == 2) o[128] = __float2bfloat16_rn(h ? f32x2_hi(accB[i]) : f32x2_lo(accB[i]));
-        }
-      }
-    }
-  }
-  return true;
 }
 
 template <int BN, bool kGateUp>
@@ -366,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile(ctl, args.E, args.n_tiles, args.chunk, t);
+        const Tile tl = decode_tile(ctl, args.E, args.n_tiles, t);
         const int a_row = tl.e * args.R + tl.m_blk * kBM;
         int b_row0, b_row1;
         if (kGateUp) {
@@ -409,11 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     warpgroup_reg_dealloc<RegSplit<kGateUp>::kCtrl>();
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
-      constexpr uint32_t kIdescNarrow = idesc_e4m3_f32(kBM, kNarrowRows);
       int consumed = 0, kcount = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const bool narrow = decode_tile(ctl, args.E, args.n_tiles, args.chunk, t).rows <= kNarrowRows;
         for (int kb = 0; kb < nkb; ++kb) {
           const int stage = consumed % kStages;
           const uint32_t phase = (consumed / kStages) & 1;
@@ -429,22 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t adesc = smem_desc_kmajor_sw128(sa);
           const uint64_t bdesc = smem_desc_kmajor_sw128(sa + L::kABytes);
           const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
-          if (narrow) {
-            // Weights on M (each 128-row half of the B slot), tokens on N:
-            // half h accumulates into columns [64h, 64h + 64) of the buffer.
-            const uint64_t bdesc1 = smem_desc_kmajor_sw128(sa + L::kABytes + kBM * kBK);
 #pragma unroll
-            for (int k = 0; k < kBK / 32; ++k) {
-              mma_e4m3(d, bdesc + 2 * k, adesc + 2 * k, kIdescNarrow, k > 0 ? 1u : 0u);
-              if (BN == 256)
-                mma_e4m3(d + kNarrowRows, bdesc1 + 2 * k, adesc + 2 * k, kIdescNarrow,
-                         k > 0 ? 1u : 0u);
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < kBK / 32; ++k)  // 32 e4m3 = 32 bytes = 2 descriptor units
-              mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < kBK / 32; ++k)  // 32 e4m3 = 32 bytes = 2 descriptor units
+            mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, kIdesc, k > 0 ? 1u : 0u);
           mma_commit(&ctl->empty[stage]);
           mma_commit(&ctl->tfull[acc]);
           ++consumed;
@@ -472,12 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kcount = 0, iter = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++iter) {
-      const Tile tl = decode_tile(ctl, args.E, args.n_tiles, args.chunk, t);
-      if (tl.rows <= kNarrowRows) {
-        ok = narrow_epilogue<BN, kGateUp>(ctl, args, tl, t_lane, lq, ch, lane, kcount, iter,
-                                           abort_flag);
-        continue;
-      }
+      const Tile tl = decode_tile(ctl, args.E, args.n_tiles, t);
       const int m = tl.m_blk * kBM + row;
       const bool in_cap = m < args.R;
       const float* asc = args.a_scale + (static_cast<size_t>(tl.e) * args.R + m) * nkb;
@@ -538,16 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        : static_cast<uint32_t>(ch * kCols + 64 * j);
           const uint64_t sx2 = (kGateUp && j) ? s1x2 : s0x2;
           tmem_load64_sync(base + col, buf);
-          if (j == kCols / 64 - 1) {
-            // Last chunk is in registers: the buffer goes back to the MMA
-            // before its FMAs.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
-          }
 #pragma unroll
           for (int i = 0; i < 32; ++i) ffma2_acc(acc2[32 * j + i], sx2, buf[2 * i], buf[2 * i + 1]);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->tempty[acc]);
         ++kcount;
       }
       if (!ok) break;
@@ -734,7 +527,6 @@ cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t
   a.R = R;
   a.nkb = H / kBK;
   a.n_tiles = I / 128;
-  a.chunk = kExpertChunk;
   a.I = I;
   a.H = H;
   a.zq = zq;
@@ -758,7 +550,6 @@ cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* 
   a.E = E;
   a.R = R;
   a.nkb = I / kBK;
-  a.chunk = kExpertChunk;
   a.I = I;
   a.H = H;
   a.out = static_cast<__nv_bfloat16*>(out);
