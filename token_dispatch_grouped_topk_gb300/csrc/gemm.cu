@@ -11,9 +11,13 @@
 // Design (one CTA per SM, persistent):
 //  - tiles are 128 rows x BN columns of one expert; the tile list is derived on
 //    the device from counts (prefix of ceil(count/128) * n_tiles per expert),
-//    walked by all CTAs with a stride of gridDim.x.  Within an expert the M
-//    blocks of one N slice are adjacent so concurrently running CTAs share the
-//    same weight slice in L2;
+//    walked by all CTAs with a stride of gridDim.x.  Within an expert the
+//    walk is M-block major: the N slices of one 128-row block are adjacent,
+//    so a block's activation rows are fetched once while the CTAs running at
+//    the same time share the expert's weight slices in L2.  (Measured on
+//    real FP8 activations at the large layer: the N-slice-major walk re-read
+//    activation blocks once per slice and moved 25 GB per gate/up launch
+//    against 20 GB, 12% slower.);
 //  - warp 0 (one thread) streams A and B tiles with TMA (128-byte swizzle) into
 //    a 4-stage shared-memory ring guarded by full/empty mbarriers;
 //  - warp 1 (one thread) issues tcgen05.mma kind::f8f6f4 (M=128, N=BN, K=32,
@@ -111,13 +115,13 @@ struct Tile {
   int e, m_blk, n_blk, rows;
 };
 
+// Tile t -> (expert, M block, N slice), M-block major within an expert.
 __device__ __forceinline__ Tile decode_tile(const Control* ctl, int E, int n_tiles, int t) {
   Tile r;
   r.e = find_expert(ctl->tile_start, E, t);
   const int local = t - ctl->tile_start[r.e];
-  const int mt = (ctl->tile_start[r.e + 1] - ctl->tile_start[r.e]) / n_tiles;
-  r.n_blk = local / mt;
-  r.m_blk = local - r.n_blk * mt;
+  r.m_blk = local / n_tiles;
+  r.n_blk = local - r.m_blk * n_tiles;
   r.rows = min(kBM, ctl->cnt[r.e] - r.m_blk * kBM);
   return r;
 }
