@@ -7,6 +7,9 @@
  *   moe_expert_compute  recv, counts, weights  -> out  [E,R,H]
  *   moe_combine         out, src_map, topk_w   -> y    [T,H]
  *
+ * plus the same three calls for a packed layout without capacity gaps
+ * (moe_*_packed, below) and a dispatch fused with the FP8 quantisation.
+ *
  * The steps follow "SGLang、NCCL 与 MoE EP" (Level 1 §1.1: the routed output
  * is the weighted sum of the expert outputs; §2.3: receive, compact and the
  * source map; §3.2: dispatch, compute, combine of one token) and "SGLang
@@ -208,6 +211,43 @@ moe_status moe_gemm_gateup_silu(const uint8_t* xq, const float* xs, const int32_
 moe_status moe_gemm_down(const uint8_t* zq, const float* zs, const int32_t* counts, int E, int R,
                          int H, int I, const uint8_t* w2, const float* w2_scale, void* out,
                          int32_t* dev_status, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Packed layout -- "SGLang Expert Compute Backend", §2.6 (compact storage):
+ * the valid rows of all experts are stored back to back, expert e's rows at
+ * [base_e, base_e + c_e) with c_e = min(counts[e], R) and base_e the sum of
+ * c_j over j < e (the page's example: counts [70, 12] -> expert 1 starts at row
+ * 70, 82 rows in all), instead of one capacity block of R rows per expert.
+ * Routing, slots, capacity drops and all arithmetic are those of the padded
+ * calls above; only the row of slot s of expert e changes from e*R + s to
+ * base_e + s, so src_map holds base_e + s.  The receive-side buffers need
+ * `rows` rows instead of E*R; the bases are derived on the device from counts.
+ *
+ * moe_dispatch_packed      as moe_dispatch, with recv device BF16 [rows, H];
+ *                          rows >= min(T*K, E*R) (room for every kept route),
+ *                          rows <= 2^30, else MOE_ERR_INVALID_ARG.
+ * moe_expert_compute_packed  as moe_expert_compute, with recv and out device
+ *                          BF16 [rows, H] in the packed layout (counts, E and R
+ *                          as given to moe_dispatch_packed) and a workspace of
+ *                          moe_expert_compute_packed_workspace_size(rows, H, I)
+ *                          bytes.  Rows at or past `rows` are never touched, even
+ *                          if counts claim more.
+ * moe_combine_packed       as moe_combine, with out device BF16 [rows, H]; a
+ *                          src_map entry outside [0, rows) counts as no route.
+ * ------------------------------------------------------------------------- */
+moe_status moe_dispatch_packed(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
+                               int H, int K, int E, int R, int64_t rows, void* recv,
+                               int32_t* counts, int32_t* src_map, int32_t* dev_status,
+                               void* workspace, size_t workspace_bytes, moe_stream_t stream);
+size_t moe_expert_compute_packed_workspace_size(int64_t rows, int H, int I);
+moe_status moe_expert_compute_packed(const void* recv, const int32_t* counts, int E, int R,
+                                     int64_t rows, int H, int I, const uint8_t* w13,
+                                     const float* w13_scale, const uint8_t* w2,
+                                     const float* w2_scale, void* out, int32_t* dev_status,
+                                     void* workspace, size_t workspace_bytes, moe_stream_t stream);
+moe_status moe_combine_packed(const void* out, int64_t rows, const int32_t* src_map,
+                              const float* topk_w, int T, int H, int K, void* y,
+                              moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_selftest_bounded_wait -- exercises the device-side failure path: one

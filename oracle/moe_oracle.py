@@ -39,6 +39,7 @@ __all__ = [
     "QUANT_GROUP", "E4M3_MAX",
     "e4m3_decode", "e4m3_encode", "bf16_bits_to_f32", "f32_to_bf16_rne",
     "f32_to_bf16_bits", "expert_placement", "RouteResult", "route", "scatter",
+    "packed_row_offsets", "packed_src_map",
     "route_stats", "quantize_rows", "gemm_block_scaled", "silu",
     "expert_forward", "combine_fp64", "combine_f32_sequential", "moe_layer",
     "m_blocks", "valid_tiles", "m_fill_rate", "align_index_capacity",
@@ -199,6 +200,30 @@ def scatter(x: np.ndarray, src_map: np.ndarray, E: int, R: int) -> np.ndarray:
             if q >= 0:
                 recv[q] = x[t]
     return recv.reshape(E, R, H)
+
+
+def packed_row_offsets(counts) -> np.ndarray:
+    """Compact storage, "SGLang Expert Compute Backend", §2.6: the valid rows
+    of the experts are laid out back to back, so expert e starts where expert
+    e-1's valid rows end.  Returns the E+1 offsets (offsets[-1] = total valid
+    rows).  In the page's example, counts [70, 12] put expert 1's first row
+    right after expert 0's 70th: offsets [0, 70, 82]."""
+    off = [0]
+    for c in counts:
+        off.append(off[-1] + int(c))
+    return np.asarray(off, dtype=np.int64)
+
+
+def packed_src_map(src_map: np.ndarray, counts, R: int) -> np.ndarray:
+    """The source map of the packed layout: route (t, k) kept at slot s of
+    expert e (flat padded row q = e*R + s) is stored at row offsets[e] + s."""
+    off = packed_row_offsets(counts)
+    out = np.full_like(src_map, -1)
+    for idx, q in np.ndenumerate(src_map):
+        if q >= 0:
+            e, s = divmod(int(q), R)
+            out[idx] = off[e] + s
+    return out
 
 
 def route_stats(topk_idx: np.ndarray, L: int, src_rank: np.ndarray) -> dict:

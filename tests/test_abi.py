@@ -94,3 +94,31 @@ def test_compute_and_combine_reject_on_host(lib):
     assert lib.moe_combine(FAKE, FAKE, FAKE, 4, 256, 40, 8, 128, FAKE, None) == -1   # K > 32
     assert lib.moe_gemm_down(FAKE, FAKE, FAKE, 2, 128, 256, 128, FAKE, FAKE, None, FAKE, None) == -1
     assert lib.moe_quantize_fp8(FAKE, FAKE, 2, 128, 250, FAKE, FAKE, None) == -1
+
+
+def test_packed_entry_points_reject_on_host(lib):
+    """The packed layout's calls validate before launching: the receive buffer
+    must have room for every kept route (min(T*K, E*R) rows)."""
+    ws = 1 << 20
+    # T*K = 224 routes, E*R = 1024 capacity rows -> at least 224 rows
+    assert lib.moe_dispatch_packed(FAKE, FAKE, None, 112, 256, 2, 8, 128, 223, FAKE, FAKE, FAKE,
+                                   FAKE, FAKE, ws, None) == -1
+    assert lib.moe_dispatch_packed(FAKE, FAKE, None, 112, 256, 2, 8, 128, 0, FAKE, FAKE, FAKE,
+                                   FAKE, FAKE, ws, None) == -1
+    assert lib.moe_dispatch_packed(FAKE, FAKE, None, 112, 256, 2, 8, 128, 224, FAKE, FAKE, FAKE,
+                                   FAKE, FAKE, 8, None) == -3          # workspace checked next
+    assert lib.moe_dispatch_packed(FAKE, FAKE, None, 112, 200, 2, 8, 128, 224, FAKE, FAKE, FAKE,
+                                   FAKE, FAKE, ws, None) == -1         # H % 128
+    # packed compute: workspace sized by rows (xq, xs, zq, zs, each 256-byte aligned)
+    al = lambda v: (v + 255) // 256 * 256
+    ws82 = lib.moe_expert_compute_packed_workspace_size(82, 256, 128)
+    assert ws82 == al(al(al(al(82 * 256) + 82 * 2 * 4) + 82 * 128) + 82 * 1 * 4)
+    assert lib.moe_expert_compute_packed_workspace_size(2 * 128, 256, 128) == \
+        lib.moe_expert_compute_workspace_size(2, 128, 256, 128)
+    assert lib.moe_expert_compute_packed_workspace_size(0, 256, 128) == 0
+    assert lib.moe_expert_compute_packed(FAKE, FAKE, 2, 128, 82, 256, 128, FAKE, FAKE, FAKE, FAKE,
+                                         FAKE, FAKE, FAKE, ws82 - 1, None) == -3
+    assert lib.moe_expert_compute_packed(FAKE, FAKE, 2, 128, 0, 256, 128, FAKE, FAKE, FAKE, FAKE,
+                                         FAKE, FAKE, FAKE, ws82, None) == -1
+    assert lib.moe_combine_packed(FAKE, 0, FAKE, FAKE, 4, 256, 2, FAKE, None) == -1
+    assert lib.moe_combine_packed(FAKE, 82, FAKE, FAKE, 4, 256, 33, FAKE, None) == -1  # K > 32

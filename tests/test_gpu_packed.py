@@ -1,0 +1,150 @@
+"""The packed layout ("SGLang Expert Compute Backend", §2.6, compact storage):
+expert rows back to back from the prefix of the clamped counts, through
+moe_dispatch_packed, moe_expert_compute_packed and moe_combine_packed.
+
+Bit-exact against the oracle's packed source map and against the padded path
+(same routing, same arithmetic, only the row addresses differ)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from token_dispatch_grouped_topk_gb300 import api
+from token_dispatch_grouped_topk_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    api._lib.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def _bits(t):
+    return t.view(torch.int16)
+
+
+@pytest.mark.parametrize("T,E,K,R,H", [(300, 33, 5, 40, 640), (4, 8, 2, 4, 256), (2000, 64, 8, 200, 1024),
+                                       (0, 6, 2, 10, 256), (257, 9, 3, 1000, 384)])
+def test_dispatch_packed_matches_oracle_and_padded(T, E, K, R, H):
+    g = torch.Generator().manual_seed(T * 7 + E)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16).to(DEV)
+    logits = torch.randn(T, E, generator=g)
+    logits[:, : E // 3] += 2.0                      # skew: some experts overflow R
+    idx = torch.topk(logits, K, dim=1).indices
+    if T > 3:
+        idx[3, 0] = -1                              # padding route
+    w = torch.rand(T, K, generator=g)
+    idx_d, w_d = idx.to(DEV), w.to(DEV)
+    recv_p, cnt_p, map_p, st_p = api.moe_dispatch_packed(x, idx_d, w_d, E, R)
+    recv_d, cnt_d, map_d, st_d = api.moe_dispatch(x, idx_d, w_d, E, R)
+    torch.cuda.synchronize()
+    rr = O.route(idx.numpy(), E, R)
+    assert cnt_p.cpu().tolist() == rr.counts.tolist() == cnt_d.cpu().tolist()
+    assert np.array_equal(map_p.cpu().numpy(), O.packed_src_map(rr.src_map, rr.counts, R))
+    assert st_p.cpu().tolist() == st_d.cpu().tolist()
+    assert recv_p.shape[0] == api.packed_rows(T, K, E, R)
+    off = O.packed_row_offsets(rr.counts)
+    for e in range(E):
+        c = int(rr.counts[e])
+        assert torch.equal(_bits(recv_p[off[e]:off[e] + c]), _bits(recv_d[e, :c])), f"expert {e}"
+
+
+def _expert_inputs(E, R, H, I, counts, seed):
+    g = torch.Generator().manual_seed(seed)
+    recv = torch.randn(E, R, H, generator=g).to(torch.bfloat16)
+    w13, s13, w2, s2 = W.expert_weights(E, H, I, seed, "cpu")
+    return recv, w13.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV)
+
+
+@pytest.mark.parametrize("E,R,H,I,counts", [
+    (4, 384, 512, 384, [300, 129, 0, 17]),
+    (13, 256, 384, 256, [1, 31, 32, 33, 63, 64, 65, 127, 129, 192, 193, 256, 0]),
+    (3, 200, 256, 128, [200, 199, 64]),
+])
+def test_expert_compute_packed_matches_padded(E, R, H, I, counts):
+    recv, w13, s13, w2, s2 = _expert_inputs(E, R, H, I, counts, seed=21)
+    cd = torch.tensor(counts, dtype=torch.int32, device=DEV)
+    out_d = api.moe_expert_compute(recv.to(DEV), cd, w13, s13, w2, s2)
+    off = O.packed_row_offsets(counts)
+    total = int(off[-1])
+    rows = total + 37                                     # spare rows must stay untouched
+    packed = torch.cat([recv[e, :c] for e, c in enumerate(counts)] +
+                       [torch.zeros(rows - total, H, dtype=torch.bfloat16)]).to(DEV)
+    out_p = torch.full((rows, H), 3.0, dtype=torch.bfloat16, device=DEV)
+    st = torch.zeros(2, dtype=torch.int32, device=DEV)
+    api.moe_expert_compute_packed(packed, cd, R, w13, s13, w2, s2, out=out_p, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, 0]
+    for e, c in enumerate(counts):
+        assert torch.equal(_bits(out_p[off[e]:off[e] + c]), _bits(out_d[e, :c])), f"expert {e}"
+    assert bool((out_p[total:].float() == 3.0).all()), "rows past the packed range were written"
+
+
+def test_expert_compute_packed_never_writes_past_rows():
+    """Counts that claim more rows than the buffer holds: every row at or past
+    `rows` stays untouched (the tail of a larger allocation is a sentinel)."""
+    E, R, H, I = 3, 256, 256, 128
+    counts = [200, 150, 100]                              # 450 rows claimed
+    recv, w13, s13, w2, s2 = _expert_inputs(E, R, H, I, counts, seed=22)
+    rows = 300                                            # buffer holds only 300
+    big_in = torch.zeros(rows + 200, H, dtype=torch.bfloat16, device=DEV)
+    big_in[:rows] = torch.randn(rows, H).to(torch.bfloat16).to(DEV)
+    big_out = torch.full((rows + 200, H), 5.0, dtype=torch.bfloat16, device=DEV)
+    cd = torch.tensor(counts, dtype=torch.int32, device=DEV)
+    st = torch.zeros(2, dtype=torch.int32, device=DEV)
+    api.moe_expert_compute_packed(big_in[:rows], cd, R, w13, s13, w2, s2, out=big_out[:rows],
+                                  dev_status=st)
+    torch.cuda.synchronize()
+    assert bool((big_out[rows:].float() == 5.0).all())
+    assert st.cpu().tolist() == [0, 0]
+
+
+@pytest.mark.parametrize("name", ["traced", "decode", "prefill"])
+def test_layer_packed_bit_identical_to_padded(name):
+    d = W.make_layer_inputs(name, seed=0, device=DEV)
+    wl = d["wl"]
+    dev = torch.device(DEV)
+    pad = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
+    pk = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev, packed=True)
+    args = (d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
+    y_pad = pad.forward(*args).clone()
+    y_pk = pk.forward(*args).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y_pk), _bits(y_pad))
+    assert pk.dev_status.cpu().tolist() == pad.dev_status.cpu().tolist()
+    assert pk.recv.shape == (api.packed_rows(wl.T, wl.K, wl.E, wl.R), wl.H)
+
+
+def test_layer_packed_graph_replay_new_routes():
+    """Captured once, replayed with new routings written into the same input
+    buffers: the packed lane's output equals the padded lane's each time."""
+    d = W.make_layer_inputs("decode", seed=0, device=DEV)
+    wl = d["wl"]
+    dev = torch.device(DEV)
+    pad = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
+    pk = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev, packed=True)
+    x, idx, w = d["x"].clone(), d["topk_idx"].clone(), d["topk_w"].clone()
+    wts = (d["w13"], d["s13"], d["w2"], d["s2"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pk.forward(x, idx, w, *wts)                        # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pk.forward(x, idx, w, *wts)
+    for seed in (5, 6):
+        i2, w2_ = W.router(wl.T, wl.E, wl.K, W.router_bias(wl, seed, DEV), seed + 1, DEV)
+        idx.copy_(i2)
+        w.copy_(w2_)
+        g.replay()
+        ref = pad.forward(x, idx, w, *wts)
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(pk.y), _bits(ref)), f"routing {seed}"

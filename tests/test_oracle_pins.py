@@ -552,3 +552,34 @@ def test_mutants_are_caught():
     def comb_noweight(out, src, w):
         return O.combine_fp64(out, src, np.ones_like(w))
     assert _fails(pin_combine_traced, comb_noweight)
+
+
+def test_packed_offsets_page_example():
+    """"SGLang Expert Compute Backend", §2.6: with compact storage expert 1's
+    first row follows expert 0's 70th valid row; 82 valid rows in place of the
+    256 capacity rows of the [70, 12] example."""
+    off = O.packed_row_offsets([70, 12])
+    assert off.tolist() == [0, 70, 82]
+    assert off[-1] == 82 and 2 * 128 == 256
+
+
+def test_packed_src_map_is_order_preserving_bijection():
+    """Brute force over random routings: the packed map sends the kept routes
+    of expert e, in slot order, onto consecutive rows starting at the sum of
+    the earlier experts' counts, and covers [0, sum(counts)) exactly once."""
+    rng = np.random.default_rng(11)
+    for _ in range(30):
+        E, R, T, K = int(rng.integers(1, 9)), int(rng.integers(1, 12)), int(rng.integers(0, 40)), 2
+        K = min(K, E)
+        idx = np.stack([rng.choice(np.arange(-1, E), size=K, replace=False) for _ in range(T)]) \
+            if T else np.zeros((0, K), np.int64)
+        r = O.route(idx, E, R)
+        p = O.packed_src_map(r.src_map, r.counts, R)
+        kept = p[p >= 0]
+        assert sorted(kept.tolist()) == list(range(int(np.sum(r.counts))))
+        start = 0
+        for e in range(E):
+            slots = sorted(int(q) - e * R for q in r.src_map.flatten() if q >= 0 and q // R == e)
+            rows = sorted(int(pp) for q, pp in zip(r.src_map.flatten(), p.flatten()) if q >= 0 and q // R == e)
+            assert rows == [start + s for s in slots]
+            start += int(r.counts[e])

@@ -13,6 +13,7 @@ import threading
 from . import build as _build
 
 c_int, c_size_t, c_void_p, c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
+c_int64 = ctypes.c_int64
 
 # name -> (restype, argtypes), mirroring include/moe.h
 SIGNATURES = {
@@ -39,6 +40,15 @@ SIGNATURES = {
                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "moe_gemm_down": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p,
                               c_void_p, c_void_p, c_void_p, c_void_p]),
+    "moe_dispatch_packed": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                    c_int, c_int64, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    c_void_p, c_size_t, c_void_p]),
+    "moe_expert_compute_packed_workspace_size": (c_size_t, [c_int64, c_int, c_int]),
+    "moe_expert_compute_packed": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int64, c_int, c_int,
+                                          c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                          c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_combine_packed": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_int, c_int, c_int,
+                                   c_void_p, c_void_p]),
 }
 
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",

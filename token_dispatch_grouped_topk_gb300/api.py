@@ -16,7 +16,8 @@ __all__ = [
     "MoeError", "dispatch_workspace_size", "expert_compute_workspace_size", "moe_dispatch",
     "moe_dispatch_quant",
     "moe_expert_compute", "moe_combine", "moe_quantize_fp8", "moe_gemm_gateup_silu",
-    "moe_gemm_down", "MoeLayerBuffers", "HostPipeline", "TwoBatchOverlap", "DEV_BAD_EXPERT_ID",
+    "moe_gemm_down", "moe_dispatch_packed", "moe_expert_compute_packed", "moe_combine_packed",
+    "packed_rows", "MoeLayerBuffers", "HostPipeline", "TwoBatchOverlap", "DEV_BAD_EXPERT_ID",
     "DEV_CAPACITY_DROPPED", "DEV_TIMEOUT",
 ]
 
@@ -136,6 +137,76 @@ def moe_expert_compute(recv, counts, w13, w13_scale, w2, w2_scale, *, out=None, 
     return out
 
 
+def packed_rows(T: int, K: int, E: int, R: int) -> int:
+    """Rows of a packed receive buffer with room for every kept route:
+    min(T*K, E*R) ("SGLang Expert Compute Backend", §2.6)."""
+    return max(1, min(T * K, E * R))
+
+
+def moe_dispatch_packed(x, topk_idx, topk_w, E: int, R: int, *, rows=None, recv=None, counts=None,
+                        src_map=None, dev_status=None, workspace=None, stream=None):
+    """Dispatch into the packed layout: expert e's rows back to back from the
+    prefix of the clamped counts.  Returns ``(recv [rows,H] bf16, counts,
+    src_map (= base_e + slot), dev_status)``."""
+    lib = _lib.load()
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    dev = x.device
+    _need(x, torch.bfloat16, "x")
+    _need(topk_idx, torch.int64, "topk_idx")
+    if rows is None:
+        rows = recv.shape[0] if recv is not None else packed_rows(T, K, E, R)
+    if recv is None:
+        recv = torch.empty(rows, H, dtype=torch.bfloat16, device=dev)
+    if counts is None:
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+    if src_map is None:
+        src_map = torch.empty(T, K, dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(2, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _workspace(lib.moe_dispatch_workspace_size(T, K, E), dev)
+    st = lib.moe_dispatch_packed(_p(x), _p(topk_idx), _p(topk_w), T, H, K, E, R, rows, _p(recv),
+                                 _p(counts), _p(src_map), _p(dev_status), _p(workspace),
+                                 workspace.numel(), _s(stream))
+    _lib.check("moe_dispatch_packed", st)
+    return recv, counts, src_map, dev_status
+
+
+def moe_expert_compute_packed(recv, counts, R: int, w13, w13_scale, w2, w2_scale, *, out=None,
+                              dev_status=None, workspace=None, stream=None):
+    """``moe_expert_compute`` on the packed layout: recv and out are [rows, H]."""
+    lib = _lib.load()
+    rows, H = recv.shape
+    E = counts.shape[0]
+    w13, w2 = _u8(w13), _u8(w2)
+    I = w13.shape[1] // 2
+    dev = recv.device
+    if out is None:
+        out = torch.empty(rows, H, dtype=torch.bfloat16, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(2, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _workspace(lib.moe_expert_compute_packed_workspace_size(rows, H, I), dev)
+    st = lib.moe_expert_compute_packed(_p(recv), _p(counts), E, R, rows, H, I, _p(w13),
+                                       _p(w13_scale), _p(w2), _p(w2_scale), _p(out),
+                                       _p(dev_status), _p(workspace), workspace.numel(), _s(stream))
+    _lib.check("moe_expert_compute_packed", st)
+    return out
+
+
+def moe_combine_packed(out, src_map, topk_w, *, y=None, stream=None):
+    """``moe_combine`` on the packed layout: out is [rows, H]."""
+    lib = _lib.load()
+    rows, H = out.shape
+    T, K = src_map.shape
+    if y is None:
+        y = torch.empty(T, H, dtype=torch.bfloat16, device=out.device)
+    st = lib.moe_combine_packed(_p(out), rows, _p(src_map), _p(topk_w), T, H, K, _p(y), _s(stream))
+    _lib.check("moe_combine_packed", st)
+    return y
+
+
 def moe_combine(out, src_map, topk_w, *, y=None, stream=None):
     """Weighted combine back into token order.  Returns ``y [T,H] bf16``."""
     lib = _lib.load()
@@ -214,38 +285,51 @@ class MoeLayerBuffers:
     I: int
     R: int
     device: torch.device
+    packed: bool = False   # packed layout (moe_*_packed): [rows, H] buffers, no capacity gaps
 
     def __post_init__(self):
         d, E, R, H, I, T, K = self.device, self.E, self.R, self.H, self.I, self.T, self.K
-        self.recv = torch.empty(E, R, H, dtype=torch.bfloat16, device=d)
-        self.out = torch.empty(E, R, H, dtype=torch.bfloat16, device=d)
+        if self.packed:
+            self.rows = packed_rows(T, K, E, R)
+            shape = (self.rows, H)
+            ws = _lib.load().moe_expert_compute_packed_workspace_size(self.rows, H, I)
+        else:
+            self.rows = E * R
+            shape = (E, R, H)
+            ws = expert_compute_workspace_size(E, R, H, I)
+        self.recv = torch.empty(*shape, dtype=torch.bfloat16, device=d)
+        self.out = torch.empty(*shape, dtype=torch.bfloat16, device=d)
         self.counts = torch.zeros(E, dtype=torch.int32, device=d)
         self.src_map = torch.empty(T, K, dtype=torch.int32, device=d)
         self.dev_status = torch.zeros(2, dtype=torch.int32, device=d)
         self.y = torch.empty(T, H, dtype=torch.bfloat16, device=d)
         self.ws_dispatch = _workspace(dispatch_workspace_size(T, K, E), d)
-        self.ws_compute = _workspace(expert_compute_workspace_size(E, R, H, I), d)
+        self.ws_compute = _workspace(ws, d)
 
     def workspace_views(self):
         """(xq, xs, zq, zs): the FP8 activations and scales inside the expert
-        compute workspace, in the layout moe_expert_compute uses."""
-        E, R, H, I = self.E, self.R, self.H, self.I
+        compute workspace, in the layout moe_expert_compute(_packed) uses:
+        [E, R, ...] padded, [rows, ...] packed."""
+        H, I, n = self.H, self.I, self.rows
+        lead = (self.rows,) if self.packed else (self.E, self.R)
         G, GI = H // 128, I // 128
         ws = self.ws_compute
         al = lambda v: (v + 255) // 256 * 256
-        o1 = al(E * R * H)
-        o2 = al(o1 + E * R * G * 4)
-        o3 = al(o2 + E * R * I)
-        xq = ws[:E * R * H].view(E, R, H)
-        xs = ws[o1:o1 + E * R * G * 4].view(torch.float32).view(E, R, G)
-        zq = ws[o2:o2 + E * R * I].view(E, R, I)
-        zs = ws[o3:o3 + E * R * GI * 4].view(torch.float32).view(E, R, GI)
+        o1 = al(n * H)
+        o2 = al(o1 + n * G * 4)
+        o3 = al(o2 + n * I)
+        xq = ws[:n * H].view(*lead, H)
+        xs = ws[o1:o1 + n * G * 4].view(torch.float32).view(*lead, G)
+        zq = ws[o2:o2 + n * I].view(*lead, I)
+        zs = ws[o3:o3 + n * GI * 4].view(torch.float32).view(*lead, GI)
         return xq, xs, zq, zs
 
     def forward_fused(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None):
         """The same layer with dispatch and quantisation fused (moe_dispatch_quant
         -> gate/up GEMM -> down GEMM -> combine); the BF16 receive buffer is not
-        used.  Returns ``y`` (bit-identical to ``forward``)."""
+        used.  Returns ``y`` (bit-identical to ``forward``).  Padded lanes only."""
+        if self.packed:
+            raise ValueError("forward_fused runs on the padded layout")
         xq, xs, zq, zs = self.workspace_views()
         moe_dispatch_quant(x, topk_idx, topk_w, self.E, self.R, xq=xq, xs=xs, counts=self.counts,
                            src_map=self.src_map, dev_status=self.dev_status,
@@ -260,12 +344,22 @@ class MoeLayerBuffers:
     def forward(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None, y=None):
         """dispatch -> expert compute -> combine on one stream; returns ``y``
         (the lane's own output buffer unless ``y`` [T, H] BF16 is given)."""
+        y = self.y if y is None else y
+        if self.packed:
+            moe_dispatch_packed(x, topk_idx, topk_w, self.E, self.R, recv=self.recv,
+                                counts=self.counts, src_map=self.src_map,
+                                dev_status=self.dev_status, workspace=self.ws_dispatch,
+                                stream=stream)
+            moe_expert_compute_packed(self.recv, self.counts, self.R, w13, w13_scale, w2,
+                                      w2_scale, out=self.out, dev_status=self.dev_status,
+                                      workspace=self.ws_compute, stream=stream)
+            moe_combine_packed(self.out, self.src_map, topk_w, y=y, stream=stream)
+            return y
         moe_dispatch(x, topk_idx, topk_w, self.E, self.R, recv=self.recv, counts=self.counts,
                      src_map=self.src_map, dev_status=self.dev_status, workspace=self.ws_dispatch,
                      stream=stream)
         moe_expert_compute(self.recv, self.counts, w13, w13_scale, w2, w2_scale, out=self.out,
                            dev_status=self.dev_status, workspace=self.ws_compute, stream=stream)
-        y = self.y if y is None else y
         moe_combine(self.out, self.src_map, topk_w, y=y, stream=stream)
         return y
 

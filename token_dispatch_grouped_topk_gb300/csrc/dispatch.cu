@@ -14,6 +14,9 @@
 //                       (warp match + per-warp counts), writes src_map and
 //                       copies each token row once from x to its K rows of
 //                       recv with 16-byte vector accesses.
+// The row of slot s of expert e is e*R + s (padded layout) or base_e + s with
+// base_e the prefix of the clamped counts (packed layout, §2.6 of "SGLang
+// Expert Compute Backend": the valid rows of all experts back to back).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -114,13 +117,16 @@ __global__ void __launch_bounds__(kScanThreads)
 
 __global__ void __launch_bounds__(kDispatchWarps * 32)
     route_scatter_kernel(const uint4* __restrict__ x, const int64_t* __restrict__ topk_idx, int T,
-                         int H, int K, int E, int R, int nblocks, const int32_t* __restrict__ base,
+                         int H, int K, int E, RowLayout rl, int nblocks,
+                         const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
                          uint4* __restrict__ recv, int32_t* __restrict__ src_map,
                          int vec_per_slice) {
   extern __shared__ int smem[];
   int* s_cnt = smem;                           // [kDispatchWarps][E]
   int* s_dest = smem + kDispatchWarps * E;     // [kDispatchWarps][32]
+  int* s_rows = s_dest + kDispatchWarps * 32;  // [E + 1] packed row bases
   for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) s_cnt[i] = 0;
+  if (rl.packed) expert_prefix(counts, E, rl.R, 1, 1, s_rows, nullptr);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kDispatchWarps + warp;
@@ -133,7 +139,7 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   if (r.e >= 0) {
     int s = base[static_cast<size_t>(r.e) * nblocks + blockIdx.x] + lane_rank;
     for (int w = 0; w < warp; ++w) s += s_cnt[w * E + r.e];
-    if (s < R) q = r.e * R + s;
+    if (s < rl.R) q = (rl.packed ? s_rows[r.e] : r.e * rl.R) + s;
   }
   if (blockIdx.y == 0 && r.active) src_map[static_cast<int64_t>(r.t) * K + r.k] = q;
   s_dest[warp * 32 + lane] = q;
@@ -180,15 +186,17 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
 // Each block takes a slice of whole 128-groups of its tokens' rows.
 __global__ void __launch_bounds__(kDispatchWarps * 32)
     route_scatter_fp8_kernel(const uint4* __restrict__ x, const int64_t* __restrict__ topk_idx,
-                             int T, int H, int K, int E, int R, int nblocks,
-                             const int32_t* __restrict__ base, uint2* __restrict__ xq,
-                             float* __restrict__ xs, int32_t* __restrict__ src_map,
-                             int groups_per_slice) {
+                             int T, int H, int K, int E, RowLayout rl, int nblocks,
+                             const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
+                             uint2* __restrict__ xq, float* __restrict__ xs,
+                             int32_t* __restrict__ src_map, int groups_per_slice) {
   extern __shared__ int smem[];
   int* s_cnt = smem;                                               // [kDispatchWarps][E]
   int* s_dest = smem + kDispatchWarps * E;                         // [kDispatchWarps][32]
-  float* s_sc = reinterpret_cast<float*>(s_dest + kDispatchWarps * 32);  // [warps][groups_per_slice]
+  int* s_rows = s_dest + kDispatchWarps * 32;                       // [E + 1] packed row bases
+  float* s_sc = reinterpret_cast<float*>(s_rows + E + 1);          // [warps][groups_per_slice]
   for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) s_cnt[i] = 0;
+  if (rl.packed) expert_prefix(counts, E, rl.R, 1, 1, s_rows, nullptr);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
@@ -202,7 +210,7 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   if (r.e >= 0) {
     int sl = base[static_cast<size_t>(r.e) * nblocks + blockIdx.x] + lane_rank;
     for (int w = 0; w < warp; ++w) sl += s_cnt[w * E + r.e];
-    if (sl < R) q = r.e * R + sl;
+    if (sl < rl.R) q = (rl.packed ? s_rows[r.e] : r.e * rl.R) + sl;
   }
   if (blockIdx.y == 0 && r.active) src_map[static_cast<int64_t>(r.t) * K + r.k] = q;
   s_dest[warp * 32 + lane] = q;
@@ -278,8 +286,9 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
 }  // namespace
 
 cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
-                            int R, void* recv, int32_t* counts, int32_t* src_map,
+                            RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
                             int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s) {
+  const int R = rl.R;
   cudaError_t err = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
   if (err != cudaSuccess) return err;
   const int nblocks = dispatch_blocks(T, K);
@@ -299,9 +308,9 @@ cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H
   hsplit = max(1, min(hsplit, nvec / 32));
   const int vec_per_slice = (nvec + hsplit - 1) / hsplit;
   hsplit = (nvec + vec_per_slice - 1) / vec_per_slice;
-  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32) * sizeof(int);
+  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + E + 1) * sizeof(int);
   route_scatter_kernel<<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
-      static_cast<const uint4*>(x), topk_idx, T, H, K, E, R, nblocks, hist,
+      static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
       static_cast<uint4*>(recv), src_map, vec_per_slice);
   return cudaGetLastError();
 }
@@ -331,10 +340,10 @@ cudaError_t launch_dispatch_quant(const void* x, const int64_t* topk_idx, int T,
   hsplit = max(1, min(hsplit, G / 4));
   const int gps = (G + hsplit - 1) / hsplit;
   hsplit = (G + gps - 1) / gps;
-  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32) * sizeof(int) +
+  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + E + 1) * sizeof(int) +
                       kDispatchWarps * gps * sizeof(float);
   route_scatter_fp8_kernel<<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
-      static_cast<const uint4*>(x), topk_idx, T, H, K, E, R, nblocks, hist,
+      static_cast<const uint4*>(x), topk_idx, T, H, K, E, padded_rows(E, R), nblocks, hist, counts,
       reinterpret_cast<uint2*>(xq), xs, src_map, gps);
   return cudaGetLastError();
 }

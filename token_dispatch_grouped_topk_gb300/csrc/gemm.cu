@@ -80,6 +80,8 @@ struct GemmArgs {
   const float* w_scale;  // [E, Ndim/128, nkb]
   int E, R, nkb, n_tiles;
   int I, H;
+  int packed;            // row layout of xq/xs, zq/zs and out (see RowLayout)
+  long long rows;        // their row count
   uint8_t* zq;           // gate/up: [E, R, I]
   float* zs;             // gate/up: [E, R, I/128]
   __nv_bfloat16* out;    // down: [E, R, H]
@@ -96,7 +98,9 @@ struct Control {
   uint32_t tmem_base;
   int abort;
   int tile_start[kMaxExperts + 1];
-  int cnt[kMaxExperts];
+  // Padded layout: clamped count of expert e.  Packed layout: prefix of the
+  // clamped counts (expert e's first row), cnt[E] = their sum.
+  int cnt[kMaxExperts + 1];
   float amax[2][2][kBM];  // [tile parity][column half][row]
 };
 
@@ -111,18 +115,26 @@ struct Layout {
       1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Control) + kOutStage;
 };
 
+// 227 KB of dynamic shared memory per block on sm_103.
+static_assert(Layout<256, true>::kSmem <= 232448 && Layout<256, false>::kSmem <= 232448 &&
+                  Layout<128, false>::kSmem <= 232448,
+              "GEMM shared memory exceeds the per-block limit");
+
 struct Tile {
   int e, m_blk, n_blk, rows;
+  int base;  // buffer row of the tile's first row
 };
 
 // Tile t -> (expert, M block, N slice), M-block major within an expert.
-__device__ __forceinline__ Tile decode_tile(const Control* ctl, int E, int n_tiles, int t) {
+__device__ __forceinline__ Tile decode_tile(const Control* ctl, const GemmArgs& a, int t) {
   Tile r;
-  r.e = find_expert(ctl->tile_start, E, t);
+  r.e = find_expert(ctl->tile_start, a.E, t);
   const int local = t - ctl->tile_start[r.e];
-  r.m_blk = local / n_tiles;
-  r.n_blk = local - r.m_blk * n_tiles;
-  r.rows = min(kBM, ctl->cnt[r.e] - r.m_blk * kBM);
+  r.m_blk = local / a.n_tiles;
+  r.n_blk = local - r.m_blk * a.n_tiles;
+  const int count = a.packed ? ctl->cnt[r.e + 1] - ctl->cnt[r.e] : ctl->cnt[r.e];
+  r.base = (a.packed ? ctl->cnt[r.e] : r.e * a.R) + r.m_blk * kBM;
+  r.rows = min(kBM, count - r.m_blk * kBM);
   return r;
 }
 
@@ -174,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Tile prefix per expert (ends with __syncthreads, which also publishes the
   // barrier initialisation and the TMEM address).
   expert_prefix(args.counts, args.E, args.R, kBM, args.n_tiles, ctl->tile_start, ctl->cnt);
+  if (args.packed) expert_prefix(args.counts, args.E, args.R, 1, 1, ctl->cnt, nullptr);
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const int total = ctl->tile_start[args.E];
@@ -187,8 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile(ctl, args.E, args.n_tiles, t);
-        const int a_row = tl.e * args.R + tl.m_blk * kBM;
+        const Tile tl = decode_tile(ctl, args, t);
+        const int a_row = tl.base;
         int b_row0, b_row1;
         if (kGateUp) {
           b_row0 = tl.e * 2 * args.I + tl.n_blk * 128;
@@ -278,10 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kcount = 0, iter = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++iter) {
-      const Tile tl = decode_tile(ctl, args.E, args.n_tiles, t);
+      const Tile tl = decode_tile(ctl, args, t);
       const int m = tl.m_blk * kBM + row;
-      const bool in_cap = m < args.R;
-      const float* asc = args.a_scale + (static_cast<size_t>(tl.e) * args.R + m) * nkb;
+      const long long grow = static_cast<long long>(tl.base) + row;  // buffer row of this thread
+      // Scales are read for rows inside the expert's capacity (padded) or the
+      // buffer (packed); rows past the count are promoted but never stored.
+      const bool in_cap = args.packed ? grow < args.rows : m < args.R;
+      const float* asc = args.a_scale + (in_cap ? grow : 0) * nkb;
       // gate/up: gate columns [64ch, 64ch+64) and up columns [128+64ch, ..+64);
       // down:    columns [kCols*ch, kCols*ch + kCols), inside one 128-column
       //          weight-scale block.
@@ -348,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++kcount;
       }
       if (!ok) break;
-      const bool valid = row < tl.rows;
+      const bool valid = row < tl.rows && grow < args.rows;
       if (kGateUp) {
         // Z = SiLU(gate) * up on this thread's 64 columns (written over the
         // gate half of acc2), then the row amax over the tile's 128 Z columns
@@ -375,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fp8_group_scale(amax, &mult, &scale);
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(
-              args.zq + (static_cast<size_t>(tl.e) * args.R + m) * args.I + tl.n_blk * 128 + ch * 64);
+              args.zq + grow * args.I + tl.n_blk * 128 + ch * 64);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint32_t w[4];
@@ -391,17 +407,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
           }
           if (ch == 0)
-            args.zs[(static_cast<size_t>(tl.e) * args.R + m) * (args.I / 128) + tl.n_blk] = scale;
+            args.zs[grow * (args.I / 128) + tl.n_blk] = scale;
         }
       } else {
         // BF16 rows through a per-warp shared-memory stage: each round the
         // 32 threads deposit 32 columns of their rows, then the warp writes
         // 8 rows x 64 bytes per store instruction.
         uint8_t* stage = out_stage + ew * kStageWarpBytes;
-        const int row0 = tl.m_blk * kBM + lq * 32;             // first row of this warp
-        const int nvalid = min(32, ctl->cnt[tl.e] - row0);     // rows of this warp to store
-        __nv_bfloat16* gbase = args.out + (static_cast<size_t>(tl.e) * args.R + row0) * args.H +
-                               tl.n_blk * BN + ch * kCols;
+        const long long grow0 = static_cast<long long>(tl.base) + lq * 32;  // warp's first row
+        const int nvalid = static_cast<int>(                   // rows of this warp to store
+            min(static_cast<long long>(min(32, tl.rows - lq * 32)), args.rows - grow0));
+        __nv_bfloat16* gbase = args.out + grow0 * args.H + tl.n_blk * BN + ch * kCols;
         // lane -> (row 8i + lane/4, 16-byte chunk lane%4) of each store instruction i
         const int c = lane & 3;
         const uint32_t goff = static_cast<uint32_t>((lane >> 2) * args.H + 8 * c);
@@ -515,12 +531,13 @@ cudaError_t launch_impl(const CUtensorMap* ta, const CUtensorMap& tb, const Gemm
 }  // namespace
 
 cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
-                               int R, int H, int I, const uint8_t* w13, const float* w13_scale,
-                               uint8_t* zq, float* zs, int32_t* dev_status, int sm_count,
-                               cudaStream_t s) {
+                               RowLayout rl, int H, int I, const uint8_t* w13,
+                               const float* w13_scale, uint8_t* zq, float* zs,
+                               int32_t* dev_status, int sm_count, cudaStream_t s) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
+  const int R = rl.R;
   CUtensorMap ta[3], tb;
-  cudaError_t err = make_activation_maps(ta, xq, H, static_cast<uint64_t>(E) * R);
+  cudaError_t err = make_activation_maps(ta, xq, H, static_cast<uint64_t>(rl.rows));
   if (err == cudaSuccess) err = make_map_u8(&tb, w13, H, static_cast<uint64_t>(E) * 2 * I, kBM);
   if (err != cudaSuccess) return err;
   GemmArgs a{};
@@ -535,16 +552,19 @@ cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t
   a.H = H;
   a.zq = zq;
   a.zs = zs;
+  a.packed = rl.packed;
+  a.rows = rl.rows;
   a.dev_status = dev_status;
   return launch_impl<256, true>(ta, tb, a, sm_count, s);
 }
 
 cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* counts, int E,
-                             int R, int H, int I, const uint8_t* w2, const float* w2_scale,
+                             RowLayout rl, int H, int I, const uint8_t* w2, const float* w2_scale,
                              void* out, int32_t* dev_status, int sm_count, cudaStream_t s) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
+  const int R = rl.R;
   CUtensorMap ta[3], tb;
-  cudaError_t err = make_activation_maps(ta, zq, I, static_cast<uint64_t>(E) * R);
+  cudaError_t err = make_activation_maps(ta, zq, I, static_cast<uint64_t>(rl.rows));
   if (err == cudaSuccess) err = make_map_u8(&tb, w2, I, static_cast<uint64_t>(E) * H, kBM);
   if (err != cudaSuccess) return err;
   GemmArgs a{};
@@ -557,6 +577,8 @@ cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* 
   a.I = I;
   a.H = H;
   a.out = static_cast<__nv_bfloat16*>(out);
+  a.packed = rl.packed;
+  a.rows = rl.rows;
   a.dev_status = dev_status;
   if (H % 256 == 0) {
     a.n_tiles = H / 256;

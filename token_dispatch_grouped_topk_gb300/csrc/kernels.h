@@ -17,6 +17,20 @@ struct DeviceInfo {
 // Cached properties of the current device; nullptr if the query fails.
 const DeviceInfo* current_device_info();
 
+// Where expert e's rows live in the buffers indexed by slot (recv, xq/xs,
+// zq/zs, out): padded, rows [e*R, e*R + R) with capacity rows between
+// experts; packed, rows [base_e, base_e + c_e) with base_e the prefix of the
+// clamped counts c_e = min(counts[e], R), so the valid rows are contiguous
+// ("SGLang Expert Compute Backend", §2.6, compact storage).  `rows` is the
+// row count of those buffers: E*R when padded, at least the largest possible
+// sum of counts when packed.
+struct RowLayout {
+  int R;
+  int packed;
+  int64_t rows;
+};
+inline RowLayout padded_rows(int E, int R) { return RowLayout{R, 0, static_cast<int64_t>(E) * R}; }
+
 // ----- dispatch (route validation, histogram, scan, stable scatter)
 constexpr int kDispatchWarps = 8;
 inline int dispatch_tokens_per_warp(int K) { return 32 / K; }
@@ -26,7 +40,7 @@ inline int dispatch_blocks(int T, int K) {
   return (T + tpb - 1) / tpb;
 }
 cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
-                            int R, void* recv, int32_t* counts, int32_t* src_map,
+                            RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
                             int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s);
 
 // ----- dispatch fused with the per-token FP8 quantisation: xq [E, R, H]
@@ -36,21 +50,21 @@ cudaError_t launch_dispatch_quant(const void* x, const int64_t* topk_idx, int T,
                                   int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s);
 
 // ----- per-token FP8 quantisation of the valid rows; xs is [E, R, H/128]
-cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, int R, int H,
+cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, RowLayout rl, int H,
                             uint8_t* xq, float* xs, int sm_count, cudaStream_t s);
 
 // ----- grouped block-scaled FP8 GEMMs on tcgen05
 cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
-                               int R, int H, int I, const uint8_t* w13, const float* w13_scale,
-                               uint8_t* zq, float* zs, int32_t* dev_status, int sm_count,
-                               cudaStream_t s);
+                               RowLayout rl, int H, int I, const uint8_t* w13,
+                               const float* w13_scale, uint8_t* zq, float* zs,
+                               int32_t* dev_status, int sm_count, cudaStream_t s);
 cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* counts, int E,
-                             int R, int H, int I, const uint8_t* w2, const float* w2_scale,
+                             RowLayout rl, int H, int I, const uint8_t* w2, const float* w2_scale,
                              void* out, int32_t* dev_status, int sm_count, cudaStream_t s);
 
 // ----- weighted combine
-// rows = E * R, the number of rows of `out`; a src_map entry outside
-// [0, rows) is treated like -1.
+// rows = the number of rows of `out` (E * R padded, the buffer's rows packed);
+// a src_map entry outside [0, rows) is treated like -1.
 cudaError_t launch_combine(const void* out, const int32_t* src_map, const float* topk_w, int T,
                            int H, int K, int64_t rows, void* y, int sm_count, cudaStream_t s);
 

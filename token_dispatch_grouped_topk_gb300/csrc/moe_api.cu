@@ -61,9 +61,12 @@ struct ComputeWorkspace {
   size_t xq, xs, zq, zs, total;
 };
 
-ComputeWorkspace compute_workspace(int E, int R, int H, int I) {
+bool valid_rows(int64_t rows) { return rows >= 1 && rows <= (int64_t{1} << 30); }
+
+// FP8 activations and their scales, Z and its scales, for `rows` buffer rows.
+ComputeWorkspace compute_workspace_rows(int64_t rows_i, int H, int I) {
   ComputeWorkspace w{};
-  const size_t rows = static_cast<size_t>(E) * R;
+  const size_t rows = static_cast<size_t>(rows_i);
   size_t off = 0;
   w.xq = off;
   off = align_up(off + rows * H, 256);
@@ -75,6 +78,30 @@ ComputeWorkspace compute_workspace(int E, int R, int H, int I) {
   off = align_up(off + rows * (I / 128) * sizeof(float), 256);
   w.total = off;
   return w;
+}
+ComputeWorkspace compute_workspace(int E, int R, int H, int I) {
+  return compute_workspace_rows(static_cast<int64_t>(E) * R, H, I);
+}
+
+moe_status from_cuda(cudaError_t e);
+
+// The three launches of the expert compute on a carved workspace.
+moe_status expert_compute_impl(const void* recv, const int32_t* counts, int E, RowLayout rl, int H,
+                               int I, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                               const float* w2_scale, void* out, int32_t* dev_status, void* workspace,
+                               const ComputeWorkspace& w, int sm_count, cudaStream_t s) {
+  auto* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* xq = ws + w.xq;
+  float* xs = reinterpret_cast<float*>(ws + w.xs);
+  uint8_t* zq = ws + w.zq;
+  float* zs = reinterpret_cast<float*>(ws + w.zs);
+  cudaError_t err = launch_quantize(recv, counts, E, rl, H, xq, xs, sm_count, s);
+  if (err == cudaSuccess)
+    err = launch_gemm_gateup(xq, xs, counts, E, rl, H, I, w13, w13_scale, zq, zs, dev_status,
+                             sm_count, s);
+  if (err == cudaSuccess)
+    err = launch_gemm_down(zq, zs, counts, E, rl, H, I, w2, w2_scale, out, dev_status, sm_count, s);
+  return from_cuda(err);
 }
 
 moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -121,9 +148,34 @@ moe_status moe_dispatch(const void* x, const int64_t* topk_idx, const float* top
   if (workspace == nullptr || workspace_bytes < need) return MOE_ERR_WORKSPACE;
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
-  return from_cuda(launch_dispatch(x, topk_idx, T, H, K, E, R, recv, counts, src_map, dev_status,
-                                   static_cast<int32_t*>(workspace), dev->sm_count,
+  return from_cuda(launch_dispatch(x, topk_idx, T, H, K, E, padded_rows(E, R), recv, counts, src_map,
+                                   dev_status, static_cast<int32_t*>(workspace), dev->sm_count,
                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch_packed(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
+                               int H, int K, int E, int R, int64_t rows, void* recv,
+                               int32_t* counts, int32_t* src_map, int32_t* dev_status,
+                               void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  (void)topk_w;
+  if (T < 0 || !valid_hidden(H) || !valid_experts(E, R) || K < 1 || K > 32 || K > E)
+    return MOE_ERR_INVALID_ARG;
+  if (counts == nullptr || dev_status == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || topk_idx == nullptr || recv == nullptr || src_map == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(x) || !aligned16(recv))) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * K > (int64_t{1} << 31) - 1) return MOE_ERR_INVALID_ARG;
+  // every kept route must have a row: at most min(T*K, E*R) of them
+  const int64_t need_rows =
+      std::min<int64_t>(static_cast<int64_t>(T) * K, static_cast<int64_t>(E) * R);
+  if (!valid_rows(rows) || rows < need_rows) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_dispatch_workspace_size(T, K, E);
+  if (workspace == nullptr || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_dispatch(x, topk_idx, T, H, K, E, RowLayout{R, 1, rows}, recv, counts,
+                                   src_map, dev_status, static_cast<int32_t*>(workspace),
+                                   dev->sm_count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_dispatch_quant(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
@@ -162,7 +214,7 @@ moe_status moe_quantize_fp8(const void* recv, const int32_t* counts, int E, int 
   if (!aligned16(recv) || (reinterpret_cast<uintptr_t>(xq) & 7u) != 0) return MOE_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
-  return from_cuda(launch_quantize(recv, counts, E, R, H, xq, xs, dev->sm_count,
+  return from_cuda(launch_quantize(recv, counts, E, padded_rows(E, R), H, xq, xs, dev->sm_count,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -176,8 +228,8 @@ moe_status moe_gemm_gateup_silu(const uint8_t* xq, const float* xs, const int32_
   if (!aligned16(xq) || !aligned16(w13) || !aligned16(zq)) return MOE_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
-  return from_cuda(launch_gemm_gateup(xq, xs, counts, E, R, H, I, w13, w13_scale, zq, zs,
-                                      dev_status, dev->sm_count,
+  return from_cuda(launch_gemm_gateup(xq, xs, counts, E, padded_rows(E, R), H, I, w13, w13_scale,
+                                      zq, zs, dev_status, dev->sm_count,
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -191,8 +243,9 @@ moe_status moe_gemm_down(const uint8_t* zq, const float* zs, const int32_t* coun
   if (!aligned16(zq) || !aligned16(w2) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
-  return from_cuda(launch_gemm_down(zq, zs, counts, E, R, H, I, w2, w2_scale, out, dev_status,
-                                    dev->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_gemm_down(zq, zs, counts, E, padded_rows(E, R), H, I, w2, w2_scale, out,
+                                    dev_status, dev->sm_count,
+                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_expert_compute(const void* recv, const int32_t* counts, int E, int R, int H, int I,
@@ -211,20 +264,37 @@ moe_status moe_expert_compute(const void* recv, const int32_t* counts, int E, in
     return MOE_ERR_WORKSPACE;
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
-  auto* ws = static_cast<uint8_t*>(workspace);
-  uint8_t* xq = ws + w.xq;
-  float* xs = reinterpret_cast<float*>(ws + w.xs);
-  uint8_t* zq = ws + w.zq;
-  float* zs = reinterpret_cast<float*>(ws + w.zs);
-  auto s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t err = launch_quantize(recv, counts, E, R, H, xq, xs, dev->sm_count, s);
-  if (err == cudaSuccess)
-    err = launch_gemm_gateup(xq, xs, counts, E, R, H, I, w13, w13_scale, zq, zs, dev_status,
-                             dev->sm_count, s);
-  if (err == cudaSuccess)
-    err = launch_gemm_down(zq, zs, counts, E, R, H, I, w2, w2_scale, out, dev_status,
-                           dev->sm_count, s);
-  return from_cuda(err);
+  return expert_compute_impl(recv, counts, E, padded_rows(E, R), H, I, w13, w13_scale, w2,
+                             w2_scale, out, dev_status, workspace, w, dev->sm_count,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_expert_compute_packed_workspace_size(int64_t rows, int H, int I) {
+  if (!valid_rows(rows) || !valid_hidden(H) || !valid_hidden(I)) return 0;
+  return compute_workspace_rows(rows, H, I).total;
+}
+
+moe_status moe_expert_compute_packed(const void* recv, const int32_t* counts, int E, int R,
+                                     int64_t rows, int H, int I, const uint8_t* w13,
+                                     const float* w13_scale, const uint8_t* w2,
+                                     const float* w2_scale, void* out, int32_t* dev_status,
+                                     void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (!valid_experts(E, R) || !valid_rows(rows) || !valid_hidden(H) || !valid_hidden(I))
+    return MOE_ERR_INVALID_ARG;
+  if (recv == nullptr || counts == nullptr || w13 == nullptr || w13_scale == nullptr ||
+      w2 == nullptr || w2_scale == nullptr || out == nullptr || dev_status == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(recv) || !aligned16(w13) || !aligned16(w2) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  const ComputeWorkspace w = compute_workspace_rows(rows, H, I);
+  if (workspace == nullptr || workspace_bytes < w.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return expert_compute_impl(recv, counts, E, RowLayout{R, 1, rows}, H, I, w13, w13_scale, w2,
+                             w2_scale, out, dev_status, workspace, w, dev->sm_count,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_combine(const void* out, const int32_t* src_map, const float* topk_w, int T, int H,
@@ -238,6 +308,19 @@ moe_status moe_combine(const void* out, const int32_t* src_map, const float* top
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
   return from_cuda(launch_combine(out, src_map, topk_w, T, H, K, static_cast<int64_t>(E) * R, y,
                                   dev->sm_count,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine_packed(const void* out, int64_t rows, const int32_t* src_map,
+                              const float* topk_w, int T, int H, int K, void* y,
+                              moe_stream_t stream) {
+  if (T < 0 || !valid_hidden(H) || !valid_rows(rows) || K < 1 || K > 32) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (out == nullptr || src_map == nullptr || topk_w == nullptr || y == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(out) || !aligned16(y))) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_combine(out, src_map, topk_w, T, H, K, rows, y, dev->sm_count,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -11,7 +11,7 @@
 // grid walks the row blocks; each warp takes whole rows, each half-warp one
 // 128-element group (16 lanes x 8 BF16 = one 16-byte load per lane), so the
 // group amax is a 4-step shuffle reduction.  Scales are staged in shared
-// memory and written row-major ([E, R, H/128], as on the pages), the block's
+// memory and written row-major ([rows, H/128], as on the pages), the block's
 // rows as one contiguous run.
 #include "common.cuh"
 #include "kernels.h"
@@ -26,12 +26,15 @@ constexpr int kRowsPerBlock = 32;
 
 __global__ void __launch_bounds__(kQuantWarps * 32)
     quantize_kernel(const uint4* __restrict__ recv, const int32_t* __restrict__ counts, int E,
-                    int R, int H, uint2* __restrict__ xq, float* __restrict__ xs) {
+                    RowLayout rl, int H, uint2* __restrict__ xq, float* __restrict__ xs) {
   extern __shared__ int smem[];
   int* s_start = smem;               // [E + 1] prefix of row blocks
   int* s_cnt = smem + E + 1;         // [E]
-  float* s_scale = reinterpret_cast<float*>(smem + 2 * E + 1);  // [G][32]
+  int* s_rows = smem + 2 * E + 1;    // [E + 1] packed row bases
+  float* s_scale = reinterpret_cast<float*>(smem + 3 * E + 2);  // [G][32]
+  const int R = rl.R;
   expert_prefix(counts, E, R, kRowsPerBlock, 1, s_start, s_cnt);
+  if (rl.packed) expert_prefix(counts, E, R, 1, 1, s_rows, nullptr);
   const int G = H / kGroup;
   const int nvec = H / 8;
   const int total = s_start[E];
@@ -40,9 +43,13 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   for (int b = blockIdx.x; b < total; b += gridDim.x) {
     const int e = find_expert(s_start, E, b);
     const int row0 = (b - s_start[e]) * kRowsPerBlock;
-    const int nrows = min(kRowsPerBlock, s_cnt[e] - row0);
+    const int64_t base = (rl.packed ? static_cast<int64_t>(s_rows[e]) : static_cast<int64_t>(e) * R) + row0;
+    // rows of the block: valid rows of e, and never past the buffer
+    const int nrows = static_cast<int>(
+        min(static_cast<int64_t>(min(kRowsPerBlock, s_cnt[e] - row0)), rl.rows - base));
+    if (nrows <= 0) continue;
     for (int r = warp; r < nrows; r += kQuantWarps) {
-      const size_t row = static_cast<size_t>(e) * R + row0 + r;
+      const size_t row = static_cast<size_t>(base) + r;
       const uint4* src = recv + row * nvec;
       uint2* dst = xq + row * (H / 8);
       // Four pairs of groups per pass: every lane has four 16-byte loads in
@@ -87,10 +94,10 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
       }
     }
     __syncthreads();
-    // scales are stored [E, R, G]: the block's rows are one contiguous run
+    // scales are stored row-major [rows, G]: the block's rows are one contiguous run
     for (int i = threadIdx.x; i < G * nrows; i += blockDim.x) {
       const int r = i / G, g = i % G;
-      xs[(static_cast<size_t>(e) * R + row0) * G + i] = s_scale[g * kRowsPerBlock + r];
+      xs[static_cast<size_t>(base) * G + i] = s_scale[g * kRowsPerBlock + r];
     }
     __syncthreads();
   }
@@ -98,10 +105,11 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 
 }  // namespace
 
-cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, int R, int H,
+cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, RowLayout rl, int H,
                             uint8_t* xq, float* xs, int sm_count, cudaStream_t s) {
+  const int R = rl.R;
   const int G = H / kGroup;
-  const size_t smem = (2 * E + 1) * sizeof(int) + G * kRowsPerBlock * sizeof(float);
+  const size_t smem = (3 * E + 2) * sizeof(int) + G * kRowsPerBlock * sizeof(float);
   // Upper bound of row blocks; the kernel walks the true count read from device memory.
   const long long max_blocks = static_cast<long long>(E) * ((R + kRowsPerBlock - 1) / kRowsPerBlock);
   const int grid = static_cast<int>(std::min<long long>(max_blocks, sm_count * 8LL));
@@ -111,7 +119,7 @@ cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, int 
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
   }
-  quantize_kernel<<<grid, kQuantWarps * 32, smem, s>>>(static_cast<const uint4*>(recv), counts, E, R,
+  quantize_kernel<<<grid, kQuantWarps * 32, smem, s>>>(static_cast<const uint4*>(recv), counts, E, rl,
                                                         H, reinterpret_cast<uint2*>(xq), xs);
   return cudaGetLastError();
 }
