@@ -376,6 +376,46 @@ def run_ours(args, rank, local, world):
     rows_total = reduce_sum(rows_local, world, dev)
     value = rows_total / (max_ms / 1e3)
 
+    # ---- packed layout (moe_*_packed): the same step with the experts' rows
+    # back to back instead of one capacity block per expert
+    pbuf = api.MoeLayerBuffers(wl.T, E, wl.K, H, I, R, dev, packed=True)
+
+    def packed_step(i):
+        idx, w = routings[i % N_ROUTINGS]
+        pbuf.forward(x, idx, w, w13, s13, w2, s2)
+
+    for i in range(args.warmup):
+        packed_step(i)
+    torch.cuda.synchronize()
+    pgraphs = []
+    for r in range(N_ROUTINGS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            packed_step(r)
+        pgraphs.append(g)
+    for i in range(args.warmup):
+        pgraphs[i % N_ROUTINGS].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    fs.record(stream)
+    for i in range(args.steps):
+        pgraphs[(args.warmup + i) % N_ROUTINGS].replay()
+    fe_.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    packed_ms = reduce_max(fs.elapsed_time(fe_), world, dev)
+
+    def lane_bytes(b):
+        return int(sum(t.numel() * t.element_size()
+                       for t in (b.recv, b.out, b.ws_compute, b.ws_dispatch, b.counts, b.src_map, b.y)))
+
+    packed = {"value": rows_total / (packed_ms / 1e3), "unit": UNIT, "ms_per_step": packed_ms / args.steps,
+              "lane_bytes": lane_bytes(pbuf), "padded_lane_bytes": lane_bytes(buf),
+              "note": "moe_dispatch_packed / moe_expert_compute_packed / moe_combine_packed: the "
+                      "receive-side buffers hold min(T*K, E*R) rows instead of E*R (CUDA-graph replay)"}
+    del pgraphs, pbuf
+    torch.cuda.empty_cache()
+
     # ---- two micro-batches: serial split and overlapped on two streams
     tbo = api.TwoBatchOverlap(wl.T, E, wl.K, H, I, R, dev)
     tbo_steps = max(3, min(args.steps, 20))
@@ -514,6 +554,7 @@ def run_ours(args, rank, local, world):
                 "serial_value": e2e_rows / (e2e_serial_ms / 1e3),
                 "serial_note": "copy in, compute, copy out back to back on one stream"},
         "gpu_launches": 7 * args.steps, "clocks": clk.summary(), "fused": fused, "tbo": tbo_res,
+        "packed": packed,
         "rows_per_step": nv, "dropped_routes_last_routing": dropped, "wl": wl,
     }
 
@@ -563,6 +604,7 @@ def main():
             "kernels": res["kernels"], "roofline": res["roofline"], "e2e": res["e2e"],
             "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
             "fused_dispatch_quant": res["fused"],
+            "packed_layout": res["packed"],
             "two_batch_overlap": res["tbo"],
         }
         sample = cpu_oracle_sample(wl, n_experts=8, rows_per_expert=128)
