@@ -250,6 +250,22 @@ moe_status moe_combine_packed(const void* out, int64_t rows, const int32_t* src_
                               moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_dispatch_ex -- the general dispatch: moe_dispatch and moe_dispatch_packed
+ * are its two common cases.
+ *   topk_idx   device, [T, K] router ids, int32 (idx_bits = 32) or int64
+ *              (idx_bits = 64); -1 marks a padding route, ids outside [-1, E)
+ *              are reported as MOE_DEV_BAD_EXPERT_ID and ignored
+ *   rows       0: padded layout, recv [E, R, H];  > 0: packed layout, recv
+ *              [rows, H] with the conditions of moe_dispatch_packed
+ * Everything else as moe_dispatch.  MOE_ERR_INVALID_ARG for idx_bits other
+ * than 32 or 64.
+ * ------------------------------------------------------------------------- */
+moe_status moe_dispatch_ex(const void* x, const void* topk_idx, int idx_bits, const float* topk_w,
+                           int T, int H, int K, int E, int R, int64_t rows, void* recv,
+                           int32_t* counts, int32_t* src_map, int32_t* dev_status,
+                           void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * moe_selftest_bounded_wait -- exercises the device-side failure path: one
  * thread runs the kernels' bounded mbarrier wait on a barrier that nothing
  * completes; after the wait limit (about 2 s) it sets MOE_DEV_TIMEOUT in

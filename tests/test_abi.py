@@ -122,3 +122,13 @@ def test_packed_entry_points_reject_on_host(lib):
                                          FAKE, FAKE, FAKE, ws82, None) == -1
     assert lib.moe_combine_packed(FAKE, 0, FAKE, FAKE, 4, 256, 2, FAKE, None) == -1
     assert lib.moe_combine_packed(FAKE, 82, FAKE, FAKE, 4, 256, 33, FAKE, None) == -1  # K > 32
+
+
+def test_dispatch_ex_rejects_on_host(lib):
+    ws = 1 << 20
+    args = lambda bits, rows: (FAKE, FAKE, bits, None, 112, 256, 2, 8, 128, rows, FAKE, FAKE, FAKE,
+                               FAKE, FAKE, ws, None)
+    assert lib.moe_dispatch_ex(*args(16, 0)) == -1       # ids are int32 or int64
+    assert lib.moe_dispatch_ex(*args(8, 0)) == -1
+    assert lib.moe_dispatch_ex(*args(32, 100)) == -1     # packed: fewer rows than routes
+    assert lib.moe_dispatch_ex(*args(64, -5)) == -1

@@ -148,3 +148,36 @@ def test_layer_packed_graph_replay_new_routes():
         ref = pad.forward(x, idx, w, *wts)
         torch.cuda.synchronize()
         assert torch.equal(_bits(pk.y), _bits(ref)), f"routing {seed}"
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_int32_ids_match_int64_ids(packed):
+    """moe_dispatch_ex with int32 router ids: the same counts, slots, payload
+    and status as int64 ids, padding routes (-1) and out-of-range ids included."""
+    T, E, K, R, H = 500, 16, 4, 100, 384
+    g = torch.Generator().manual_seed(31)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16).to(DEV)
+    logits = torch.randn(T, E, generator=g)
+    logits[:, :3] += 2.5
+    idx = torch.topk(logits, K, dim=1).indices
+    idx[5, 1] = -1
+    idx[7, 0] = E + 3                                     # bad id
+    idx[9, 2] = -7                                        # bad id
+    w = torch.rand(T, K, generator=g).to(DEV)
+    fn = api.moe_dispatch_packed if packed else api.moe_dispatch
+    r64 = fn(x, idx.to(DEV), w, E, R)
+    r32 = fn(x, idx.to(torch.int32).to(DEV), w, E, R)
+    torch.cuda.synchronize()
+    for a, b in zip(r64[1:], r32[1:]):                    # counts, src_map, status
+        assert torch.equal(a, b)
+    counts = r64[1].cpu().tolist()
+    if packed:
+        total = sum(counts)
+        assert torch.equal(_bits(r64[0][:total]), _bits(r32[0][:total]))
+    else:
+        for e, c in enumerate(counts):                    # capacity rows are never written
+            assert torch.equal(_bits(r64[0][e, :c]), _bits(r32[0][e, :c]))
+    st = r32[3].cpu().tolist()
+    assert st[0] & api.DEV_BAD_EXPERT_ID and st[0] & api.DEV_CAPACITY_DROPPED
+    rr = O.route(idx.numpy(), E, R)
+    assert r32[1].cpu().tolist() == rr.counts.tolist() and st[1] == rr.dropped

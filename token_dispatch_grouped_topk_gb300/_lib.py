@@ -49,6 +49,9 @@ SIGNATURES = {
                                           c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_combine_packed": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_int, c_int, c_int,
                                    c_void_p, c_void_p]),
+    "moe_dispatch_ex": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_int,
+                                c_int, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                c_size_t, c_void_p]),
 }
 
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",

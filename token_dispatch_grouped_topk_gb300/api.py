@@ -60,16 +60,27 @@ def _workspace(nbytes, device):
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
+def _idx_bits(topk_idx):
+    """Router ids may be int64 or int32 (moe_dispatch_ex)."""
+    if topk_idx.dtype == torch.int64:
+        return 64
+    if topk_idx.dtype == torch.int32:
+        return 32
+    raise TypeError(f"topk_idx: expected int64 or int32, got {topk_idx.dtype}")
+
+
 def moe_dispatch(x, topk_idx, topk_w, E: int, R: int, *, recv=None, counts=None, src_map=None,
                  dev_status=None, workspace=None, stream=None):
-    """Top-k dispatch into the expert-major receive buffer.  Returns
-    ``(recv [E,R,H] bf16, counts [E] int32, src_map [T,K] int32, dev_status [2] int32)``."""
+    """Top-k dispatch into the expert-major receive buffer; ``topk_idx`` int64
+    or int32.  Returns ``(recv [E,R,H] bf16, counts [E] int32, src_map [T,K]
+    int32, dev_status [2] int32)``."""
     lib = _lib.load()
     T, H = x.shape
     K = topk_idx.shape[1]
     dev = x.device
     _need(x, torch.bfloat16, "x")
-    _need(topk_idx, torch.int64, "topk_idx")
+    bits = _idx_bits(topk_idx)
+    _need(topk_idx, topk_idx.dtype, "topk_idx")
     if recv is None:
         recv = torch.empty(E, R, H, dtype=torch.bfloat16, device=dev)
     if counts is None:
@@ -80,9 +91,10 @@ def moe_dispatch(x, topk_idx, topk_w, E: int, R: int, *, recv=None, counts=None,
         dev_status = torch.empty(2, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = _workspace(lib.moe_dispatch_workspace_size(T, K, E), dev)
-    st = lib.moe_dispatch(_p(x), _p(topk_idx), _p(topk_w), T, H, K, E, R, _p(recv), _p(counts),
-                          _p(src_map), _p(dev_status), _p(workspace), workspace.numel(), _s(stream))
-    _lib.check("moe_dispatch", st)
+    st = lib.moe_dispatch_ex(_p(x), _p(topk_idx), bits, _p(topk_w), T, H, K, E, R, 0, _p(recv),
+                             _p(counts), _p(src_map), _p(dev_status), _p(workspace),
+                             workspace.numel(), _s(stream))
+    _lib.check("moe_dispatch_ex", st)
     return recv, counts, src_map, dev_status
 
 
@@ -153,7 +165,8 @@ def moe_dispatch_packed(x, topk_idx, topk_w, E: int, R: int, *, rows=None, recv=
     K = topk_idx.shape[1]
     dev = x.device
     _need(x, torch.bfloat16, "x")
-    _need(topk_idx, torch.int64, "topk_idx")
+    bits = _idx_bits(topk_idx)
+    _need(topk_idx, topk_idx.dtype, "topk_idx")
     if rows is None:
         rows = recv.shape[0] if recv is not None else packed_rows(T, K, E, R)
     if recv is None:
@@ -166,10 +179,10 @@ def moe_dispatch_packed(x, topk_idx, topk_w, E: int, R: int, *, rows=None, recv=
         dev_status = torch.empty(2, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = _workspace(lib.moe_dispatch_workspace_size(T, K, E), dev)
-    st = lib.moe_dispatch_packed(_p(x), _p(topk_idx), _p(topk_w), T, H, K, E, R, rows, _p(recv),
-                                 _p(counts), _p(src_map), _p(dev_status), _p(workspace),
-                                 workspace.numel(), _s(stream))
-    _lib.check("moe_dispatch_packed", st)
+    st = lib.moe_dispatch_ex(_p(x), _p(topk_idx), bits, _p(topk_w), T, H, K, E, R, rows, _p(recv),
+                             _p(counts), _p(src_map), _p(dev_status), _p(workspace),
+                             workspace.numel(), _s(stream))
+    _lib.check("moe_dispatch_ex", st)
     return recv, counts, src_map, dev_status
 
 

@@ -30,7 +30,9 @@ struct RouteLane {
   bool active;  // the lane maps to a real route (t < T)
 };
 
-__device__ __forceinline__ RouteLane load_route(const int64_t* __restrict__ topk_idx, int T, int K,
+// Router ids are int64 or int32 (IdT); -1 marks a padding route.
+template <typename IdT>
+__device__ __forceinline__ RouteLane load_route(const IdT* __restrict__ topk_idx, int T, int K,
                                                 int E, int gw, int lane, int32_t* dev_status) {
   const int tpw = 32 / K;
   RouteLane r;
@@ -39,7 +41,7 @@ __device__ __forceinline__ RouteLane load_route(const int64_t* __restrict__ topk
   r.active = (lane < tpw * K) && (r.t < T);
   r.e = -1;
   if (r.active) {
-    const int64_t id = topk_idx[static_cast<int64_t>(r.t) * K + r.k];
+    const int64_t id = static_cast<int64_t>(topk_idx[static_cast<int64_t>(r.t) * K + r.k]);
     if (id >= 0 && id < E) {
       r.e = static_cast<int>(id);
     } else if (id != -1 && dev_status != nullptr) {
@@ -49,8 +51,9 @@ __device__ __forceinline__ RouteLane load_route(const int64_t* __restrict__ topk
   return r;
 }
 
+template <typename IdT>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
-    route_hist_kernel(const int64_t* __restrict__ topk_idx, int T, int K, int E, int nblocks,
+    route_hist_kernel(const IdT* __restrict__ topk_idx, int T, int K, int E, int nblocks,
                       int32_t* __restrict__ hist, int32_t* dev_status) {
   extern __shared__ int s_hist[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
@@ -115,8 +118,9 @@ __global__ void __launch_bounds__(kScanThreads)
   }
 }
 
+template <typename IdT>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
-    route_scatter_kernel(const uint4* __restrict__ x, const int64_t* __restrict__ topk_idx, int T,
+    route_scatter_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx, int T,
                          int H, int K, int E, RowLayout rl, int nblocks,
                          const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
                          uint4* __restrict__ recv, int32_t* __restrict__ src_map,
@@ -184,8 +188,9 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
 // fp32 scales are written to every kept destination row; the BF16 receive
 // buffer is never formed.  Rank derivation is the one of route_scatter_kernel.
 // Each block takes a slice of whole 128-groups of its tokens' rows.
+template <typename IdT>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
-    route_scatter_fp8_kernel(const uint4* __restrict__ x, const int64_t* __restrict__ topk_idx,
+    route_scatter_fp8_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx,
                              int T, int H, int K, int E, RowLayout rl, int nblocks,
                              const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
                              uint2* __restrict__ xq, float* __restrict__ xs,
@@ -285,16 +290,18 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
 
 }  // namespace
 
-cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
-                            RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
-                            int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s) {
+namespace {
+template <typename IdT>
+cudaError_t dispatch_impl(const void* x, const IdT* topk_idx, int T, int H, int K, int E,
+                          RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
+                          int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s) {
   const int R = rl.R;
   cudaError_t err = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
   if (err != cudaSuccess) return err;
   const int nblocks = dispatch_blocks(T, K);
   if (nblocks > 0) {
-    route_hist_kernel<<<nblocks, kDispatchWarps * 32, E * sizeof(int), s>>>(topk_idx, T, K, E,
-                                                                            nblocks, hist, dev_status);
+    route_hist_kernel<IdT><<<nblocks, kDispatchWarps * 32, E * sizeof(int), s>>>(
+        topk_idx, T, K, E, nblocks, hist, dev_status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   route_scan_kernel<<<E, kScanThreads, 0, s>>>(hist, nblocks, R, counts, dev_status);
@@ -309,10 +316,21 @@ cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H
   const int vec_per_slice = (nvec + hsplit - 1) / hsplit;
   hsplit = (nvec + vec_per_slice - 1) / vec_per_slice;
   const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + E + 1) * sizeof(int);
-  route_scatter_kernel<<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
+  route_scatter_kernel<IdT><<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
       static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
       static_cast<uint4*>(recv), src_map, vec_per_slice);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_dispatch(const void* x, const void* topk_idx, int idx_bits, int T, int H, int K,
+                            int E, RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
+                            int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s) {
+  if (idx_bits == 32)
+    return dispatch_impl(x, static_cast<const int32_t*>(topk_idx), T, H, K, E, rl, recv, counts,
+                         src_map, dev_status, hist, sm_count, s);
+  return dispatch_impl(x, static_cast<const int64_t*>(topk_idx), T, H, K, E, rl, recv, counts,
+                       src_map, dev_status, hist, sm_count, s);
 }
 
 }  // namespace moe
@@ -326,8 +344,8 @@ cudaError_t launch_dispatch_quant(const void* x, const int64_t* topk_idx, int T,
   if (err != cudaSuccess) return err;
   const int nblocks = dispatch_blocks(T, K);
   if (nblocks > 0) {
-    route_hist_kernel<<<nblocks, kDispatchWarps * 32, E * sizeof(int), s>>>(topk_idx, T, K, E,
-                                                                            nblocks, hist, dev_status);
+    route_hist_kernel<int64_t><<<nblocks, kDispatchWarps * 32, E * sizeof(int), s>>>(
+        topk_idx, T, K, E, nblocks, hist, dev_status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   route_scan_kernel<<<E, kScanThreads, 0, s>>>(hist, nblocks, R, counts, dev_status);
@@ -342,7 +360,7 @@ cudaError_t launch_dispatch_quant(const void* x, const int64_t* topk_idx, int T,
   hsplit = (G + gps - 1) / gps;
   const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + E + 1) * sizeof(int) +
                       kDispatchWarps * gps * sizeof(float);
-  route_scatter_fp8_kernel<<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
+  route_scatter_fp8_kernel<int64_t><<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
       static_cast<const uint4*>(x), topk_idx, T, H, K, E, padded_rows(E, R), nblocks, hist, counts,
       reinterpret_cast<uint2*>(xq), xs, src_map, gps);
   return cudaGetLastError();

@@ -39,8 +39,9 @@ inline int dispatch_blocks(int T, int K) {
   const int tpb = dispatch_tokens_per_block(K);
   return (T + tpb - 1) / tpb;
 }
-cudaError_t launch_dispatch(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
-                            RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
+// topk_idx holds int64 ids (idx_bits = 64) or int32 ids (idx_bits = 32).
+cudaError_t launch_dispatch(const void* x, const void* topk_idx, int idx_bits, int T, int H, int K,
+                            int E, RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
                             int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s);
 
 // ----- dispatch fused with the per-token FP8 quantisation: xq [E, R, H]

@@ -132,50 +132,51 @@ size_t moe_dispatch_workspace_size(int T, int K, int E) {
   return align_up(std::max<size_t>(nb * E * sizeof(int32_t), 1), 256);
 }
 
-moe_status moe_dispatch(const void* x, const int64_t* topk_idx, const float* topk_w, int T, int H,
-                        int K, int E, int R, void* recv, int32_t* counts, int32_t* src_map,
-                        int32_t* dev_status, void* workspace, size_t workspace_bytes,
-                        moe_stream_t stream) {
+moe_status moe_dispatch_ex(const void* x, const void* topk_idx, int idx_bits, const float* topk_w,
+                           int T, int H, int K, int E, int R, int64_t rows, void* recv,
+                           int32_t* counts, int32_t* src_map, int32_t* dev_status,
+                           void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   (void)topk_w;  // router weights stay at the source; combine reads them
   if (T < 0 || !valid_hidden(H) || !valid_experts(E, R) || K < 1 || K > 32 || K > E)
     return MOE_ERR_INVALID_ARG;
+  if (idx_bits != 32 && idx_bits != 64) return MOE_ERR_INVALID_ARG;
   if (counts == nullptr || dev_status == nullptr) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (x == nullptr || topk_idx == nullptr || recv == nullptr || src_map == nullptr))
     return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!aligned16(x) || !aligned16(recv))) return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(T) * K > (int64_t{1} << 31) - 1) return MOE_ERR_INVALID_ARG;
+  RowLayout rl = padded_rows(E, R);
+  if (rows != 0) {
+    // packed: every kept route must have a row, at most min(T*K, E*R) of them
+    const int64_t need_rows =
+        std::min<int64_t>(static_cast<int64_t>(T) * K, static_cast<int64_t>(E) * R);
+    if (!valid_rows(rows) || rows < need_rows) return MOE_ERR_INVALID_ARG;
+    rl = RowLayout{R, 1, rows};
+  }
   const size_t need = moe_dispatch_workspace_size(T, K, E);
   if (workspace == nullptr || workspace_bytes < need) return MOE_ERR_WORKSPACE;
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
-  return from_cuda(launch_dispatch(x, topk_idx, T, H, K, E, padded_rows(E, R), recv, counts, src_map,
+  return from_cuda(launch_dispatch(x, topk_idx, idx_bits, T, H, K, E, rl, recv, counts, src_map,
                                    dev_status, static_cast<int32_t*>(workspace), dev->sm_count,
                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch(const void* x, const int64_t* topk_idx, const float* topk_w, int T, int H,
+                        int K, int E, int R, void* recv, int32_t* counts, int32_t* src_map,
+                        int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                        moe_stream_t stream) {
+  return moe_dispatch_ex(x, topk_idx, 64, topk_w, T, H, K, E, R, 0, recv, counts, src_map,
+                         dev_status, workspace, workspace_bytes, stream);
 }
 
 moe_status moe_dispatch_packed(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
                                int H, int K, int E, int R, int64_t rows, void* recv,
                                int32_t* counts, int32_t* src_map, int32_t* dev_status,
                                void* workspace, size_t workspace_bytes, moe_stream_t stream) {
-  (void)topk_w;
-  if (T < 0 || !valid_hidden(H) || !valid_experts(E, R) || K < 1 || K > 32 || K > E)
-    return MOE_ERR_INVALID_ARG;
-  if (counts == nullptr || dev_status == nullptr) return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (x == nullptr || topk_idx == nullptr || recv == nullptr || src_map == nullptr))
-    return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!aligned16(x) || !aligned16(recv))) return MOE_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(T) * K > (int64_t{1} << 31) - 1) return MOE_ERR_INVALID_ARG;
-  // every kept route must have a row: at most min(T*K, E*R) of them
-  const int64_t need_rows =
-      std::min<int64_t>(static_cast<int64_t>(T) * K, static_cast<int64_t>(E) * R);
-  if (!valid_rows(rows) || rows < need_rows) return MOE_ERR_INVALID_ARG;
-  const size_t need = moe_dispatch_workspace_size(T, K, E);
-  if (workspace == nullptr || workspace_bytes < need) return MOE_ERR_WORKSPACE;
-  const DeviceInfo* dev = nullptr;
-  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
-  return from_cuda(launch_dispatch(x, topk_idx, T, H, K, E, RowLayout{R, 1, rows}, recv, counts,
-                                   src_map, dev_status, static_cast<int32_t*>(workspace),
-                                   dev->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+  if (rows == 0) return MOE_ERR_INVALID_ARG;
+  return moe_dispatch_ex(x, topk_idx, 64, topk_w, T, H, K, E, R, rows, recv, counts, src_map,
+                         dev_status, workspace, workspace_bytes, stream);
 }
 
 moe_status moe_dispatch_quant(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
