@@ -266,6 +266,28 @@ moe_status moe_dispatch_ex(const void* x, const void* topk_idx, int idx_bits, co
                            void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_expert_compute_ex -- the general expert compute: moe_expert_compute and
+ * moe_expert_compute_packed are its flags = 0 cases.
+ *   rows   0: padded layout, recv/out [E, R, H];  > 0: packed layout [rows, H]
+ *   flags  MOE_W13_INTERLEAVED: W13 output rows alternate gate and up (row 2j
+ *          is gate feature j, row 2j+1 up feature j; the scale blocks are the
+ *          128x128 blocks of this layout): the expert of "XTuner Domino EP"
+ *          (section on the complete runtime path), whose SiLU takes the even
+ *          output columns of the first GEMM and multiplies by the odd ones.
+ *          Default: the first I rows gate, the last I up ("SGLang Expert
+ *          Compute Backend", §3.6).
+ * Workspace: moe_expert_compute_ex_workspace_size(E, R, rows, H, I) bytes.
+ * MOE_ERR_INVALID_ARG for unknown flag bits.
+ * ------------------------------------------------------------------------- */
+#define MOE_W13_INTERLEAVED 1
+size_t moe_expert_compute_ex_workspace_size(int E, int R, int64_t rows, int H, int I);
+moe_status moe_expert_compute_ex(const void* recv, const int32_t* counts, int E, int R, int64_t rows,
+                                 int H, int I, const uint8_t* w13, const float* w13_scale,
+                                 const uint8_t* w2, const float* w2_scale, void* out,
+                                 int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                 int flags, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * moe_selftest_bounded_wait -- exercises the device-side failure path: one
  * thread runs the kernels' bounded mbarrier wait on a barrier that nothing
  * completes; after the wait limit (about 2 s) it sets MOE_DEV_TIMEOUT in

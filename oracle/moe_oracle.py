@@ -312,18 +312,23 @@ def silu(g: np.ndarray) -> np.ndarray:
         return g / (1.0 + np.exp(-g))
 
 
-def expert_forward(xq, sx, w13q, s13, w2q, s2):
+def expert_forward(xq, sx, w13q, s13, w2q, s2, interleaved: bool = False):
     """One expert on its valid rows.
 
     "SGLang Expert Compute Backend", §1.1: X[m,H] -> gate/up GEMM [m, 2I] ->
     SiLU(gate) * up [m, I] -> down GEMM [m, H]; §3.6: the first I columns are
     gate and the last I are up, and the down input is re-quantised per row per
-    128 like the activations.  G and Z are fp64; Z is taken to fp32 before the
-    fp32 quantisation rule.  Returns ``(out, zq, sz, G)``.
+    128 like the activations.  With ``interleaved`` the gate/up weight rows
+    alternate instead ("XTuner Domino EP", complete runtime path: SiLU of the
+    even output columns times the odd ones).  G and Z are fp64; Z is taken to
+    fp32 before the fp32 quantisation rule.  Returns ``(out, zq, sz, G)``.
     """
     I = w13q.shape[0] // 2
     G = gemm_block_scaled(xq, sx, w13q, s13)
-    Z = silu(G[:, :I]) * G[:, I:]
+    if interleaved:
+        Z = silu(G[:, 0::2]) * G[:, 1::2]
+    else:
+        Z = silu(G[:, :I]) * G[:, I:]
     zq, sz = quantize_rows(Z.astype(np.float32))
     out = gemm_block_scaled(zq, sz, w2q, s2)
     return out, zq, sz, G

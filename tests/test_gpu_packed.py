@@ -181,3 +181,63 @@ def test_int32_ids_match_int64_ids(packed):
     assert st[0] & api.DEV_BAD_EXPERT_ID and st[0] & api.DEV_CAPACITY_DROPPED
     rr = O.route(idx.numpy(), E, R)
     assert r32[1].cpu().tolist() == rr.counts.tolist() and st[1] == rr.dropped
+
+
+# ------------------------------------------------ interleaved gate/up weights
+
+def _unit_scale_weights(E, H, I, seed):
+    """e4m3 codes of both signs (no NaN codes) and one scale for every block,
+    so the standard and interleaved layouts describe the same expert."""
+    g = torch.Generator().manual_seed(seed)
+    def codes(*shape):
+        c = torch.randint(0, 256, shape, generator=g, dtype=torch.int32).to(torch.uint8)
+        c[(c & 0x7F) == 0x7F] = 0
+        return c
+    w13, w2 = codes(E, 2 * I, H), codes(E, H, I)
+    s13 = torch.full((E, 2 * I // 128, H // 128), 1e-3)
+    s2 = torch.full((E, H // 128, I // 128), 2e-3)
+    return w13, s13, w2, s2
+
+
+@pytest.mark.parametrize("packed", [False, True])
+@pytest.mark.parametrize("shape", [(112, 8, 2, 256, 128, 128), (600, 16, 4, 512, 384, 256)])
+def test_interleaved_w13_bit_identical_to_standard(packed, shape):
+    """Uniform block scales: interleaving W13's rows (2j gate, 2j+1 up) and
+    flagging MOE_W13_INTERLEAVED gives the standard layer's bytes."""
+    T, E, K, H, I, R = shape
+    w13, s13, w2, s2 = _unit_scale_weights(E, H, I, seed=41)
+    inter = torch.empty_like(w13)
+    inter[:, 0::2], inter[:, 1::2] = w13[:, :I], w13[:, I:]
+    dev = torch.device(DEV)
+    g = torch.Generator().manual_seed(42)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16).to(DEV)
+    idx = torch.topk(torch.randn(T, E, generator=g), K, dim=1).indices.to(DEV)
+    w = torch.rand(T, K, generator=g).to(DEV)
+    std = api.MoeLayerBuffers(T, E, K, H, I, R, dev, packed=packed)
+    itl = api.MoeLayerBuffers(T, E, K, H, I, R, dev, packed=packed, w13_interleaved=True)
+    args = (x, idx, w)
+    y_std = std.forward(*args, w13.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV)).clone()
+    y_itl = itl.forward(*args, inter.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV)).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y_itl), _bits(y_std))
+    assert float(y_std.float().abs().max()) > 0
+
+
+def test_interleaved_w13_matches_oracle():
+    """Block-scaled interleaved weights (each 128x128 block of the interleaved
+    layout with its own scale) against the oracle's interleaved expert."""
+    E, R, H, I = 3, 256, 512, 256
+    counts = [200, 70, 13]
+    g = torch.Generator().manual_seed(43)
+    recv = torch.randn(E, R, H, generator=g).to(torch.bfloat16)
+    w13, s13, w2, s2 = W.expert_weights(E, H, I, 44, "cpu")   # read as interleaved rows
+    cd = torch.tensor(counts, dtype=torch.int32, device=DEV)
+    out = api.moe_expert_compute(recv.to(DEV), cd, w13.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV),
+                                 w13_interleaved=True)
+    torch.cuda.synchronize()
+    from helpers import assert_rows_close, f32, u8
+    for e, c in enumerate(counts):
+        xq, sx = O.quantize_rows(f32(recv[e, :c]))
+        ref, _, _, _ = O.expert_forward(xq, sx, u8(w13[e]), f32(s13[e]), u8(w2[e]), f32(s2[e]),
+                                        interleaved=True)
+        assert_rows_close(f32(out[e, :c]), ref, what=f"expert {e}")

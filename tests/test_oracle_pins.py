@@ -583,3 +583,30 @@ def test_packed_src_map_is_order_preserving_bijection():
             rows = sorted(int(pp) for q, pp in zip(r.src_map.flatten(), p.flatten()) if q >= 0 and q // R == e)
             assert rows == [start + s for s in slots]
             start += int(r.counts[e])
+
+
+def test_interleaved_gateup_is_a_row_permutation():
+    """With one scale for every weight block, interleaving the gate/up rows
+    (row 2j gate j, row 2j+1 up j) must give exactly the standard expert: the
+    same products and sums with G's columns permuted."""
+    rng = np.random.default_rng(12)
+    m, H, I = 5, 256, 256
+    def codes(*shape):   # signed e4m3 codes of both signs, NaN codes (0x7F, 0xFF) excluded
+        c = rng.integers(0, 256, size=shape, dtype=np.uint8)
+        c[(c & 0x7F) == 0x7F] = 0
+        return c
+    xq, w13, w2 = codes(m, H), codes(2 * I, H), codes(H, I)
+    sx = rng.uniform(0.5, 2.0, size=(m, H // 128)).astype(np.float32) * 1e-3
+    s13 = np.full((2 * I // 128, H // 128), 1e-3, np.float32)
+    s2 = np.full((H // 128, I // 128), 2e-3, np.float32)
+    inter = np.empty_like(w13)
+    inter[0::2], inter[1::2] = w13[:I], w13[I:]
+    out_std, zq_std, sz_std, _ = O.expert_forward(xq, sx, w13, s13, w2, s2)
+    out_int, zq_int, sz_int, _ = O.expert_forward(xq, sx, inter, s13, w2, s2, interleaved=True)
+    assert np.array_equal(zq_std, zq_int) and np.array_equal(sz_std, sz_int)
+    assert np.array_equal(out_std, out_int)
+    # reading the halves the other way round (up first) is not the same expert
+    swapped = np.empty_like(w13)
+    swapped[0::2], swapped[1::2] = w13[I:], w13[:I]
+    out_bad, _, _, _ = O.expert_forward(xq, sx, swapped, s13, w2, s2, interleaved=True)
+    assert not np.array_equal(out_bad, out_std)

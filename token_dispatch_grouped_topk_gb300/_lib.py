@@ -52,7 +52,12 @@ SIGNATURES = {
     "moe_dispatch_ex": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_int,
                                 c_int, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                 c_size_t, c_void_p]),
+    "moe_expert_compute_ex_workspace_size": (c_size_t, [c_int, c_int, c_int64, c_int, c_int]),
+    "moe_expert_compute_ex": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int64, c_int, c_int,
+                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                      c_void_p, c_size_t, c_int, c_void_p]),
 }
+W13_INTERLEAVED = 1
 
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
           -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA"}

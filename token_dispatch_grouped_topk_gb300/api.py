@@ -128,9 +128,10 @@ def moe_dispatch_quant(x, topk_idx, topk_w, E: int, R: int, *, xq=None, xs=None,
 
 
 def moe_expert_compute(recv, counts, w13, w13_scale, w2, w2_scale, *, out=None, dev_status=None,
-                       workspace=None, stream=None):
+                       workspace=None, stream=None, w13_interleaved=False):
     """Quantise the valid rows and run the grouped gated-SiLU FP8 expert MLP.
-    Returns ``out [E,R,H] bf16`` (rows past counts[e] untouched)."""
+    Returns ``out [E,R,H] bf16`` (rows past counts[e] untouched).  With
+    ``w13_interleaved`` the W13 rows alternate gate and up (moe_expert_compute_ex)."""
     lib = _lib.load()
     E, R, H = recv.shape
     w13, w2 = _u8(w13), _u8(w2)
@@ -142,10 +143,11 @@ def moe_expert_compute(recv, counts, w13, w13_scale, w2, w2_scale, *, out=None, 
         dev_status = torch.zeros(2, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = _workspace(lib.moe_expert_compute_workspace_size(E, R, H, I), dev)
-    st = lib.moe_expert_compute(_p(recv), _p(counts), E, R, H, I, _p(w13), _p(w13_scale), _p(w2),
-                                _p(w2_scale), _p(out), _p(dev_status), _p(workspace),
-                                workspace.numel(), _s(stream))
-    _lib.check("moe_expert_compute", st)
+    st = lib.moe_expert_compute_ex(_p(recv), _p(counts), E, R, 0, H, I, _p(w13), _p(w13_scale),
+                                   _p(w2), _p(w2_scale), _p(out), _p(dev_status), _p(workspace),
+                                   workspace.numel(), _lib.W13_INTERLEAVED if w13_interleaved else 0,
+                                   _s(stream))
+    _lib.check("moe_expert_compute_ex", st)
     return out
 
 
@@ -187,7 +189,7 @@ def moe_dispatch_packed(x, topk_idx, topk_w, E: int, R: int, *, rows=None, recv=
 
 
 def moe_expert_compute_packed(recv, counts, R: int, w13, w13_scale, w2, w2_scale, *, out=None,
-                              dev_status=None, workspace=None, stream=None):
+                              dev_status=None, workspace=None, stream=None, w13_interleaved=False):
     """``moe_expert_compute`` on the packed layout: recv and out are [rows, H]."""
     lib = _lib.load()
     rows, H = recv.shape
@@ -201,10 +203,11 @@ def moe_expert_compute_packed(recv, counts, R: int, w13, w13_scale, w2, w2_scale
         dev_status = torch.zeros(2, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = _workspace(lib.moe_expert_compute_packed_workspace_size(rows, H, I), dev)
-    st = lib.moe_expert_compute_packed(_p(recv), _p(counts), E, R, rows, H, I, _p(w13),
-                                       _p(w13_scale), _p(w2), _p(w2_scale), _p(out),
-                                       _p(dev_status), _p(workspace), workspace.numel(), _s(stream))
-    _lib.check("moe_expert_compute_packed", st)
+    st = lib.moe_expert_compute_ex(_p(recv), _p(counts), E, R, rows, H, I, _p(w13), _p(w13_scale),
+                                   _p(w2), _p(w2_scale), _p(out), _p(dev_status), _p(workspace),
+                                   workspace.numel(), _lib.W13_INTERLEAVED if w13_interleaved else 0,
+                                   _s(stream))
+    _lib.check("moe_expert_compute_ex", st)
     return out
 
 
@@ -299,6 +302,7 @@ class MoeLayerBuffers:
     R: int
     device: torch.device
     packed: bool = False   # packed layout (moe_*_packed): [rows, H] buffers, no capacity gaps
+    w13_interleaved: bool = False   # W13 rows alternate gate and up
 
     def __post_init__(self):
         d, E, R, H, I, T, K = self.device, self.E, self.R, self.H, self.I, self.T, self.K
@@ -365,14 +369,16 @@ class MoeLayerBuffers:
                                 stream=stream)
             moe_expert_compute_packed(self.recv, self.counts, self.R, w13, w13_scale, w2,
                                       w2_scale, out=self.out, dev_status=self.dev_status,
-                                      workspace=self.ws_compute, stream=stream)
+                                      workspace=self.ws_compute, stream=stream,
+                                      w13_interleaved=self.w13_interleaved)
             moe_combine_packed(self.out, self.src_map, topk_w, y=y, stream=stream)
             return y
         moe_dispatch(x, topk_idx, topk_w, self.E, self.R, recv=self.recv, counts=self.counts,
                      src_map=self.src_map, dev_status=self.dev_status, workspace=self.ws_dispatch,
                      stream=stream)
         moe_expert_compute(self.recv, self.counts, w13, w13_scale, w2, w2_scale, out=self.out,
-                           dev_status=self.dev_status, workspace=self.ws_compute, stream=stream)
+                           dev_status=self.dev_status, workspace=self.ws_compute, stream=stream,
+                           w13_interleaved=self.w13_interleaved)
         moe_combine(self.out, self.src_map, topk_w, y=y, stream=stream)
         return y
 

@@ -81,6 +81,8 @@ struct GemmArgs {
   int E, R, nkb, n_tiles;
   int I, H;
   int packed;            // row layout of xq/xs, zq/zs and out (see RowLayout)
+  int inter;             // gate/up: W13 rows interleaved (2j gate, 2j+1 up) instead of
+                         // the first I gate and the last I up
   long long rows;        // their row count
   uint8_t* zq;           // gate/up: [E, R, I]
   float* zs;             // gate/up: [E, R, I/128]
@@ -203,7 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Tile tl = decode_tile(ctl, args, t);
         const int a_row = tl.base;
         int b_row0, b_row1;
-        if (kGateUp) {
+        if (kGateUp && args.inter) {         // 256 consecutive interleaved rows
+          b_row0 = tl.e * 2 * args.I + tl.n_blk * 256;
+          b_row1 = b_row0 + 128;
+        } else if (kGateUp) {
           b_row0 = tl.e * 2 * args.I + tl.n_blk * 128;
           b_row1 = b_row0 + args.I;
         } else {
@@ -301,17 +306,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       // gate/up: gate columns [64ch, 64ch+64) and up columns [128+64ch, ..+64);
       // down:    columns [kCols*ch, kCols*ch + kCols), inside one 128-column
       //          weight-scale block.
+      //          Interleaved gate/up: columns [128ch, 128ch+128), 64 (gate, up)
+      //          pairs inside one 128-row weight-scale block.
       const float* wsc0;
       const float* wsc1;
-      if (kGateUp) {
+      uint32_t col0, col1;  // TMEM columns of this thread's two 64-column chunks
+      if (kGateUp && args.inter) {
+        const int nb = 2 * args.I / 128;
+        wsc0 = args.w_scale + (static_cast<size_t>(tl.e) * nb + 2 * tl.n_blk + ch) * nkb;
+        wsc1 = wsc0;
+        col0 = static_cast<uint32_t>(ch * 128);
+        col1 = col0 + 64;
+      } else if (kGateUp) {
         const int nb = 2 * args.I / 128;
         wsc0 = args.w_scale + (static_cast<size_t>(tl.e) * nb + tl.n_blk) * nkb;
         wsc1 = args.w_scale + (static_cast<size_t>(tl.e) * nb + args.I / 128 + tl.n_blk) * nkb;
+        col0 = static_cast<uint32_t>(ch * 64);
+        col1 = col0 + 128;
       } else {
         const int nb = args.H / 128;
         const int cb = (tl.n_blk * BN + ch * kCols) / 128;
         wsc0 = args.w_scale + (static_cast<size_t>(tl.e) * nb + cb) * nkb;
         wsc1 = wsc0;
+        col0 = static_cast<uint32_t>(ch * kCols);
+        col1 = col0 + 64;
       }
       uint64_t acc2[kPairs];
 #pragma unroll
@@ -351,8 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t buf[64];
 #pragma unroll
         for (int j = 0; j < kCols / 64; ++j) {
-          const uint32_t col = kGateUp ? static_cast<uint32_t>((j ? 128 : 0) + ch * 64)
-                                       : static_cast<uint32_t>(ch * kCols + 64 * j);
+          const uint32_t col = j ? col1 : col0;
           const uint64_t sx2 = (kGateUp && j) ? s1x2 : s0x2;
           tmem_load64_sync(base + col, buf);
 #pragma unroll
@@ -370,14 +387,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // gate half of acc2), then the row amax over the tile's 128 Z columns
         // shared with the partner warp holding the other half.
         float amax = 0.f;
+        if (args.inter) {
+          // pair p holds (gate, up) of feature 64ch + p; Z of features 2i and
+          // 2i+1 go to acc2[i] (written after both pairs are read)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float g0 = f32x2_lo(acc2[i]), g1 = f32x2_hi(acc2[i]);
-          const float u0 = f32x2_lo(acc2[32 + i]), u1 = f32x2_hi(acc2[32 + i]);
-          const float z0 = (g0 / (1.0f + expf(-g0))) * u0;
-          const float z1 = (g1 / (1.0f + expf(-g1))) * u1;
-          acc2[i] = f32x2_pack(z0, z1);
-          amax = fmaxf(amax, fmaxf(fabsf(z0), fabsf(z1)));
+          for (int i = 0; i < 32; ++i) {
+            const float g0 = f32x2_lo(acc2[2 * i]), u0 = f32x2_hi(acc2[2 * i]);
+            const float g1 = f32x2_lo(acc2[2 * i + 1]), u1 = f32x2_hi(acc2[2 * i + 1]);
+            const float z0 = (g0 / (1.0f + expf(-g0))) * u0;
+            const float z1 = (g1 / (1.0f + expf(-g1))) * u1;
+            acc2[i] = f32x2_pack(z0, z1);
+            amax = fmaxf(amax, fmaxf(fabsf(z0), fabsf(z1)));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float g0 = f32x2_lo(acc2[i]), g1 = f32x2_hi(acc2[i]);
+            const float u0 = f32x2_lo(acc2[32 + i]), u1 = f32x2_hi(acc2[32 + i]);
+            const float z0 = (g0 / (1.0f + expf(-g0))) * u0;
+            const float z1 = (g1 / (1.0f + expf(-g1))) * u1;
+            acc2[i] = f32x2_pack(z0, z1);
+            amax = fmaxf(amax, fmaxf(fabsf(z0), fabsf(z1)));
+          }
         }
         const int par = iter & 1;
         ctl->amax[par][ch][row] = amax;
@@ -533,7 +564,8 @@ cudaError_t launch_impl(const CUtensorMap* ta, const CUtensorMap& tb, const Gemm
 cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
                                RowLayout rl, int H, int I, const uint8_t* w13,
                                const float* w13_scale, uint8_t* zq, float* zs,
-                               int32_t* dev_status, int sm_count, cudaStream_t s) {
+                               int32_t* dev_status, int sm_count, cudaStream_t s,
+                               int w13_interleaved) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
   const int R = rl.R;
   CUtensorMap ta[3], tb;
@@ -552,6 +584,7 @@ cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t
   a.H = H;
   a.zq = zq;
   a.zs = zs;
+  a.inter = w13_interleaved ? 1 : 0;
   a.packed = rl.packed;
   a.rows = rl.rows;
   a.dev_status = dev_status;

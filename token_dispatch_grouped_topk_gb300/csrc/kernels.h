@@ -55,10 +55,13 @@ cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, RowL
                             uint8_t* xq, float* xs, int sm_count, cudaStream_t s);
 
 // ----- grouped block-scaled FP8 GEMMs on tcgen05
+// w13_interleaved: W13 output rows alternate gate and up (2j gate, 2j+1 up)
+// instead of the first I rows gate and the last I up.
 cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
                                RowLayout rl, int H, int I, const uint8_t* w13,
                                const float* w13_scale, uint8_t* zq, float* zs,
-                               int32_t* dev_status, int sm_count, cudaStream_t s);
+                               int32_t* dev_status, int sm_count, cudaStream_t s,
+                               int w13_interleaved = 0);
 cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* counts, int E,
                              RowLayout rl, int H, int I, const uint8_t* w2, const float* w2_scale,
                              void* out, int32_t* dev_status, int sm_count, cudaStream_t s);

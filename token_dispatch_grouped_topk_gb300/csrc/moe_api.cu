@@ -89,7 +89,8 @@ moe_status from_cuda(cudaError_t e);
 moe_status expert_compute_impl(const void* recv, const int32_t* counts, int E, RowLayout rl, int H,
                                int I, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
                                const float* w2_scale, void* out, int32_t* dev_status, void* workspace,
-                               const ComputeWorkspace& w, int sm_count, cudaStream_t s) {
+                               const ComputeWorkspace& w, int sm_count, cudaStream_t s,
+                               int flags = 0) {
   auto* ws = static_cast<uint8_t*>(workspace);
   uint8_t* xq = ws + w.xq;
   float* xs = reinterpret_cast<float*>(ws + w.xs);
@@ -98,7 +99,7 @@ moe_status expert_compute_impl(const void* recv, const int32_t* counts, int E, R
   cudaError_t err = launch_quantize(recv, counts, E, rl, H, xq, xs, sm_count, s);
   if (err == cudaSuccess)
     err = launch_gemm_gateup(xq, xs, counts, E, rl, H, I, w13, w13_scale, zq, zs, dev_status,
-                             sm_count, s);
+                             sm_count, s, (flags & MOE_W13_INTERLEAVED) ? 1 : 0);
   if (err == cudaSuccess)
     err = launch_gemm_down(zq, zs, counts, E, rl, H, I, w2, w2_scale, out, dev_status, sm_count, s);
   return from_cuda(err);
@@ -296,6 +297,36 @@ moe_status moe_expert_compute_packed(const void* recv, const int32_t* counts, in
   return expert_compute_impl(recv, counts, E, RowLayout{R, 1, rows}, H, I, w13, w13_scale, w2,
                              w2_scale, out, dev_status, workspace, w, dev->sm_count,
                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_expert_compute_ex_workspace_size(int E, int R, int64_t rows, int H, int I) {
+  if (rows == 0) return moe_expert_compute_workspace_size(E, R, H, I);
+  return moe_expert_compute_packed_workspace_size(rows, H, I);
+}
+
+moe_status moe_expert_compute_ex(const void* recv, const int32_t* counts, int E, int R, int64_t rows,
+                                 int H, int I, const uint8_t* w13, const float* w13_scale,
+                                 const uint8_t* w2, const float* w2_scale, void* out,
+                                 int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                 int flags, moe_stream_t stream) {
+  if (!valid_experts(E, R) || !valid_hidden(H) || !valid_hidden(I)) return MOE_ERR_INVALID_ARG;
+  if ((flags & ~MOE_W13_INTERLEAVED) != 0) return MOE_ERR_INVALID_ARG;
+  if (rows != 0 && !valid_rows(rows)) return MOE_ERR_INVALID_ARG;
+  if (recv == nullptr || counts == nullptr || w13 == nullptr || w13_scale == nullptr ||
+      w2 == nullptr || w2_scale == nullptr || out == nullptr || dev_status == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(recv) || !aligned16(w13) || !aligned16(w2) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  const RowLayout rl = rows == 0 ? padded_rows(E, R) : RowLayout{R, 1, rows};
+  const ComputeWorkspace w = compute_workspace_rows(rl.rows, H, I);
+  if (workspace == nullptr || workspace_bytes < w.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return expert_compute_impl(recv, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, out,
+                             dev_status, workspace, w, dev->sm_count,
+                             reinterpret_cast<cudaStream_t>(stream), flags);
 }
 
 moe_status moe_combine(const void* out, const int32_t* src_map, const float* topk_w, int T, int H,
