@@ -213,6 +213,37 @@ moe_status moe_gemm_down(const uint8_t* zq, const float* zs, const int32_t* coun
                          int32_t* dev_status, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_gemm_gateup_down -- moe_gemm_gateup_silu followed by moe_gemm_down, in
+ * one persistent launch.  The arithmetic is that of "SGLang Expert Compute
+ * Backend", §3.5-3.7.  The scheduling applies the tile events of "XTuner
+ * Domino EP" (HyperParallel-MoE section, from whole collectives to
+ * destination tile events): a task waits on a per-tile counter reaching its
+ * threshold rather than on the whole preceding operator.  Here a down tile of
+ * a 128-row block starts once every gate/up tile of that block has written
+ * its Z rows.  Results are bit-identical to the two calls.
+ *
+ *   xq, xs     as for moe_gemm_gateup_silu, in the layout given by rows:
+ *              rows = 0 padded [E, R, ...], rows > 0 packed [rows, ...]
+ *              (see "Packed layout" below)
+ *   zq, zs     device scratch for Z, [E, R, I] / [E, R, I/128] or [rows, ...]
+ *   out        device BF16, [E, R, H] or [rows, H]; valid rows only
+ *   sync       device scratch of moe_gemm_gateup_down_sync_size(E, R, rows)
+ *              bytes, 4-byte aligned, overwritten (zeroed) by the call;
+ *              not shared with another call in flight
+ *   flags      0 or MOE_W13_INTERLEAVED (see moe_expert_compute_ex)
+ * Returns MOE_ERR_INVALID_ARG for bad sizes, pointers or flags,
+ * MOE_ERR_WORKSPACE if sync is too small.  Waits between tiles are bounded:
+ * one that runs out raises MOE_DEV_TIMEOUT in dev_status.  moe_expert_compute
+ * and its variants run this launch after their quantisation.
+ * ------------------------------------------------------------------------- */
+size_t moe_gemm_gateup_down_sync_size(int E, int R, int64_t rows);
+moe_status moe_gemm_gateup_down(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
+                                int R, int64_t rows, int H, int I, const uint8_t* w13,
+                                const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                uint8_t* zq, float* zs, void* out, int32_t* dev_status, void* sync,
+                                size_t sync_bytes, int flags, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Packed layout -- "SGLang Expert Compute Backend", §2.6 (compact storage):
  * the valid rows of all experts are stored back to back, expert e's rows at
  * [base_e, base_e + c_e) with c_e = min(counts[e], R) and base_e the sum of

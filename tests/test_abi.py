@@ -51,7 +51,11 @@ def test_workspace_sizes(lib):
     # one int32 per (expert, block of 8 warps x 32/K tokens)
     assert lib.moe_dispatch_workspace_size(16384, 8, 256) == 256 * (16384 // 32) * 4
     ws = lib.moe_expert_compute_workspace_size(2, 128, 256, 128)
-    assert ws == 2 * 128 * 256 + 2 * 2 * 128 * 4 + 2 * 128 * 128 + 2 * 1 * 128 * 4
+    # xq, xs, zq, zs, then the fused GEMM's scratch: a tile ticket and one
+    # count per 128-row block (ceil(rows/128) plus one per possible expert)
+    sync = (1 + 2 + 1024) * 4
+    assert ws == 2 * 128 * 256 + 2 * 2 * 128 * 4 + 2 * 128 * 128 + 2 * 1 * 128 * 4 + \
+        (sync + 255) // 256 * 256
     assert lib.moe_expert_compute_workspace_size(2, 128, 200, 128) == 0   # H % 128 != 0
 
 
@@ -112,7 +116,8 @@ def test_packed_entry_points_reject_on_host(lib):
     # packed compute: workspace sized by rows (xq, xs, zq, zs, each 256-byte aligned)
     al = lambda v: (v + 255) // 256 * 256
     ws82 = lib.moe_expert_compute_packed_workspace_size(82, 256, 128)
-    assert ws82 == al(al(al(al(82 * 256) + 82 * 2 * 4) + 82 * 128) + 82 * 1 * 4)
+    assert ws82 == al(al(al(al(al(82 * 256) + 82 * 2 * 4) + 82 * 128) + 82 * 1 * 4) +
+                      (1 + 1 + 1024) * 4)
     assert lib.moe_expert_compute_packed_workspace_size(2 * 128, 256, 128) == \
         lib.moe_expert_compute_workspace_size(2, 128, 256, 128)
     assert lib.moe_expert_compute_packed_workspace_size(0, 256, 128) == 0
@@ -132,3 +137,29 @@ def test_dispatch_ex_rejects_on_host(lib):
     assert lib.moe_dispatch_ex(*args(8, 0)) == -1
     assert lib.moe_dispatch_ex(*args(32, 100)) == -1     # packed: fewer rows than routes
     assert lib.moe_dispatch_ex(*args(64, -5)) == -1
+
+
+def test_gemm_gateup_down_sync_size_and_rejections(lib):
+    """The fused GEMM launch's scratch: a tile ticket plus one completion count
+    per 128-row block, bounded by E*ceil(R/128) (padded) and additionally by
+    ceil(rows/128) + E (packed, one partial block per expert)."""
+    sz = lib.moe_gemm_gateup_down_sync_size
+    assert sz(2, 128, 0) == (1 + 2) * 4
+    assert sz(4, 1000, 0) == (1 + 4 * 8) * 4
+    assert sz(4, 1000, 300) == (1 + 3 + 4) * 4
+    assert sz(256, 4096, 131072) == (1 + 1024 + 256) * 4
+    assert sz(0, 128, 0) == 0 and sz(2, 128, -5) == 0
+    args = lambda **k: [k.get(n, d) for n, d in (
+        ("xq", FAKE), ("xs", FAKE), ("counts", FAKE), ("E", 2), ("R", 128), ("rows", 0),
+        ("H", 256), ("I", 128), ("w13", FAKE), ("s13", FAKE), ("w2", FAKE), ("s2", FAKE),
+        ("zq", FAKE), ("zs", FAKE), ("out", FAKE), ("st", FAKE), ("sync", FAKE),
+        ("sync_bytes", 12), ("flags", 0), ("stream", None))]
+    f = lib.moe_gemm_gateup_down
+    assert f(*args(sync_bytes=11)) == -3                  # one int short
+    assert f(*args(sync=None)) == -3
+    assert f(*args(sync=ctypes.c_void_p(4096 + 2))) == -3  # counts are 4-byte words
+    assert f(*args(H=200)) == -1
+    assert f(*args(flags=2)) == -1                        # unknown flag bit
+    assert f(*args(rows=-1)) == -1
+    assert f(*args(out=None)) == -1
+    assert f(*args(zq=ctypes.c_void_p(4096 + 8))) == -1   # TMA source must be 16-byte aligned

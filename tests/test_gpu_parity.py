@@ -224,21 +224,69 @@ def test_expert_compute_capacity_not_multiple_of_tile():
 
 
 @pytest.mark.parametrize("H", [512, 384])
-def test_expert_compute_narrow_tile_boundaries(H):
-    """Blocks of 1..64 valid rows run with swapped operands (weights on M,
-    tokens on N), 65..128 as wide tiles: both sides of each boundary, alone
-    and after full blocks, with 256-wide (H=512) and 128-wide (H=384) down
-    tiles."""
+def test_expert_compute_activation_box_boundaries(H):
+    """Blocks of 1..32, 33..64 and 65..128 valid rows fetch 32-, 64- and
+    128-row activation boxes: both sides of each boundary, alone and after
+    full blocks, with 256-wide (H=512) and 128-wide (H=384) down tiles."""
     counts = [1, 31, 32, 33, 63, 64, 65, 127, 129, 192, 193, 256, 0]
     _check_expert_compute(len(counts), 256, H, 256, counts, seed=11)
 
 
 @pytest.mark.parametrize("H", [512, 384])
-def test_expert_compute_all_narrow(H):
-    """No expert above 64 rows: every tile is narrow, several per CTA, with
-    K groups rotating through both accumulator buffers."""
+def test_expert_compute_short_blocks_only(H):
+    """No expert above 64 rows: every tile fetches a short activation box,
+    several tiles per CTA, with K groups rotating through both accumulator
+    buffers."""
     counts = [1, 64, 33, 0, 17, 64, 2, 40, 63, 5, 64, 31]
     _check_expert_compute(len(counts), 64, H, 512, counts, seed=12)
+
+
+@pytest.mark.parametrize("E,R,H,I,seed", [(5, 384, 512, 256, 21), (48, 256, 1024, 512, 22),
+                                          (3, 256, 384, 256, 23), (1, 1024, 256, 1024, 24)])
+def test_gemm_gateup_down_matches_stage_calls(E, R, H, I, seed):
+    """Both GEMMs in one launch (down tiles of a block start once that block's
+    gate/up tiles are done) against the two stage launches: Z codes, Z scales
+    and out bit-identical on the valid rows, capacity rows of out untouched;
+    three launches in a row reuse one scratch (each resets it); the packed
+    layout on the same rows gives the same rows.  H = 384 takes the two-launch
+    form (128-wide down tiles)."""
+    g = torch.Generator().manual_seed(seed)
+    counts = torch.randint(0, R + 1, (E,), generator=g)
+    counts[0] = R
+    if E > 2:
+        counts[1] = 0
+    recv, w13, s13, w2, s2 = _expert_setup(E, R, H, I, counts.tolist(), seed)
+    cd = counts.to(torch.int32).to(DEV)
+    w13, s13, w2, s2 = (t.to(DEV) for t in (w13, s13, w2, s2))
+    xq, xs = api.moe_quantize_fp8(recv.to(DEV), cd)
+    zq1, zs1 = api.moe_gemm_gateup_silu(xq, xs, cd, w13, s13)
+    out1 = api.moe_gemm_down(zq1, zs1, cd, w2, s2)
+    sentinel = torch.full((E, R, H), 3.0, dtype=torch.bfloat16, device=DEV)
+    zq2 = torch.zeros_like(zq1)
+    zs2 = torch.zeros_like(zs1)
+    sync = torch.empty(max(256, api._lib.load().moe_gemm_gateup_down_sync_size(E, R, 0)),
+                       dtype=torch.uint8, device=DEV)
+    st = torch.zeros(2, dtype=torch.int32, device=DEV)
+    outs = []
+    for _ in range(3):
+        outs.append(api.moe_gemm_gateup_down(xq, xs, cd, w13, s13, w2, s2, zq=zq2, zs=zs2,
+                                             out=sentinel.clone(), sync=sync, dev_status=st))
+    torch.cuda.synchronize()
+    assert st.cpu().tolist() == [0, 0]
+    valid = torch.arange(R).unsqueeze(0) < counts.unsqueeze(1)          # [E, R]
+    vd = valid.to(DEV)
+    assert torch.equal(zq1[vd], zq2[vd]) and torch.equal(zs1[vd], zs2[vd])
+    for out2 in outs:
+        assert torch.equal(out1[vd].view(torch.int16), out2[vd].view(torch.int16))
+        assert bool((out2[~vd] == 3.0).all()), "capacity rows of out were written"
+    # packed layout: the valid rows back to back
+    xq_p, xs_p = xq[vd].contiguous(), xs[vd].contiguous()
+    rows = xq_p.shape[0]
+    if rows > 0:
+        out_p = api.moe_gemm_gateup_down(xq_p, xs_p, cd, w13, s13, w2, s2, R=R, dev_status=st)
+        torch.cuda.synchronize()
+        assert st.cpu().tolist() == [0, 0]
+        assert torch.equal(out_p.view(torch.int16), out1[vd].view(torch.int16))
 
 
 # ------------------------------------------------------------------ combine

@@ -56,6 +56,11 @@ SIGNATURES = {
     "moe_expert_compute_ex": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int64, c_int, c_int,
                                       c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                       c_void_p, c_size_t, c_int, c_void_p]),
+    "moe_gemm_gateup_down_sync_size": (c_size_t, [c_int, c_int, c_int64]),
+    "moe_gemm_gateup_down": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int64, c_int,
+                                     c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_int,
+                                     c_void_p]),
 }
 W13_INTERLEAVED = 1
 

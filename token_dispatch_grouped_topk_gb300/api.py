@@ -16,7 +16,8 @@ __all__ = [
     "MoeError", "dispatch_workspace_size", "expert_compute_workspace_size", "moe_dispatch",
     "moe_dispatch_quant",
     "moe_expert_compute", "moe_combine", "moe_quantize_fp8", "moe_gemm_gateup_silu",
-    "moe_gemm_down", "moe_dispatch_packed", "moe_expert_compute_packed", "moe_combine_packed",
+    "moe_gemm_down", "moe_gemm_gateup_down", "moe_dispatch_packed", "moe_expert_compute_packed",
+    "moe_combine_packed",
     "packed_rows", "MoeLayerBuffers", "HostPipeline", "TwoBatchOverlap", "DEV_BAD_EXPERT_ID",
     "DEV_CAPACITY_DROPPED", "DEV_TIMEOUT",
 ]
@@ -286,6 +287,44 @@ def moe_gemm_down(zq, zs, counts, w2, w2_scale, *, out=None, dev_status=None, st
     return out
 
 
+def moe_gemm_gateup_down(xq, xs, counts, w13, w13_scale, w2, w2_scale, *, R=None, zq=None,
+                         zs=None, out=None, sync=None, dev_status=None, stream=None,
+                         w13_interleaved=False):
+    """Both GEMMs in one launch (down tiles start per 128-row block as soon as
+    that block's Z is written); bit-identical to ``moe_gemm_gateup_silu`` then
+    ``moe_gemm_down``.  ``xq [E,R,H]`` is the padded layout; ``xq [rows,H]``
+    with ``R`` given is the packed one.  Returns ``out``."""
+    lib = _lib.load()
+    w13, w2 = _u8(w13), _u8(w2)
+    E = counts.shape[0]
+    I = w13.shape[1] // 2
+    dev = xq.device
+    if xq.dim() == 3:
+        E, R, H = xq.shape
+        rows, lead = 0, (E, R)
+    else:
+        if R is None:
+            raise ValueError("the packed layout needs R")
+        rows, H = xq.shape
+        lead = (rows,)
+    if zq is None:
+        zq = torch.empty(*lead, I, dtype=torch.uint8, device=dev)
+    if zs is None:
+        zs = torch.empty(*lead, I // 128, dtype=torch.float32, device=dev)
+    if out is None:
+        out = torch.empty(*lead, H, dtype=torch.bfloat16, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(2, dtype=torch.int32, device=dev)
+    if sync is None:
+        sync = _workspace(lib.moe_gemm_gateup_down_sync_size(E, R, rows), dev)
+    st = lib.moe_gemm_gateup_down(_p(_u8(xq)), _p(xs), _p(counts), E, R, rows, H, I, _p(w13),
+                                  _p(w13_scale), _p(w2), _p(w2_scale), _p(zq), _p(zs), _p(out),
+                                  _p(dev_status), _p(sync), sync.numel() * sync.element_size(),
+                                  _lib.W13_INTERLEAVED if w13_interleaved else 0, _s(stream))
+    _lib.check("moe_gemm_gateup_down", st)
+    return out
+
+
 @dataclass
 class MoeLayerBuffers:
     """One resource set ("lane") for a routed MoE layer: every buffer the three
@@ -341,9 +380,17 @@ class MoeLayerBuffers:
         zs = ws[o3:o3 + n * GI * 4].view(torch.float32).view(*lead, GI)
         return xq, xs, zq, zs
 
+    def sync_view(self):
+        """The fused GEMM launch's scratch inside the expert compute workspace
+        (a tile ticket and one count per 128-row block)."""
+        n, GI = self.rows, self.I // 128
+        al = lambda v: (v + 255) // 256 * 256
+        o4 = al(al(al(al(n * self.H) + n * (self.H // 128) * 4) + n * self.I) + n * GI * 4)
+        return self.ws_compute[o4:o4 + (1 + (n + 127) // 128 + 1024) * 4]
+
     def forward_fused(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None):
         """The same layer with dispatch and quantisation fused (moe_dispatch_quant
-        -> gate/up GEMM -> down GEMM -> combine); the BF16 receive buffer is not
+        -> both GEMMs in one launch -> combine); the BF16 receive buffer is not
         used.  Returns ``y`` (bit-identical to ``forward``).  Padded lanes only."""
         if self.packed:
             raise ValueError("forward_fused runs on the padded layout")
@@ -351,10 +398,9 @@ class MoeLayerBuffers:
         moe_dispatch_quant(x, topk_idx, topk_w, self.E, self.R, xq=xq, xs=xs, counts=self.counts,
                            src_map=self.src_map, dev_status=self.dev_status,
                            workspace=self.ws_dispatch, stream=stream)
-        moe_gemm_gateup_silu(xq, xs, self.counts, w13, w13_scale, zq=zq, zs=zs,
-                             dev_status=self.dev_status, stream=stream)
-        moe_gemm_down(zq, zs, self.counts, w2, w2_scale, out=self.out, dev_status=self.dev_status,
-                      stream=stream)
+        moe_gemm_gateup_down(xq, xs, self.counts, w13, w13_scale, w2, w2_scale, zq=zq, zs=zs,
+                             out=self.out, sync=self.sync_view(), dev_status=self.dev_status,
+                             stream=stream, w13_interleaved=self.w13_interleaved)
         moe_combine(self.out, self.src_map, topk_w, y=self.y, stream=stream)
         return self.y
 

@@ -32,12 +32,25 @@
 //    in flight for eight warps to drain 128x256 fp32 per K group in time) and
 //    updated with packed two-lane fp32 FMAs.  The
 //    register file is re-split per warpgroup (setmaxnreg): the producer/MMA
-//    warpgroup drops to 40 (24) registers, the two epilogue warpgroups rise to
-//    232 (240) in the gate/up (down) GEMM.
+//    warpgroup drops to 40 registers, the two epilogue warpgroups rise to 232.
 //    After the last K group they run the fused epilogue: SiLU(gate) * up and
 //    the per-row FP8 requantisation of Z for the gate/up GEMM; for the down
 //    GEMM BF16 rows staged through shared memory so each store instruction
 //    writes 64-byte row segments.  Only rows below counts[e] are stored.
+//  - one kernel serves three launch forms: the gate/up GEMM alone, the down
+//    GEMM alone, or both ("XTuner Domino EP", HyperParallel-MoE section: a
+//    task starts when the per-tile event counter it depends on reaches its
+//    threshold, not when the whole preceding operator ends).  In the fused
+//    form the tile list is every gate/up tile followed by every down tile;
+//    the producer takes tiles in list order from a global ticket, so a tile
+//    only ever waits for tiles already held by running CTAs, and passes each
+//    to the MMA and epilogue warps through a small shared-memory ring.  Each
+//    epilogue warp of a gate/up tile, after storing its 32 rows x 64 columns
+//    of Z, adds one to its block's count (release); a down tile of that block
+//    waits (acquire, bounded) until the count reaches 8 x the gate/up tiles
+//    per block before its producer loads Z with TMA and its epilogue reads
+//    Z's scales.  The down GEMM of the first blocks so runs under the last
+//    gate/up wave instead of after it.
 // Every wait is bounded; on expiry the kernel raises MOE_DEV_TIMEOUT in the
 // status word, drains its own copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -57,17 +70,21 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+// What one launch computes: the gate/up GEMM, the down GEMM, or both, with
+// each down tile starting once the gate/up tiles of its 128-row block are done.
+constexpr int kModeGateUp = 0;
+constexpr int kModeDown = 1;
+constexpr int kModeFused = 2;
+// Fused launches hand tiles from the producer to the MMA and epilogue warps
+// through a ring of this many slots.
+constexpr int kTileSlots = 8;
 // Register split: launched at kLaunchRegs per thread (the __launch_bounds__
-// maximum for 384 threads); warpgroup 0 gives back to CtrlRegs, warpgroups 1-2
-// take EpiRegs, with 4*32*CtrlRegs + 8*32*EpiRegs == 12*32*kLaunchRegs.  The
-// down GEMM's epilogue holds more live state, so it takes a larger share.
+// maximum for 384 threads); warpgroup 0 (producer, MMA, TMEM owner) gives
+// back to kCtrlRegs, warpgroups 1-2 (epilogue) take kEpiRegs.
 constexpr int kLaunchRegs = 168;
-template <bool kGateUp>
-struct RegSplit {
-  static constexpr int kCtrl = kGateUp ? 40 : 24;
-  static constexpr int kEpi = kGateUp ? 232 : 240;
-  static_assert(4 * kCtrl + 8 * kEpi == 12 * kLaunchRegs, "register split must fit the launch");
-};
+constexpr int kCtrlRegs = 40;
+constexpr int kEpiRegs = 232;
+static_assert(4 * kCtrlRegs + 8 * kEpiRegs == 12 * kLaunchRegs, "register split must fit the launch");
 // Down-GEMM output staging: per epilogue warp 32 rows x 32 BF16 columns, rows
 // padded to 80 bytes.
 constexpr int kStageRowBytes = 80;
@@ -76,18 +93,27 @@ constexpr int kMaxExperts = 1024;
 
 struct GemmArgs {
   const int32_t* counts;
-  const float* a_scale;  // [E, R, nkb], one row's scales contiguous
-  const float* w_scale;  // [E, Ndim/128, nkb]
-  int E, R, nkb, n_tiles;
-  int I, H;
-  int packed;            // row layout of xq/xs, zq/zs and out (see RowLayout)
-  int inter;             // gate/up: W13 rows interleaved (2j gate, 2j+1 up) instead of
-                         // the first I gate and the last I up
-  long long rows;        // their row count
-  uint8_t* zq;           // gate/up: [E, R, I]
-  float* zs;             // gate/up: [E, R, I/128]
-  __nv_bfloat16* out;    // down: [E, R, H]
+  const float* xs;         // [rows, H/128]: scales of the gate/up GEMM's activations
+  const float* w13_scale;  // [E, 2I/128, H/128]
+  const float* w2_scale;   // [E, H/128, I/128]
+  uint8_t* zq;             // [rows, I]: written by gate/up tiles, read by down tiles
+  float* zs;               // [rows, I/128]
+  __nv_bfloat16* out;      // [rows, H]
+  int* sched;              // fused: [0] tile ticket, [1 + b] epilogue warps done on block b
+  int E, R, I, H;
+  int nt_gu, nt_dn;        // N slices per 128-row block of each GEMM
+  int packed;              // row layout of xq/xs, zq/zs and out (see RowLayout)
+  int inter;               // W13 rows interleaved (2j gate, 2j+1 up) instead of the
+                           // first I gate and the last I up
+  long long rows;          // their row count
   int32_t* dev_status;
+};
+
+// Tensor maps: activation boxes of 128, 64 and 32 rows and the weights, for
+// the gate/up GEMM ([0]: xq, W13) and the down GEMM ([1]: zq, W2).
+struct GemmMaps {
+  CUtensorMap a[2][3];
+  CUtensorMap b[2];
 };
 
 struct Control {
@@ -95,45 +121,59 @@ struct Control {
   uint64_t empty[kStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t tile_full[kTileSlots];
+  uint64_t tile_empty[kTileSlots];
   uint64_t drain;
   uint64_t amax_bar;
   uint32_t tmem_base;
   int abort;
-  int tile_start[kMaxExperts + 1];
+  int tile_slot[kTileSlots];
+  int blk_start[kMaxExperts + 1];  // prefix of ceil(count / 128): expert e's first block
   // Padded layout: clamped count of expert e.  Packed layout: prefix of the
   // clamped counts (expert e's first row), cnt[E] = their sum.
   int cnt[kMaxExperts + 1];
   float amax[2][2][kBM];  // [tile parity][column half][row]
 };
 
-template <int BN, bool kGateUp>
+template <int BN, int kMode>
 struct Layout {
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kOutStage = kGateUp ? 0 : kEpiWarps * kStageWarpBytes;
+  static constexpr int kOutStage = kMode == kModeGateUp ? 0 : kEpiWarps * kStageWarpBytes;
   static constexpr size_t kSmem =
       1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Control) + kOutStage;
 };
 
 // 227 KB of dynamic shared memory per block on sm_103.
-static_assert(Layout<256, true>::kSmem <= 232448 && Layout<256, false>::kSmem <= 232448 &&
-                  Layout<128, false>::kSmem <= 232448,
+static_assert(Layout<256, kModeGateUp>::kSmem <= 232448 &&
+                  Layout<256, kModeDown>::kSmem <= 232448 &&
+                  Layout<128, kModeDown>::kSmem <= 232448 &&
+                  Layout<256, kModeFused>::kSmem <= 232448,
               "GEMM shared memory exceeds the per-block limit");
 
 struct Tile {
+  bool gu;   // a gate/up tile (else a down tile)
+  int blk;   // 128-row block over all experts
   int e, m_blk, n_blk, rows;
   int base;  // buffer row of the tile's first row
 };
 
-// Tile t -> (expert, M block, N slice), M-block major within an expert.
+// Tile t -> (GEMM, block, expert, N slice).  Each GEMM's tiles are M-block
+// major (the N slices of one block adjacent); a fused launch lists all gate/up
+// tiles before all down tiles.
+template <int kMode>
 __device__ __forceinline__ Tile decode_tile(const Control* ctl, const GemmArgs& a, int t) {
   Tile r;
-  r.e = find_expert(ctl->tile_start, a.E, t);
-  const int local = t - ctl->tile_start[r.e];
-  r.m_blk = local / a.n_tiles;
-  r.n_blk = local - r.m_blk * a.n_tiles;
+  const int gu_tiles = kMode == kModeFused ? ctl->blk_start[a.E] * a.nt_gu : 0;
+  r.gu = kMode == kModeGateUp || (kMode == kModeFused && t < gu_tiles);
+  const int local = r.gu ? t : t - gu_tiles;
+  const int nt = r.gu ? a.nt_gu : a.nt_dn;
+  r.blk = local / nt;
+  r.n_blk = local - r.blk * nt;
+  r.e = find_expert(ctl->blk_start, a.E, r.blk);
+  r.m_blk = r.blk - ctl->blk_start[r.e];
   const int count = a.packed ? ctl->cnt[r.e + 1] - ctl->cnt[r.e] : ctl->cnt[r.e];
   r.base = (a.packed ? ctl->cnt[r.e] : r.e * a.R) + r.m_blk * kBM;
   r.rows = min(kBM, count - r.m_blk * kBM);
@@ -146,13 +186,41 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   mbar_wait(bar, parity, &dummy);
 }
 
-template <int BN, bool kGateUp>
+// Generic-proxy writes of Z (epilogue stores) and async-proxy reads of Z (the
+// down tiles' TMA loads) are ordered on both sides with a proxy fence.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void red_add_release_gpu(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Waits until *p >= target (another CTA's release); false once `abort` is set
+// or after kWaitLimitNs.
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(128);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+// Scales written by this launch (Z's, in a fused launch) are read through L2.
+__device__ __forceinline__ float ld_scale(const float* p, bool coherent) {
+  return coherent ? __ldcg(p) : __ldg(p);
+}
+
+template <int BN, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmA64,
-                        const __grid_constant__ CUtensorMap tmA32,
-                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
-  using L = Layout<BN, kGateUp>;
+    grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
+  using L = Layout<BN, kMode>;
+  constexpr bool kFused = kMode == kModeFused;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -169,52 +237,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->tfull[i], 1);
       mbar_init(&ctl->tempty[i], kEpiThreads / 32);
     }
+    for (int i = 0; i < kTileSlots; ++i) {
+      mbar_init(&ctl->tile_full[i], 1);
+      mbar_init(&ctl->tile_empty[i], 1 + kEpiWarps);   // the MMA thread + each epilogue warp
+    }
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->amax_bar, kEpiThreads);
     ctl->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmA64);
-    tma_prefetch_desc(&tmA32);
-    tma_prefetch_desc(&tmB);
+  if (warp == 0 && lane < 4) {
+    const int g = kMode == kModeDown ? 1 : 0;
+    tma_prefetch_desc(lane < 3 ? &maps.a[g][lane] : &maps.b[g]);
+    if (kFused) tma_prefetch_desc(lane < 3 ? &maps.a[1][lane] : &maps.b[1]);
   }
   if (warp == 2) {
     tmem_alloc(&ctl->tmem_base, L::kTmemCols);
     tmem_relinquish();
     tc_fence_before();
   }
-  // Tile prefix per expert (ends with __syncthreads, which also publishes the
+  // Block prefix per expert (ends with __syncthreads, which also publishes the
   // barrier initialisation and the TMEM address).
-  expert_prefix(args.counts, args.E, args.R, kBM, args.n_tiles, ctl->tile_start, ctl->cnt);
+  expert_prefix(args.counts, args.E, args.R, kBM, 1, ctl->blk_start, ctl->cnt);
   if (args.packed) expert_prefix(args.counts, args.E, args.R, 1, 1, ctl->cnt, nullptr);
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int total = ctl->tile_start[args.E];
+  const int nblk = ctl->blk_start[args.E];
+  const int total = nblk * ((kMode == kModeDown ? 0 : args.nt_gu) +
+                            (kMode == kModeGateUp ? 0 : args.nt_dn));
+  const int done_target = kEpiWarps * args.nt_gu;   // fused: signals that complete a block's Z
   volatile int* abort_flag = &ctl->abort;
-  const int nkb = args.nkb;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    warpgroup_reg_dealloc<RegSplit<kGateUp>::kCtrl>();
+    warpgroup_reg_dealloc<kCtrlRegs>();
     if (lane == 0) {
       int issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile(ctl, args, t);
+      for (int it = 0;; ++it) {
+        int t;
+        if (kFused) {
+          // Tiles are taken in list order by whichever CTAs are running, so
+          // every gate/up tile a down tile waits for is held by a running CTA
+          // that never waits on anything else first.
+          const int slot = it % kTileSlots;
+          if (!mbar_wait(&ctl->tile_empty[slot], ((it / kTileSlots) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          t = atomicAdd(args.sched, 1);
+          if (t >= total) t = -1;
+          ctl->tile_slot[slot] = t;
+          mbar_arrive(&ctl->tile_full[slot]);
+        } else {
+          t = blockIdx.x + it * gridDim.x;
+          if (t >= total) t = -1;
+        }
+        if (t < 0) break;
+        const Tile tl = decode_tile<kMode>(ctl, args, t);
+        if (kFused && !tl.gu) {
+          if (!wait_count(args.sched + 1 + tl.blk, done_target, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        const int g = tl.gu ? 0 : 1;
+        const int nkb = (tl.gu ? args.H : args.I) / kBK;
         const int a_row = tl.base;
         int b_row0, b_row1;
-        if (kGateUp && args.inter) {         // 256 consecutive interleaved rows
+        if (tl.gu && args.inter) {         // 256 consecutive interleaved rows
           b_row0 = tl.e * 2 * args.I + tl.n_blk * 256;
           b_row1 = b_row0 + 128;
-        } else if (kGateUp) {
+        } else if (tl.gu) {
           b_row0 = tl.e * 2 * args.I + tl.n_blk * 128;
           b_row1 = b_row0 + args.I;
         } else {
           b_row0 = tl.e * args.H + tl.n_blk * BN;
           b_row1 = b_row0 + 128;
         }
+        // Only the tile's valid activation rows are fetched (32, 64 or 128):
+        // the rest of the A tile keeps stale bytes, which reach only output
+        // rows that are never stored.
+        const int a_box = tl.rows <= 32 ? 32 : (tl.rows <= 64 ? 64 : kBM);
+        const CUtensorMap* ma = &maps.a[g][a_box == kBM ? 0 : (a_box == 64 ? 1 : 2)];
+        const CUtensorMap* mb = &maps.b[g];
         for (int kb = 0; kb < nkb; ++kb) {
           const int stage = issued % kStages;
           const uint32_t phase = (issued / kStages) & 1;
@@ -224,17 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + stage * L::kStageBytes;
           uint8_t* sb = sa + L::kABytes;
-          // Only the tile's valid activation rows are fetched (32, 64 or 128):
-          // the rest of the A tile keeps stale bytes, which reach only output
-          // rows that are never stored.
-          const int a_box = tl.rows <= 32 ? 32 : (tl.rows <= 64 ? 64 : kBM);
           mbar_arrive_expect_tx(&ctl->full[stage], L::kBBytes + a_box * kBK);
-          tma_load_2d(sa, a_box == kBM ? &tmA : (a_box == 64 ? &tmA64 : &tmA32), &ctl->full[stage],
-                      kb * kBK, a_row);
-          tma_load_2d(sb, &tmB, &ctl->full[stage], kb * kBK, b_row0);
-          if (BN == 256) tma_load_2d(sb + 128 * kBK, &tmB, &ctl->full[stage], kb * kBK, b_row1);
+          tma_load_2d(sa, ma, &ctl->full[stage], kb * kBK, a_row);
+          tma_load_2d(sb, mb, &ctl->full[stage], kb * kBK, b_row0);
+          if (BN == 256) tma_load_2d(sb + 128 * kBK, mb, &ctl->full[stage], kb * kBK, b_row1);
           ++issued;
         }
+        if (!ok) break;
       }
       if (!ok) *abort_flag = 1;
       // No copy may land after the block exits: wait for the last loads.
@@ -245,12 +348,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
-    warpgroup_reg_dealloc<RegSplit<kGateUp>::kCtrl>();
+    warpgroup_reg_dealloc<kCtrlRegs>();
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_e4m3_f32(kBM, BN);
       int consumed = 0, kcount = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int it = 0; ok; ++it) {
+        int t;
+        if (kFused) {
+          const int slot = it % kTileSlots;
+          if (!mbar_wait(&ctl->tile_full[slot], (it / kTileSlots) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          t = ctl->tile_slot[slot];
+          mbar_arrive(&ctl->tile_empty[slot]);
+        } else {
+          t = blockIdx.x + it * gridDim.x;
+          if (t >= total) t = -1;
+        }
+        if (t < 0) break;
+        const int gu_tiles = kFused ? nblk * args.nt_gu : 0;
+        const bool gu = kMode == kModeGateUp || (kFused && t < gu_tiles);
+        const int nkb = (gu ? args.H : args.I) / kBK;
         for (int kb = 0; kb < nkb; ++kb) {
           const int stage = consumed % kStages;
           const uint32_t phase = (consumed / kStages) & 1;
@@ -282,10 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < kEpiWarp0) {
-    warpgroup_reg_dealloc<RegSplit<kGateUp>::kCtrl>();   // warps 2-3: TMEM owner and spare
+    warpgroup_reg_dealloc<kCtrlRegs>();   // warps 2-3: TMEM owner and spare
   } else {
     // ------------------------------------------------------------ epilogue
-    warpgroup_reg_alloc<RegSplit<kGateUp>::kEpi>();
+    warpgroup_reg_alloc<kEpiRegs>();
     constexpr int kCols = BN / 2;   // columns of the tile this thread owns
     constexpr int kPairs = kCols / 2;
     const int ew = warp - kEpiWarp0;
@@ -293,16 +413,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ch = ew >> 2;         // which half of the tile's columns
     const int row = lq * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(lq * 32) << 16);
-    int kcount = 0, iter = 0;
+    int kcount = 0, gu_iter = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++iter) {
-      const Tile tl = decode_tile(ctl, args, t);
+    for (int it = 0;; ++it) {
+      int t;
+      if (kFused) {
+        const int slot = it % kTileSlots;
+        const bool got = mbar_wait(&ctl->tile_full[slot], (it / kTileSlots) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        t = ctl->tile_slot[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->tile_empty[slot]);
+      } else {
+        t = blockIdx.x + it * gridDim.x;
+        if (t >= total) t = -1;
+      }
+      if (t < 0) break;
+      const Tile tl = decode_tile<kMode>(ctl, args, t);
+      const int nkb = (tl.gu ? args.H : args.I) / kBK;
+      // A fused down tile reads Z's scales, written by other CTAs of this
+      // launch: acquire the block's completion first, then load through L2.
+      const bool coherent = kFused && !tl.gu;
+      if (coherent) {
+        const bool ready = wait_count(args.sched + 1 + tl.blk, done_target, abort_flag);
+        if (!__all_sync(0xffffffffu, ready)) {
+          ok = false;
+          break;
+        }
+      }
       const int m = tl.m_blk * kBM + row;
       const long long grow = static_cast<long long>(tl.base) + row;  // buffer row of this thread
       // Scales are read for rows inside the expert's capacity (padded) or the
       // buffer (packed); rows past the count are promoted but never stored.
       const bool in_cap = args.packed ? grow < args.rows : m < args.R;
-      const float* asc = args.a_scale + (in_cap ? grow : 0) * nkb;
+      const float* asc = (tl.gu ? args.xs : args.zs) + (in_cap ? grow : 0) * nkb;
       // gate/up: gate columns [64ch, 64ch+64) and up columns [128+64ch, ..+64);
       // down:    columns [kCols*ch, kCols*ch + kCols), inside one 128-column
       //          weight-scale block.
@@ -311,22 +458,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* wsc0;
       const float* wsc1;
       uint32_t col0, col1;  // TMEM columns of this thread's two 64-column chunks
-      if (kGateUp && args.inter) {
+      if (tl.gu && args.inter) {
         const int nb = 2 * args.I / 128;
-        wsc0 = args.w_scale + (static_cast<size_t>(tl.e) * nb + 2 * tl.n_blk + ch) * nkb;
+        wsc0 = args.w13_scale + (static_cast<size_t>(tl.e) * nb + 2 * tl.n_blk + ch) * nkb;
         wsc1 = wsc0;
         col0 = static_cast<uint32_t>(ch * 128);
         col1 = col0 + 64;
-      } else if (kGateUp) {
+      } else if (tl.gu) {
         const int nb = 2 * args.I / 128;
-        wsc0 = args.w_scale + (static_cast<size_t>(tl.e) * nb + tl.n_blk) * nkb;
-        wsc1 = args.w_scale + (static_cast<size_t>(tl.e) * nb + args.I / 128 + tl.n_blk) * nkb;
+        wsc0 = args.w13_scale + (static_cast<size_t>(tl.e) * nb + tl.n_blk) * nkb;
+        wsc1 = args.w13_scale + (static_cast<size_t>(tl.e) * nb + args.I / 128 + tl.n_blk) * nkb;
         col0 = static_cast<uint32_t>(ch * 64);
         col1 = col0 + 128;
       } else {
         const int nb = args.H / 128;
         const int cb = (tl.n_blk * BN + ch * kCols) / 128;
-        wsc0 = args.w_scale + (static_cast<size_t>(tl.e) * nb + cb) * nkb;
+        wsc0 = args.w2_scale + (static_cast<size_t>(tl.e) * nb + cb) * nkb;
         wsc1 = wsc0;
         col0 = static_cast<uint32_t>(ch * kCols);
         col1 = col0 + 64;
@@ -335,11 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < kPairs; ++i) acc2[i] = 0;
       // Scales of K groups kb+1 and kb+2 are in flight while group kb is promoted.
-      float sa1 = in_cap ? __ldg(asc) : 0.f;
+      float sa1 = in_cap ? ld_scale(asc, coherent) : 0.f;
       float w01 = __ldg(wsc0), w11 = __ldg(wsc1);
       float sa2 = 0.f, w02 = 0.f, w12 = 0.f;
       if (nkb > 1) {
-        sa2 = in_cap ? __ldg(asc + 1) : 0.f;
+        sa2 = in_cap ? ld_scale(asc + 1, coherent) : 0.f;
         w02 = __ldg(wsc0 + 1);
         w12 = __ldg(wsc1 + 1);
       }
@@ -350,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         w01 = w02;
         w11 = w12;
         if (kb + 2 < nkb) {
-          sa2 = in_cap ? __ldg(asc + kb + 2) : 0.f;
+          sa2 = in_cap ? ld_scale(asc + kb + 2, coherent) : 0.f;
           w02 = __ldg(wsc0 + kb + 2);
           w12 = __ldg(wsc1 + kb + 2);
         }
@@ -365,12 +512,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t s0x2 = f32x2_pack(s0, s0);
         const uint64_t s1x2 = f32x2_pack(s1, s1);
         // Chunk j of 64 columns (one TMEM load, 8 KB per warp in flight):
-        // gate/up j = 0 gate, j = 1 up; down j = 0 .. kCols/64-1.
+        // gate/up j = 0 gate, j = 1 up; down j = 0 .. kCols/64-1, all with
+        // the one scale of their 128-column block.
         uint32_t buf[64];
 #pragma unroll
         for (int j = 0; j < kCols / 64; ++j) {
           const uint32_t col = j ? col1 : col0;
-          const uint64_t sx2 = (kGateUp && j) ? s1x2 : s0x2;
+          const uint64_t sx2 = (tl.gu && j) ? s1x2 : s0x2;
           tmem_load64_sync(base + col, buf);
 #pragma unroll
           for (int i = 0; i < 32; ++i) ffma2_acc(acc2[32 * j + i], sx2, buf[2 * i], buf[2 * i + 1]);
@@ -382,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       const bool valid = row < tl.rows && grow < args.rows;
-      if (kGateUp) {
+      if (kMode != kModeDown && tl.gu) {
         // Z = SiLU(gate) * up on this thread's 64 columns (written over the
         // gate half of acc2), then the row amax over the tile's 128 Z columns
         // shared with the partner warp holding the other half.
@@ -410,7 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             amax = fmaxf(amax, fmaxf(fabsf(z0), fabsf(z1)));
           }
         }
-        const int par = iter & 1;
+        const int par = gu_iter & 1;
+        ++gu_iter;
         ctl->amax[par][ch][row] = amax;
         mbar_arrive(&ctl->amax_bar);
         if (!mbar_wait(&ctl->amax_bar, par, abort_flag)) {
@@ -440,7 +589,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ch == 0)
             args.zs[grow * (args.I / 128) + tl.n_blk] = scale;
         }
-      } else {
+        if (kFused) {
+          // Publish this warp's part of the block's Z (32 rows x 64 columns
+          // and their scales) to the down tiles of other CTAs.
+          fence_proxy_async_global();
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) red_add_release_gpu(args.sched + 1 + tl.blk, 1);
+        }
+      } else if (kMode != kModeGateUp) {
         // BF16 rows through a per-warp shared-memory stage: each round the
         // 32 threads deposit 32 columns of their rows, then the warp writes
         // 8 rows x 64 bytes per store instruction.
@@ -534,29 +691,67 @@ cudaError_t make_activation_maps(CUtensorMap* m, const void* base, uint64_t cols
   return err;
 }
 
-template <int BN, bool kGateUp>
-cudaError_t launch_impl(const CUtensorMap* ta, const CUtensorMap& tb, const GemmArgs& a,
-                        int sm_count, cudaStream_t s) {
-  using L = Layout<BN, kGateUp>;
+template <int BN, int kMode>
+cudaError_t launch_impl(const GemmMaps& maps, const GemmArgs& a, long long max_tiles, int sm_count,
+                        cudaStream_t s) {
+  using L = Layout<BN, kMode>;
   // The setmaxnreg split assumes the kernel was compiled to exactly
   // kLaunchRegs registers per thread; any other count could leave the
   // epilogue's register increase waiting forever, so refuse to launch.
   static const int compiled_regs = [] {
     cudaFuncAttributes attr{};
-    return cudaFuncGetAttributes(&attr, grouped_gemm_kernel<BN, kGateUp>) == cudaSuccess
+    return cudaFuncGetAttributes(&attr, grouped_gemm_kernel<BN, kMode>) == cudaSuccess
                ? attr.numRegs
                : -1;
   }();
   if (compiled_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  const long long ub = static_cast<long long>(a.E) * ((a.R + kBM - 1) / kBM) * a.n_tiles;
-  const int grid = static_cast<int>(std::min<long long>(ub, sm_count));
+  const int grid = static_cast<int>(std::min<long long>(max_tiles, sm_count));
   if (grid <= 0) return cudaSuccess;
-  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BN, kGateUp>,
+  cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<BN, kMode>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::kSmem));
   if (err != cudaSuccess) return err;
-  grouped_gemm_kernel<BN, kGateUp><<<grid, kThreads, L::kSmem, s>>>(ta[0], ta[1], ta[2], tb, a);
+  grouped_gemm_kernel<BN, kMode><<<grid, kThreads, L::kSmem, s>>>(maps, a);
   return cudaGetLastError();
+}
+
+// Upper bound on the 128-row blocks of a launch: every expert's count is
+// clamped to R, and in the packed layout the blocks also fit in ceil(rows/128)
+// plus one partial block per expert.
+long long max_blocks(int E, RowLayout rl) {
+  const long long padded = static_cast<long long>(E) * ((rl.R + kBM - 1) / kBM);
+  return rl.packed ? std::min<long long>(padded, (rl.rows + kBM - 1) / kBM + E) : padded;
+}
+
+GemmArgs common_args(const int32_t* counts, int E, RowLayout rl, int H, int I,
+                     int32_t* dev_status) {
+  GemmArgs a{};
+  a.counts = counts;
+  a.E = E;
+  a.R = rl.R;
+  a.I = I;
+  a.H = H;
+  a.nt_gu = I / 128;
+  a.nt_dn = H % 256 == 0 ? H / 256 : H / 128;
+  a.packed = rl.packed;
+  a.rows = rl.rows;
+  a.dev_status = dev_status;
+  return a;
+}
+
+cudaError_t gateup_maps(GemmMaps* m, const uint8_t* xq, int E, RowLayout rl, int H, int I,
+                        const uint8_t* w13) {
+  cudaError_t err = make_activation_maps(m->a[0], xq, H, static_cast<uint64_t>(rl.rows));
+  if (err == cudaSuccess)
+    err = make_map_u8(&m->b[0], w13, H, static_cast<uint64_t>(E) * 2 * I, kBM);
+  return err;
+}
+
+cudaError_t down_maps(GemmMaps* m, const uint8_t* zq, int E, RowLayout rl, int H, int I,
+                      const uint8_t* w2) {
+  cudaError_t err = make_activation_maps(m->a[1], zq, I, static_cast<uint64_t>(rl.rows));
+  if (err == cudaSuccess) err = make_map_u8(&m->b[1], w2, I, static_cast<uint64_t>(E) * H, kBM);
+  return err;
 }
 
 }  // namespace
@@ -567,58 +762,74 @@ cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t
                                int32_t* dev_status, int sm_count, cudaStream_t s,
                                int w13_interleaved) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
-  const int R = rl.R;
-  CUtensorMap ta[3], tb;
-  cudaError_t err = make_activation_maps(ta, xq, H, static_cast<uint64_t>(rl.rows));
-  if (err == cudaSuccess) err = make_map_u8(&tb, w13, H, static_cast<uint64_t>(E) * 2 * I, kBM);
+  GemmMaps maps{};
+  cudaError_t err = gateup_maps(&maps, xq, E, rl, H, I, w13);
   if (err != cudaSuccess) return err;
-  GemmArgs a{};
-  a.counts = counts;
-  a.a_scale = xs;
-  a.w_scale = w13_scale;
-  a.E = E;
-  a.R = R;
-  a.nkb = H / kBK;
-  a.n_tiles = I / 128;
-  a.I = I;
-  a.H = H;
+  GemmArgs a = common_args(counts, E, rl, H, I, dev_status);
+  a.xs = xs;
+  a.w13_scale = w13_scale;
   a.zq = zq;
   a.zs = zs;
   a.inter = w13_interleaved ? 1 : 0;
-  a.packed = rl.packed;
-  a.rows = rl.rows;
-  a.dev_status = dev_status;
-  return launch_impl<256, true>(ta, tb, a, sm_count, s);
+  return launch_impl<256, kModeGateUp>(maps, a, max_blocks(E, rl) * a.nt_gu, sm_count, s);
 }
 
 cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* counts, int E,
                              RowLayout rl, int H, int I, const uint8_t* w2, const float* w2_scale,
                              void* out, int32_t* dev_status, int sm_count, cudaStream_t s) {
   if (E > kMaxExperts) return cudaErrorInvalidValue;
-  const int R = rl.R;
-  CUtensorMap ta[3], tb;
-  cudaError_t err = make_activation_maps(ta, zq, I, static_cast<uint64_t>(rl.rows));
-  if (err == cudaSuccess) err = make_map_u8(&tb, w2, I, static_cast<uint64_t>(E) * H, kBM);
+  GemmMaps maps{};
+  cudaError_t err = down_maps(&maps, zq, E, rl, H, I, w2);
   if (err != cudaSuccess) return err;
-  GemmArgs a{};
-  a.counts = counts;
-  a.a_scale = zs;
-  a.w_scale = w2_scale;
-  a.E = E;
-  a.R = R;
-  a.nkb = I / kBK;
-  a.I = I;
-  a.H = H;
+  GemmArgs a = common_args(counts, E, rl, H, I, dev_status);
+  a.zq = const_cast<uint8_t*>(zq);
+  a.zs = const_cast<float*>(zs);
+  a.w2_scale = w2_scale;
   a.out = static_cast<__nv_bfloat16*>(out);
-  a.packed = rl.packed;
-  a.rows = rl.rows;
-  a.dev_status = dev_status;
-  if (H % 256 == 0) {
-    a.n_tiles = H / 256;
-    return launch_impl<256, false>(ta, tb, a, sm_count, s);
+  const long long tiles = max_blocks(E, rl) * a.nt_dn;
+  if (H % 256 == 0) return launch_impl<256, kModeDown>(maps, a, tiles, sm_count, s);
+  return launch_impl<128, kModeDown>(maps, a, tiles, sm_count, s);
+}
+
+size_t gemm_sync_ints(int E, RowLayout rl) {
+  return 1 + static_cast<size_t>(max_blocks(E, rl));
+}
+
+cudaError_t launch_gemm_gateup_down(const uint8_t* xq, const float* xs, const int32_t* counts,
+                                    int E, RowLayout rl, int H, int I, const uint8_t* w13,
+                                    const float* w13_scale, const uint8_t* w2,
+                                    const float* w2_scale, uint8_t* zq, float* zs, void* out,
+                                    int* sync, size_t sync_ints, int32_t* dev_status,
+                                    int sm_count, cudaStream_t s, int w13_interleaved) {
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
+  // The fused kernel runs 256-column down tiles only.
+  if (H % 256 != 0) {
+    cudaError_t err = launch_gemm_gateup(xq, xs, counts, E, rl, H, I, w13, w13_scale, zq, zs,
+                                         dev_status, sm_count, s, w13_interleaved);
+    if (err != cudaSuccess) return err;
+    return launch_gemm_down(zq, zs, counts, E, rl, H, I, w2, w2_scale, out, dev_status,
+                            sm_count, s);
   }
-  a.n_tiles = H / 128;
-  return launch_impl<128, false>(ta, tb, a, sm_count, s);
+  const size_t need = gemm_sync_ints(E, rl);
+  if (sync == nullptr || sync_ints < need) return cudaErrorInvalidValue;
+  GemmMaps maps{};
+  cudaError_t err = gateup_maps(&maps, xq, E, rl, H, I, w13);
+  if (err == cudaSuccess) err = down_maps(&maps, zq, E, rl, H, I, w2);
+  if (err != cudaSuccess) return err;
+  GemmArgs a = common_args(counts, E, rl, H, I, dev_status);
+  a.xs = xs;
+  a.w13_scale = w13_scale;
+  a.w2_scale = w2_scale;
+  a.zq = zq;
+  a.zs = zs;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.sched = sync;
+  a.inter = w13_interleaved ? 1 : 0;
+  // Tile ticket and per-block completion counts start at zero every launch.
+  err = cudaMemsetAsync(sync, 0, need * sizeof(int), s);
+  if (err != cudaSuccess) return err;
+  return launch_impl<256, kModeFused>(maps, a, max_blocks(E, rl) * (a.nt_gu + a.nt_dn), sm_count,
+                                      s);
 }
 
 }  // namespace moe

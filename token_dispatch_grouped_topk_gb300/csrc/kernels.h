@@ -65,6 +65,17 @@ cudaError_t launch_gemm_gateup(const uint8_t* xq, const float* xs, const int32_t
 cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* counts, int E,
                              RowLayout rl, int H, int I, const uint8_t* w2, const float* w2_scale,
                              void* out, int32_t* dev_status, int sm_count, cudaStream_t s);
+// Both GEMMs in one persistent launch: a down tile starts as soon as the
+// gate/up tiles of its 128-row block have written their Z rows.  `sync` holds
+// gemm_sync_ints(E, rl) ints of device scratch (zeroed by the launch).  With
+// H % 256 != 0 it runs the two launches above instead.
+size_t gemm_sync_ints(int E, RowLayout rl);
+cudaError_t launch_gemm_gateup_down(const uint8_t* xq, const float* xs, const int32_t* counts,
+                                    int E, RowLayout rl, int H, int I, const uint8_t* w13,
+                                    const float* w13_scale, const uint8_t* w2,
+                                    const float* w2_scale, uint8_t* zq, float* zs, void* out,
+                                    int* sync, size_t sync_ints, int32_t* dev_status,
+                                    int sm_count, cudaStream_t s, int w13_interleaved);
 
 // ----- weighted combine
 // rows = the number of rows of `out` (E * R padded, the buffer's rows packed);

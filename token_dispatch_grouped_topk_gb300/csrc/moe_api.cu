@@ -58,7 +58,7 @@ bool valid_experts(int E, int R) {
 }
 
 struct ComputeWorkspace {
-  size_t xq, xs, zq, zs, total;
+  size_t xq, xs, zq, zs, sync, sync_ints, total;
 };
 
 bool valid_rows(int64_t rows) { return rows >= 1 && rows <= (int64_t{1} << 30); }
@@ -76,6 +76,12 @@ ComputeWorkspace compute_workspace_rows(int64_t rows_i, int H, int I) {
   off = align_up(off + rows * I, 256);
   w.zs = off;
   off = align_up(off + rows * (I / 128) * sizeof(float), 256);
+  // Scratch of the fused GEMM launch: a tile ticket and one completion count
+  // per 128-row block (at most ceil(rows / 128) plus one partial block for each
+  // of up to 1024 experts).
+  w.sync = off;
+  w.sync_ints = 1 + (rows + 127) / 128 + 1024;
+  off = align_up(off + w.sync_ints * sizeof(int), 256);
   w.total = off;
   return w;
 }
@@ -85,7 +91,8 @@ ComputeWorkspace compute_workspace(int E, int R, int H, int I) {
 
 moe_status from_cuda(cudaError_t e);
 
-// The three launches of the expert compute on a carved workspace.
+// The expert compute on a carved workspace: quantisation, then both GEMMs in
+// one launch.
 moe_status expert_compute_impl(const void* recv, const int32_t* counts, int E, RowLayout rl, int H,
                                int I, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
                                const float* w2_scale, void* out, int32_t* dev_status, void* workspace,
@@ -96,12 +103,12 @@ moe_status expert_compute_impl(const void* recv, const int32_t* counts, int E, R
   float* xs = reinterpret_cast<float*>(ws + w.xs);
   uint8_t* zq = ws + w.zq;
   float* zs = reinterpret_cast<float*>(ws + w.zs);
+  int* sync = reinterpret_cast<int*>(ws + w.sync);
   cudaError_t err = launch_quantize(recv, counts, E, rl, H, xq, xs, sm_count, s);
   if (err == cudaSuccess)
-    err = launch_gemm_gateup(xq, xs, counts, E, rl, H, I, w13, w13_scale, zq, zs, dev_status,
-                             sm_count, s, (flags & MOE_W13_INTERLEAVED) ? 1 : 0);
-  if (err == cudaSuccess)
-    err = launch_gemm_down(zq, zs, counts, E, rl, H, I, w2, w2_scale, out, dev_status, sm_count, s);
+    err = launch_gemm_gateup_down(xq, xs, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, zq,
+                                  zs, out, sync, w.sync_ints, dev_status, sm_count, s,
+                                  (flags & MOE_W13_INTERLEAVED) ? 1 : 0);
   return from_cuda(err);
 }
 
@@ -248,6 +255,39 @@ moe_status moe_gemm_down(const uint8_t* zq, const float* zs, const int32_t* coun
   return from_cuda(launch_gemm_down(zq, zs, counts, E, padded_rows(E, R), H, I, w2, w2_scale, out,
                                     dev_status, dev->sm_count,
                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_gemm_gateup_down_sync_size(int E, int R, int64_t rows) {
+  if (!valid_experts(E, R) || (rows != 0 && !valid_rows(rows))) return 0;
+  const RowLayout rl = rows == 0 ? padded_rows(E, R) : RowLayout{R, 1, rows};
+  return gemm_sync_ints(E, rl) * sizeof(int);
+}
+
+moe_status moe_gemm_gateup_down(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
+                                int R, int64_t rows, int H, int I, const uint8_t* w13,
+                                const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                uint8_t* zq, float* zs, void* out, int32_t* dev_status, void* sync,
+                                size_t sync_bytes, int flags, moe_stream_t stream) {
+  if (!valid_experts(E, R) || !valid_hidden(H) || !valid_hidden(I)) return MOE_ERR_INVALID_ARG;
+  if ((flags & ~MOE_W13_INTERLEAVED) != 0) return MOE_ERR_INVALID_ARG;
+  if (rows != 0 && !valid_rows(rows)) return MOE_ERR_INVALID_ARG;
+  if (xq == nullptr || xs == nullptr || counts == nullptr || w13 == nullptr ||
+      w13_scale == nullptr || w2 == nullptr || w2_scale == nullptr || zq == nullptr ||
+      zs == nullptr || out == nullptr || dev_status == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xq) || !aligned16(w13) || !aligned16(w2) || !aligned16(zq) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  const RowLayout rl = rows == 0 ? padded_rows(E, R) : RowLayout{R, 1, rows};
+  const size_t need = gemm_sync_ints(E, rl);
+  if (sync == nullptr || sync_bytes < need * sizeof(int) ||
+      (reinterpret_cast<uintptr_t>(sync) & 3u) != 0)
+    return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_gemm_gateup_down(
+      xq, xs, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, zq, zs, out,
+      static_cast<int*>(sync), sync_bytes / sizeof(int), dev_status, dev->sm_count,
+      reinterpret_cast<cudaStream_t>(stream), (flags & MOE_W13_INTERLEAVED) ? 1 : 0));
 }
 
 moe_status moe_expert_compute(const void* recv, const int32_t* counts, int E, int R, int H, int I,
