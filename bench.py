@@ -256,10 +256,13 @@ def run_ours(args, rank, local, world):
         n_active.append(int((c > 0).sum()))
     dropped = int(buf.dev_status[1].item())
 
-    # One step = the five stages of the layer, each bracketed by events on the
-    # launching stream so every kernel's duration is measured in place.
-    n_stage = 5
-    stage_names = ["dispatch", "quant", "gemm_gateup", "gemm_down", "combine"]
+    # One step = dispatch -> quantisation -> both GEMMs in one launch ->
+    # combine (the kernels moe_dispatch, moe_expert_compute and moe_combine
+    # run), each stage bracketed by events on the launching stream so every
+    # launch's duration is measured in place.
+    stage_names = ["dispatch", "quant", "gemm_gateup_down", "combine"]
+    n_stage = len(stage_names)
+    sync = buf.sync_view()
 
     def step(i, evs=None):
         idx, w = routings[i % N_ROUTINGS]
@@ -269,12 +272,11 @@ def run_ours(args, rank, local, world):
         if evs: evs[1].record(stream)
         api.moe_quantize_fp8(buf.recv, buf.counts, xq=xq, xs=xs)
         if evs: evs[2].record(stream)
-        api.moe_gemm_gateup_silu(xq, xs, buf.counts, w13, s13, zq=zq, zs=zs, dev_status=buf.dev_status)
+        api.moe_gemm_gateup_down(xq, xs, buf.counts, w13, s13, w2, s2, zq=zq, zs=zs, out=buf.out,
+                                 sync=sync, dev_status=buf.dev_status)
         if evs: evs[3].record(stream)
-        api.moe_gemm_down(zq, zs, buf.counts, w2, s2, out=buf.out, dev_status=buf.dev_status)
-        if evs: evs[4].record(stream)
         api.moe_combine(buf.out, buf.src_map, w, y=buf.y)
-        if evs: evs[5].record(stream)
+        if evs: evs[4].record(stream)
 
     for i in range(args.warmup):
         step(i)
@@ -320,8 +322,34 @@ def run_ours(args, rank, local, world):
     stage_ms = {n: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]))
                 for j, n in enumerate(stage_names)}
 
+    # ---- the two GEMMs as separate launches (moe_gemm_gateup_silu, then
+    # moe_gemm_down), for the rate of each GEMM on its own
+    def split_step(i, se):
+        idx, w = routings[i % N_ROUTINGS]
+        api.moe_dispatch(x, idx, w, E, R, recv=buf.recv, counts=buf.counts, src_map=buf.src_map,
+                         dev_status=buf.dev_status, workspace=buf.ws_dispatch)
+        api.moe_quantize_fp8(buf.recv, buf.counts, xq=xq, xs=xs)
+        se[0].record(stream)
+        api.moe_gemm_gateup_silu(xq, xs, buf.counts, w13, s13, zq=zq, zs=zs, dev_status=buf.dev_status)
+        se[1].record(stream)
+        api.moe_gemm_down(zq, zs, buf.counts, w2, s2, out=buf.out, dev_status=buf.dev_status)
+        se[2].record(stream)
+        api.moe_combine(buf.out, buf.src_map, w, y=buf.y)
+
+    split_steps = max(3, min(args.steps, 30))
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(split_steps)]
+    for i in range(args.warmup):
+        split_step(i, sevs[0])
+    torch.cuda.synchronize()
+    for i in range(split_steps):
+        split_step(args.warmup + i, sevs[i])
+    torch.cuda.synchronize()
+    split_ms = {n: float(np.mean([sevs[i][j].elapsed_time(sevs[i][j + 1]) for i in range(split_steps)]))
+                for j, n in enumerate(["gemm_gateup", "gemm_down"])}
+    split_rows = float(np.mean([n_valid[(args.warmup + i) % N_ROUTINGS] for i in range(split_steps)]))
+
     # ---- the same layer with dispatch and quantisation fused (moe_dispatch_quant)
-    fused_names = ["dispatch_quant", "gemm_gateup", "gemm_down", "combine"]
+    fused_names = ["dispatch_quant", "gemm_gateup_down", "combine"]
 
     def fused_step(i, fe=None):
         idx, w = routings[i % N_ROUTINGS]
@@ -329,17 +357,17 @@ def run_ours(args, rank, local, world):
         api.moe_dispatch_quant(x, idx, w, E, R, xq=xq, xs=xs, counts=buf.counts, src_map=buf.src_map,
                                dev_status=buf.dev_status, workspace=buf.ws_dispatch)
         if fe: fe[1].record(stream)
-        api.moe_gemm_gateup_silu(xq, xs, buf.counts, w13, s13, zq=zq, zs=zs, dev_status=buf.dev_status)
+        api.moe_gemm_gateup_down(xq, xs, buf.counts, w13, s13, w2, s2, zq=zq, zs=zs, out=buf.out,
+                                 sync=sync, dev_status=buf.dev_status)
         if fe: fe[2].record(stream)
-        api.moe_gemm_down(zq, zs, buf.counts, w2, s2, out=buf.out, dev_status=buf.dev_status)
-        if fe: fe[3].record(stream)
         api.moe_combine(buf.out, buf.src_map, w, y=buf.y)
-        if fe: fe[4].record(stream)
+        if fe: fe[3].record(stream)
 
     for i in range(args.warmup):
         fused_step(i)
     torch.cuda.synchronize()
-    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fused_names) + 1)]
+            for _ in range(args.steps)]
     fs, fe_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -488,27 +516,39 @@ def run_ours(args, rank, local, world):
     h2d = x.numel() * 2 + routings[0][0].numel() * 8 + routings[0][1].numel() * 4
     d2h = wl.T * wl.H * 2
 
-    # ---- roofline of the dominant kernel (gate/up GEMM) and per-kernel rates
+    # ---- roofline of the dominant kernel (the two-GEMM launch) and per-kernel rates
     peaks = load_peaks()
     nv = float(np.mean(rows_steps))
     na = int(round(np.mean([n_active[(args.warmup + i) % N_ROUTINGS] for i in range(args.steps)])))
 
     acct = layer_bytes_flops(wl, int(nv), na)
     fp8_peak = 2.0 * peaks["bf16_tflops"]        # nominal fp8 : bf16 dense ratio 4.5 / 2.25
-    g1_tflops = acct["gemm_gateup_flops"] / (stage_ms["gemm_gateup"] * 1e-3) / 1e12
-    g2_tflops = acct["gemm_down_flops"] / (stage_ms["gemm_down"] * 1e-3) / 1e12
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+    tfs = lambda f, ms: f / (ms * 1e-3) / 1e12
+    gemm_flops = acct["gemm_gateup_flops"] + acct["gemm_down_flops"]
+    gemm_bytes = acct["gemm_gateup_bytes"] + acct["gemm_down_bytes"]
+    g12 = tfs(gemm_flops, stage_ms["gemm_gateup_down"])
+    # the separate-launch GEMM rates, on the rows of the steps they ran
+    sacct = layer_bytes_flops(wl, int(split_rows), na)
+    g1 = tfs(sacct["gemm_gateup_flops"], split_ms["gemm_gateup"])
+    g2 = tfs(sacct["gemm_down_flops"], split_ms["gemm_down"])
     kernels = {
         "dispatch": {"ms": stage_ms["dispatch"], "GB/s": gbs(acct["dispatch_bytes"], stage_ms["dispatch"]),
                      "frac_hbm": gbs(acct["dispatch_bytes"], stage_ms["dispatch"]) / peaks["hbm_gbs"]},
         "quant": {"ms": stage_ms["quant"], "GB/s": gbs(acct["quant_bytes"], stage_ms["quant"]),
                   "frac_hbm": gbs(acct["quant_bytes"], stage_ms["quant"]) / peaks["hbm_gbs"]},
-        "gemm_gateup": {"ms": stage_ms["gemm_gateup"], "TFLOP/s": g1_tflops, "frac_fp8": g1_tflops / fp8_peak,
-                        "GB/s": gbs(acct["gemm_gateup_bytes"], stage_ms["gemm_gateup"])},
-        "gemm_down": {"ms": stage_ms["gemm_down"], "TFLOP/s": g2_tflops, "frac_fp8": g2_tflops / fp8_peak,
-                      "GB/s": gbs(acct["gemm_down_bytes"], stage_ms["gemm_down"])},
+        "gemm_gateup_down": {"ms": stage_ms["gemm_gateup_down"], "TFLOP/s": g12, "frac_fp8": g12 / fp8_peak,
+                             "GB/s": gbs(gemm_bytes, stage_ms["gemm_gateup_down"]),
+                             "note": "both GEMMs in one launch (moe_gemm_gateup_down)"},
         "combine": {"ms": stage_ms["combine"], "GB/s": gbs(acct["combine_bytes"], stage_ms["combine"]),
                     "frac_hbm": gbs(acct["combine_bytes"], stage_ms["combine"]) / peaks["hbm_gbs"]},
+        "separate_launches": {
+            "gemm_gateup": {"ms": split_ms["gemm_gateup"], "TFLOP/s": g1, "frac_fp8": g1 / fp8_peak,
+                            "GB/s": gbs(sacct["gemm_gateup_bytes"], split_ms["gemm_gateup"])},
+            "gemm_down": {"ms": split_ms["gemm_down"], "TFLOP/s": g2, "frac_fp8": g2 / fp8_peak,
+                          "GB/s": gbs(sacct["gemm_down_bytes"], split_ms["gemm_down"])},
+            "steps": split_steps,
+            "note": "moe_gemm_gateup_silu then moe_gemm_down (eager, events around each)"},
     }
     mean_rows = rows_total / args.steps / world
     tbo_res = {
@@ -526,14 +566,13 @@ def run_ours(args, rank, local, world):
             "dispatch_quant": {"ms": fused_stage_ms["dispatch_quant"],
                                "GB/s": gbs(acct["dispatch_quant_bytes"], fused_stage_ms["dispatch_quant"]),
                                "frac_hbm": gbs(acct["dispatch_quant_bytes"], fused_stage_ms["dispatch_quant"]) / peaks["hbm_gbs"]},
-            "gemm_gateup": {"ms": fused_stage_ms["gemm_gateup"]},
-            "gemm_down": {"ms": fused_stage_ms["gemm_down"]},
+            "gemm_gateup_down": {"ms": fused_stage_ms["gemm_gateup_down"]},
             "combine": {"ms": fused_stage_ms["combine"]},
         },
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": 5 * args.steps,
     }
     dom = max(stage_ms, key=stage_ms.get)
-    if dom in ("gemm_gateup", "gemm_down"):
+    if dom == "gemm_gateup_down":
         achieved = kernels[dom]["TFLOP/s"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak,
@@ -553,7 +592,7 @@ def run_ours(args, rank, local, world):
                         "step i-1's copy-out run on two copy streams beside step i's compute",
                 "serial_value": e2e_rows / (e2e_serial_ms / 1e3),
                 "serial_note": "copy in, compute, copy out back to back on one stream"},
-        "gpu_launches": 7 * args.steps, "clocks": clk.summary(), "fused": fused, "tbo": tbo_res,
+        "gpu_launches": 6 * args.steps, "clocks": clk.summary(), "fused": fused, "tbo": tbo_res,
         "packed": packed,
         "rows_per_step": nv, "dropped_routes_last_routing": dropped, "wl": wl,
     }
