@@ -319,11 +319,14 @@ moe_status moe_expert_compute_ex(const void* recv, const int32_t* counts, int E,
                                  int flags, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
- * moe_selftest_bounded_wait -- exercises the device-side failure path: one
- * thread runs the kernels' bounded mbarrier wait on a barrier that nothing
- * completes; after the wait limit (about 2 s) it sets MOE_DEV_TIMEOUT in
- * dev_status[0] and the kernel returns normally.  For tests of failure
- * handling; no GPU fault is involved.
+ * moe_selftest_bounded_wait -- exercises the device-side failure path: the
+ * kernels' two bounded waits run on things nothing completes, at the same
+ * time (an mbarrier wait, and the acquire wait on a global completion counter
+ * used by moe_gemm_gateup_down's down tiles).  After the wait limit (about
+ * 2 s) each sets MOE_DEV_TIMEOUT in dev_status[0] and its bit in dev_status[1]
+ * (1: mbarrier, 2: counter); the kernel returns normally.  dev_status is
+ * int32[2], zeroed by the caller.  For tests of failure handling; no GPU fault
+ * is involved.
  * ------------------------------------------------------------------------- */
 moe_status moe_selftest_bounded_wait(int32_t* dev_status, moe_stream_t stream);
 

@@ -27,6 +27,7 @@ def test_bounded_wait_times_out_and_context_survives():
     assert rc == 0
     torch.cuda.synchronize()
     assert st[0].item() & api.DEV_TIMEOUT
+    assert st[1].item() == 3          # both the mbarrier wait and the counter wait gave up
     # the context is still usable: a full layer runs and reports no timeout
     d = W.make_layer_inputs("traced", seed=0, device=DEV)
     wl = d["wl"]

@@ -194,23 +194,6 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ void red_add_release_gpu(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-// Waits until *p >= target (another CTA's release); false once `abort` is set
-// or after kWaitLimitNs.
-__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* abort) {
-  if (ld_acquire_gpu(p) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    __nanosleep(128);
-    if (ld_acquire_gpu(p) >= target) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
 // Scales written by this launch (Z's, in a fused launch) are read through L2.
 __device__ __forceinline__ float ld_scale(const float* p, bool coherent) {
   return coherent ? __ldcg(p) : __ldg(p);
