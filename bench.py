@@ -449,17 +449,29 @@ def run_ours(args, rank, local, world):
     tbo_steps = max(3, min(args.steps, 20))
 
     def tbo_ms(overlap):
+        # one CUDA graph per routing holds the whole split step (both lanes and,
+        # when overlapped, both side streams forked from the capturing stream)
         for i in range(args.warmup):
             idx, w = routings[i % N_ROUTINGS]
             tbo.forward(x, idx, w, w13, s13, w2, s2, overlap=overlap)
         torch.cuda.synchronize()
+        tgraphs = []
+        for r in range(N_ROUTINGS):
+            idx, w = routings[r]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                tbo.forward(x, idx, w, w13, s13, w2, s2, overlap=overlap)
+            tgraphs.append(g)
+        for i in range(args.warmup):
+            tgraphs[i % N_ROUTINGS].replay()
+        torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for i in range(tbo_steps):
-            idx, w = routings[(args.warmup + i) % N_ROUTINGS]
-            tbo.forward(x, idx, w, w13, s13, w2, s2, overlap=overlap)
+            tgraphs[(args.warmup + i) % N_ROUTINGS].replay()
         b.record(stream)
         torch.cuda.synchronize()
+        del tgraphs
         return a.elapsed_time(b) / tbo_steps
 
     split_serial_ms = tbo_ms(False)
@@ -557,7 +569,8 @@ def run_ours(args, rank, local, world):
         "rows_per_s": {"no_split": value, "serial_split": mean_rows / (split_serial_ms / 1e3),
                        "overlapped_split": mean_rows / (split_overlap_ms / 1e3)},
         "note": "two token halves, one buffer lane each; overlapped = B's dispatch beside A's expert "
-                "compute and B's expert compute beside A's combine on two streams",
+                "compute and B's expert compute beside A's combine on two streams; every mode "
+                "timed as CUDA-graph replays",
     }
     fused = {
         "value": rows_total / (fused_ms / 1e3), "unit": UNIT, "ms_per_step": fused_ms / args.steps,

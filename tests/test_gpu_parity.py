@@ -498,6 +498,37 @@ def test_two_batch_overlap_equals_serial_split():
         assert lane.dev_status[0].item() & api.DEV_TIMEOUT == 0
 
 
+def test_two_batch_overlap_graph_replay():
+    """The overlapped two-micro-batch schedule captured in one CUDA graph (the
+    side streams fork from and join the capturing stream): replays equal the
+    eager overlapped forward, also after new routes are copied into the
+    captured input buffers."""
+    d = W.make_layer_inputs("prefill", seed=6, device=DEV)
+    d2 = W.make_layer_inputs("prefill", seed=7, device=DEV)
+    wl = d["wl"]
+    dev = torch.device(DEV)
+    tbo = api.TwoBatchOverlap(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
+    x, idx, w = d["x"].clone(), d["topk_idx"].clone(), d["topk_w"].clone()
+    wts = (d["w13"], d["s13"], d["w2"], d["s2"])
+    tbo.forward(x, idx, w, *wts, overlap=True)          # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tbo.forward(x, idx, w, *wts, overlap=True)
+    ref = api.TwoBatchOverlap(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
+    for inputs in (d, d2):
+        x.copy_(inputs["x"])
+        idx.copy_(inputs["topk_idx"])
+        w.copy_(inputs["topk_w"])
+        g.replay()
+        got = tbo.y.clone()
+        want = ref.forward(inputs["x"], inputs["topk_idx"], inputs["topk_w"], *wts, overlap=True)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+        for lane in tbo.lanes:
+            assert lane.dev_status[0].item() & api.DEV_TIMEOUT == 0
+
+
 def test_layer_large_config_sampled():
     """Large layer (T=16384, E=256, H=7168, I=2048, R=4096, ~11 GB of FP8
     weights), in the launch configuration the benchmark times: dispatch
