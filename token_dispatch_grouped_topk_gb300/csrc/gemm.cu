@@ -46,11 +46,13 @@
 //    only ever waits for tiles already held by running CTAs, and passes each
 //    to the MMA and epilogue warps through a small shared-memory ring.  Each
 //    epilogue warp of a gate/up tile, after storing its 32 rows x 64 columns
-//    of Z, adds one to its block's count (release); a down tile of that block
-//    waits (acquire, bounded) until the count reaches 8 x the gate/up tiles
-//    per block before its producer loads Z with TMA and its epilogue reads
-//    Z's scales.  The down GEMM of the first blocks so runs under the last
-//    gate/up wave instead of after it.
+//    of Z, adds one to its block's count (release); the producer publishes a
+//    down tile of that block only after the count reaches 8 x the gate/up
+//    tiles per block (acquire, bounded), then loads Z with TMA; the epilogue
+//    reads Z's scales after taking the tile from the ring.  The down GEMM of
+//    the first blocks so runs under the last gate/up wave instead of after it;
+//  - the epilogue takes its next tile, and requests that tile's first scales,
+//    before the current tile's tail whenever the tile is already published.
 // Every wait is bounded; on expiry the kernel raises MOE_DEV_TIMEOUT in the
 // status word, drains its own copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -199,6 +201,98 @@ __device__ __forceinline__ float ld_scale(const float* p, bool coherent) {
   return coherent ? __ldcg(p) : __ldg(p);
 }
 
+// Per-tile state of one epilogue thread: the tile, where its scales and TMEM
+// columns are, and the scales of its first two K groups (requested ahead).
+struct EpiTile {
+  int t;  // tile index, -1: none left
+  Tile tl;
+  int nkb;
+  bool in_cap, coherent;
+  long long grow;  // buffer row of this thread
+  const float* asc;
+  const float* wsc0;
+  const float* wsc1;
+  uint32_t col0, col1;  // TMEM columns of this thread's two 64-column chunks
+  float sa1, w01, w11, sa2, w02, w12;
+};
+
+// Tile `it` of this CTA for an epilogue warp.  Fused launches read it from the
+// ring: with `wait` the warp waits (bounded) for the slot, without it takes the
+// slot only if it is already published.  Returns 1 with *t set (-1: no tiles
+// left), 0 if not yet published, -1 if the wait gave up.
+__device__ __forceinline__ int epi_claim(Control* ctl, int it, bool fused, int total, bool wait,
+                                         volatile int* abort, int lane, int* t) {
+  if (!fused) {
+    const int v = blockIdx.x + it * gridDim.x;
+    *t = v < total ? v : -1;
+    return 1;
+  }
+  const int slot = it % kTileSlots;
+  const uint32_t par = (it / kTileSlots) & 1;
+  const bool got = wait ? mbar_wait(&ctl->tile_full[slot], par, abort)
+                        : mbar_try_wait(&ctl->tile_full[slot], par);
+  if (!__all_sync(0xffffffffu, got)) return wait ? -1 : 0;
+  *t = ctl->tile_slot[slot];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ctl->tile_empty[slot]);
+  return 1;
+}
+
+// Decodes p->t and requests the scales of its first two K groups.
+template <int BN, int kMode>
+__device__ __forceinline__ void epi_prepare(EpiTile* p, const Control* ctl, const GemmArgs& args,
+                                            int row, int ch) {
+  constexpr int kCols = BN / 2;
+  const Tile tl = decode_tile<kMode>(ctl, args, p->t);
+  p->tl = tl;
+  const int nkb = (tl.gu ? args.H : args.I) / kBK;
+  p->nkb = nkb;
+  // A fused down tile reads Z's scales, written by other CTAs of this launch:
+  // the producer published the tile only after acquiring its block's
+  // completion, and the loads go through L2.
+  p->coherent = kMode == kModeFused && !tl.gu;
+  const int m = tl.m_blk * kBM + row;
+  p->grow = static_cast<long long>(tl.base) + row;
+  // Scales are read for rows inside the expert's capacity (padded) or the
+  // buffer (packed); rows past the count are promoted but never stored.
+  p->in_cap = args.packed ? p->grow < args.rows : m < args.R;
+  p->asc = (tl.gu ? args.xs : args.zs) + (p->in_cap ? p->grow : 0) * nkb;
+  // gate/up: gate columns [64ch, 64ch+64) and up columns [128+64ch, ..+64);
+  // down:    columns [kCols*ch, kCols*ch + kCols), inside one 128-column
+  //          weight-scale block.
+  //          Interleaved gate/up: columns [128ch, 128ch+128), 64 (gate, up)
+  //          pairs inside one 128-row weight-scale block.
+  if (tl.gu && args.inter) {
+    const int nb = 2 * args.I / 128;
+    p->wsc0 = args.w13_scale + (static_cast<size_t>(tl.e) * nb + 2 * tl.n_blk + ch) * nkb;
+    p->wsc1 = p->wsc0;
+    p->col0 = static_cast<uint32_t>(ch * 128);
+    p->col1 = p->col0 + 64;
+  } else if (tl.gu) {
+    const int nb = 2 * args.I / 128;
+    p->wsc0 = args.w13_scale + (static_cast<size_t>(tl.e) * nb + tl.n_blk) * nkb;
+    p->wsc1 = args.w13_scale + (static_cast<size_t>(tl.e) * nb + args.I / 128 + tl.n_blk) * nkb;
+    p->col0 = static_cast<uint32_t>(ch * 64);
+    p->col1 = p->col0 + 128;
+  } else {
+    const int nb = args.H / 128;
+    const int cb = (tl.n_blk * BN + ch * kCols) / 128;
+    p->wsc0 = args.w2_scale + (static_cast<size_t>(tl.e) * nb + cb) * nkb;
+    p->wsc1 = p->wsc0;
+    p->col0 = static_cast<uint32_t>(ch * kCols);
+    p->col1 = p->col0 + 64;
+  }
+  p->sa1 = p->in_cap ? ld_scale(p->asc, p->coherent) : 0.f;
+  p->w01 = __ldg(p->wsc0);
+  p->w11 = __ldg(p->wsc1);
+  p->sa2 = p->w02 = p->w12 = 0.f;
+  if (nkb > 1) {
+    p->sa2 = p->in_cap ? ld_scale(p->asc + 1, p->coherent) : 0.f;
+    p->w02 = __ldg(p->wsc0 + 1);
+    p->w12 = __ldg(p->wsc1 + 1);
+  }
+}
+
 template <int BN, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
@@ -270,6 +364,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           t = atomicAdd(args.sched, 1);
           if (t >= total) t = -1;
+          // A down tile is published only once the gate/up tiles of its block
+          // are done (acquire): the MMA and epilogue warps that take it from
+          // the ring are then ordered after Z's stores.
+          if (t >= 0) {
+            const Tile dt = decode_tile<kMode>(ctl, args, t);
+            if (!dt.gu) {
+              if (!wait_count(args.sched + 1 + dt.blk, done_target, abort_flag)) {
+                ok = false;
+                break;
+              }
+              fence_proxy_async_global();
+            }
+          }
           ctl->tile_slot[slot] = t;
           mbar_arrive(&ctl->tile_full[slot]);
         } else {
@@ -278,13 +385,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (t < 0) break;
         const Tile tl = decode_tile<kMode>(ctl, args, t);
-        if (kFused && !tl.gu) {
-          if (!wait_count(args.sched + 1 + tl.blk, done_target, abort_flag)) {
-            ok = false;
-            break;
-          }
-          fence_proxy_async_global();
-        }
         const int g = tl.gu ? 0 : 1;
         const int nkb = (tl.gu ? args.H : args.I) / kBK;
         const int a_row = tl.base;
@@ -398,81 +498,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(lq * 32) << 16);
     int kcount = 0, gu_iter = 0;
     bool ok = true;
-    for (int it = 0;; ++it) {
-      int t;
-      if (kFused) {
-        const int slot = it % kTileSlots;
-        const bool got = mbar_wait(&ctl->tile_full[slot], (it / kTileSlots) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        t = ctl->tile_slot[slot];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->tile_empty[slot]);
-      } else {
-        t = blockIdx.x + it * gridDim.x;
-        if (t >= total) t = -1;
-      }
-      if (t < 0) break;
-      const Tile tl = decode_tile<kMode>(ctl, args, t);
-      const int nkb = (tl.gu ? args.H : args.I) / kBK;
-      // A fused down tile reads Z's scales, written by other CTAs of this
-      // launch: acquire the block's completion first, then load through L2.
-      const bool coherent = kFused && !tl.gu;
-      if (coherent) {
-        const bool ready = wait_count(args.sched + 1 + tl.blk, done_target, abort_flag);
-        if (!__all_sync(0xffffffffu, ready)) {
-          ok = false;
-          break;
-        }
-      }
-      const int m = tl.m_blk * kBM + row;
-      const long long grow = static_cast<long long>(tl.base) + row;  // buffer row of this thread
-      // Scales are read for rows inside the expert's capacity (padded) or the
-      // buffer (packed); rows past the count are promoted but never stored.
-      const bool in_cap = args.packed ? grow < args.rows : m < args.R;
-      const float* asc = (tl.gu ? args.xs : args.zs) + (in_cap ? grow : 0) * nkb;
-      // gate/up: gate columns [64ch, 64ch+64) and up columns [128+64ch, ..+64);
-      // down:    columns [kCols*ch, kCols*ch + kCols), inside one 128-column
-      //          weight-scale block.
-      //          Interleaved gate/up: columns [128ch, 128ch+128), 64 (gate, up)
-      //          pairs inside one 128-row weight-scale block.
-      const float* wsc0;
-      const float* wsc1;
-      uint32_t col0, col1;  // TMEM columns of this thread's two 64-column chunks
-      if (tl.gu && args.inter) {
-        const int nb = 2 * args.I / 128;
-        wsc0 = args.w13_scale + (static_cast<size_t>(tl.e) * nb + 2 * tl.n_blk + ch) * nkb;
-        wsc1 = wsc0;
-        col0 = static_cast<uint32_t>(ch * 128);
-        col1 = col0 + 64;
-      } else if (tl.gu) {
-        const int nb = 2 * args.I / 128;
-        wsc0 = args.w13_scale + (static_cast<size_t>(tl.e) * nb + tl.n_blk) * nkb;
-        wsc1 = args.w13_scale + (static_cast<size_t>(tl.e) * nb + args.I / 128 + tl.n_blk) * nkb;
-        col0 = static_cast<uint32_t>(ch * 64);
-        col1 = col0 + 128;
-      } else {
-        const int nb = args.H / 128;
-        const int cb = (tl.n_blk * BN + ch * kCols) / 128;
-        wsc0 = args.w2_scale + (static_cast<size_t>(tl.e) * nb + cb) * nkb;
-        wsc1 = wsc0;
-        col0 = static_cast<uint32_t>(ch * kCols);
-        col1 = col0 + 64;
-      }
+    EpiTile cur;
+    cur.t = -1;
+    {
+      int t = -1;
+      if (epi_claim(ctl, 0, kFused, total, true, abort_flag, lane, &t) < 0) ok = false;
+      cur.t = t;
+      if (ok && t >= 0) epi_prepare<BN, kMode>(&cur, ctl, args, row, ch);
+    }
+    for (int it = 0; ok && cur.t >= 0; ++it) {
+      const Tile tl = cur.tl;
+      const long long grow = cur.grow;   // buffer row of this thread
       uint64_t acc2[kPairs];
 #pragma unroll
       for (int i = 0; i < kPairs; ++i) acc2[i] = 0;
       // Scales of K groups kb+1 and kb+2 are in flight while group kb is promoted.
-      float sa1 = in_cap ? ld_scale(asc, coherent) : 0.f;
-      float w01 = __ldg(wsc0), w11 = __ldg(wsc1);
-      float sa2 = 0.f, w02 = 0.f, w12 = 0.f;
-      if (nkb > 1) {
-        sa2 = in_cap ? ld_scale(asc + 1, coherent) : 0.f;
-        w02 = __ldg(wsc0 + 1);
-        w12 = __ldg(wsc1 + 1);
-      }
+      float sa1 = cur.sa1, w01 = cur.w01, w11 = cur.w11;
+      float sa2 = cur.sa2, w02 = cur.w02, w12 = cur.w12;
+      const int nkb = cur.nkb;
       for (int kb = 0; kb < nkb; ++kb) {
         const float s0 = sa1 * w01;
         const float s1 = sa1 * w11;
@@ -480,9 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         w01 = w02;
         w11 = w12;
         if (kb + 2 < nkb) {
-          sa2 = in_cap ? ld_scale(asc + kb + 2, coherent) : 0.f;
-          w02 = __ldg(wsc0 + kb + 2);
-          w12 = __ldg(wsc1 + kb + 2);
+          sa2 = cur.in_cap ? ld_scale(cur.asc + kb + 2, cur.coherent) : 0.f;
+          w02 = __ldg(cur.wsc0 + kb + 2);
+          w12 = __ldg(cur.wsc1 + kb + 2);
         }
         const int acc = kcount & 1;
         const uint32_t acc_phase = (kcount >> 1) & 1;
@@ -500,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t buf[64];
 #pragma unroll
         for (int j = 0; j < kCols / 64; ++j) {
-          const uint32_t col = j ? col1 : col0;
+          const uint32_t col = j ? cur.col1 : cur.col0;
           const uint64_t sx2 = (tl.gu && j) ? s1x2 : s0x2;
           tmem_load64_sync(base + col, buf);
 #pragma unroll
@@ -512,6 +555,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++kcount;
       }
       if (!ok) break;
+      // The next tile is taken, and its first scales requested, before this
+      // tile's tail when it is already published, so their latency is hidden
+      // behind the tail.  Otherwise (its block may be waiting for this very
+      // tile's Z) it is taken after the tail.
+      EpiTile nxt;
+      nxt.t = -1;
+      int t_next = -1;
+      const bool early = epi_claim(ctl, it + 1, kFused, total, false, abort_flag, lane, &t_next) > 0;
+      if (early) {
+        nxt.t = t_next;
+        if (t_next >= 0) epi_prepare<BN, kMode>(&nxt, ctl, args, row, ch);
+      }
       const bool valid = row < tl.rows && grow < args.rows;
       if (kMode != kModeDown && tl.gu) {
         // Z = SiLU(gate) * up on this thread's 64 columns (written over the
@@ -622,6 +677,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
       }
+      if (!early) {
+        if (epi_claim(ctl, it + 1, kFused, total, true, abort_flag, lane, &t_next) < 0) {
+          ok = false;
+          break;
+        }
+        nxt.t = t_next;
+        if (t_next >= 0) epi_prepare<BN, kMode>(&nxt, ctl, args, row, ch);
+      }
+      cur = nxt;
     }
     if (!ok) *abort_flag = 1;
   }
