@@ -87,8 +87,8 @@ constexpr int kLaunchRegs = 168;
 constexpr int kCtrlRegs = 40;
 constexpr int kEpiRegs = 232;
 static_assert(4 * kCtrlRegs + 8 * kEpiRegs == 12 * kLaunchRegs, "register split must fit the launch");
-// Down-GEMM output staging: per epilogue warp 32 rows x 32 BF16 columns, rows
-// padded to 80 bytes.
+// Output staging (Z codes of gate/up tiles, BF16 rows of down tiles): per
+// epilogue warp 32 rows x 64 bytes, rows padded to 80 bytes.
 constexpr int kStageRowBytes = 80;
 constexpr int kStageWarpBytes = 32 * kStageRowBytes;
 constexpr int kMaxExperts = 1024;
@@ -143,7 +143,7 @@ struct Layout {
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr int kOutStage = kMode == kModeGateUp ? 0 : kEpiWarps * kStageWarpBytes;
+  static constexpr int kOutStage = kEpiWarps * kStageWarpBytes;
   static constexpr size_t kSmem =
       1024 + static_cast<size_t>(kStages) * kStageBytes + sizeof(Control) + kOutStage;
 };
@@ -611,9 +611,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         amax = fmaxf(ctl->amax[par][0][row], ctl->amax[par][1][row]);
         float mult, scale;
         fp8_group_scale(amax, &mult, &scale);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(
-              args.zq + grow * args.I + tl.n_blk * 128 + ch * 64);
+        {
+          // The warp's 32 rows x 64 Z bytes go through its shared-memory stage,
+          // so each store instruction writes 8 rows x 64 bytes.
+          uint8_t* stage = out_stage + ew * kStageWarpBytes;
+          uint4* srow = reinterpret_cast<uint4*>(stage + lane * kStageRowBytes);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint32_t w[4];
@@ -626,8 +628,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                         __fmul_rn(f32x2_hi(zb), mult)))
                       << 16);
             }
-            dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+            srow[j] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+          __syncwarp();
+          const long long grow0 = static_cast<long long>(tl.base) + lq * 32;  // warp's first row
+          const int nvalid = static_cast<int>(                   // rows of this warp to store
+              min(static_cast<long long>(min(32, tl.rows - lq * 32)), args.rows - grow0));
+          const int c = lane & 3;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = 8 * i + (lane >> 2);
+            if (r < nvalid) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stage + r * kStageRowBytes + 16 * c);
+              *reinterpret_cast<uint4*>(args.zq + (grow0 + r) * args.I + tl.n_blk * 128 + ch * 64 +
+                                        16 * c) = v;
+            }
+          }
+          __syncwarp();
+        }
+        if (valid) {
           if (ch == 0)
             args.zs[grow * (args.I / 128) + tl.n_blk] = scale;
         }
