@@ -242,14 +242,17 @@ def test_expert_compute_short_blocks_only(H):
 
 
 @pytest.mark.parametrize("E,R,H,I,seed", [(5, 384, 512, 256, 21), (48, 256, 1024, 512, 22),
-                                          (3, 256, 384, 256, 23), (1, 1024, 256, 1024, 24)])
+                                          (3, 256, 384, 256, 23), (1, 1024, 256, 1024, 24),
+                                          (200, 128, 256, 128, 25)])
 def test_gemm_gateup_down_matches_stage_calls(E, R, H, I, seed):
     """Both GEMMs in one launch (down tiles of a block start once that block's
     gate/up tiles are done) against the two stage launches: Z codes, Z scales
     and out bit-identical on the valid rows, capacity rows of out untouched;
     three launches in a row reuse one scratch (each resets it); the packed
     layout on the same rows gives the same rows.  H = 384 takes the two-launch
-    form (128-wide down tiles)."""
+    form (128-wide down tiles).  E = 200 with H = 256, I = 128 makes tiles of one
+    or two K groups: the producer runs far ahead through the tile ring and many
+    down tiles reach their block's wait."""
     g = torch.Generator().manual_seed(seed)
     counts = torch.randint(0, R + 1, (E,), generator=g)
     counts[0] = R
