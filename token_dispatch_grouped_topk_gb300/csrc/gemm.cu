@@ -10,8 +10,9 @@
 //
 // Design (one CTA per SM, persistent):
 //  - tiles are 128 rows x BN columns of one expert; the tile list is derived on
-//    the device from counts (prefix of ceil(count/128) * n_tiles per expert),
-//    walked by all CTAs with a stride of gridDim.x.  Within an expert the
+//    the device from counts (prefix of ceil(count/128) per expert, times the
+//    N slices per block).  The one-GEMM launch forms walk it with a stride of
+//    gridDim.x; the two-GEMM form takes tiles from a ticket.  Within an expert the
 //    walk is M-block major: the N slices of one 128-row block are adjacent,
 //    so a block's activation rows are fetched once while the CTAs running at
 //    the same time share the expert's weight slices in L2.  (Measured on
