@@ -687,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             srow[j] = o;
           }
           __syncwarp();
-#pragma unroll 1
+#pragma unroll
           for (int i = 0; i < 4; ++i) {
             if (8 * i + (lane >> 2) < nvalid) {
               const uint4 v = *reinterpret_cast<const uint4*>(stage + sidx + i * 8 * kStageRowBytes);
