@@ -164,17 +164,19 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
     for (int k = 0; k < K; ++k) any |= dq[k] >= 0;
     if (!any) continue;
     const uint4* src = x + static_cast<size_t>(t) * nvec;
-    for (int v = v0 + lane; v < v1; v += 32 * 4) {
-      uint4 a[4];
+    // eight 16-byte vectors per lane in flight (four left the large layer's
+    // scatter 6 % slower)
+    for (int v = v0 + lane; v < v1; v += 32 * 8) {
+      uint4 a[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+      for (int u = 0; u < 8; ++u)
         if (v + 32 * u < v1) a[u] = ld_stream(src + v + 32 * u);
       for (int k = 0; k < K; ++k) {
         const int qq = dq[k];
         if (qq < 0) continue;
         uint4* dst = recv + static_cast<size_t>(qq) * nvec;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 8; ++u)
           if (v + 32 * u < v1) dst[v + 32 * u] = a[u];
       }
     }
