@@ -203,7 +203,8 @@ def _unit_scale_weights(E, H, I, seed):
 @pytest.mark.parametrize("shape", [(112, 8, 2, 256, 128, 128), (600, 16, 4, 512, 384, 256)])
 def test_interleaved_w13_bit_identical_to_standard(packed, shape):
     """Uniform block scales: interleaving W13's rows (2j gate, 2j+1 up) and
-    flagging MOE_W13_INTERLEAVED gives the standard layer's bytes."""
+    flagging MOE_W13_INTERLEAVED gives the standard layer's bytes, through
+    moe_expert_compute and (padded) through the fused dispatch+quant path."""
     T, E, K, H, I, R = shape
     w13, s13, w2, s2 = _unit_scale_weights(E, H, I, seed=41)
     inter = torch.empty_like(w13)
@@ -221,6 +222,11 @@ def test_interleaved_w13_bit_identical_to_standard(packed, shape):
     torch.cuda.synchronize()
     assert torch.equal(_bits(y_itl), _bits(y_std))
     assert float(y_std.float().abs().max()) > 0
+    if not packed:
+        # the fused dispatch+quant path hands the flag to moe_gemm_gateup_down
+        y_fused = itl.forward_fused(*args, inter.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV))
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(y_fused), _bits(y_std))
 
 
 def test_interleaved_w13_matches_oracle():
