@@ -292,6 +292,40 @@ def test_gemm_gateup_down_matches_stage_calls(E, R, H, I, seed):
         assert torch.equal(out_p.view(torch.int16), out1[vd].view(torch.int16))
 
 
+def test_gemm_gateup_down_two_streams_at_once():
+    """Two one-launch GEMMs on two streams at the same time, so their
+    persistent CTAs compete for the SMs.  Tiles are taken in list order only by
+    CTAs that are running, so a down tile never waits on a gate/up tile held by
+    a CTA that has not started.  Both finish without a timeout and equal their
+    results run alone."""
+    E, R, H, I = 24, 512, 1024, 512
+    dev = torch.device(DEV)
+    runs = []
+    for seed in (31, 32):
+        g = torch.Generator().manual_seed(seed)
+        counts = torch.randint(0, R + 1, (E,), generator=g)
+        recv, w13, s13, w2, s2 = _expert_setup(E, R, H, I, counts.tolist(), seed)
+        cd = counts.to(torch.int32).to(DEV)
+        w13, s13, w2, s2 = (t.to(DEV) for t in (w13, s13, w2, s2))
+        xq, xs = api.moe_quantize_fp8(recv.to(DEV), cd)
+        alone = api.moe_gemm_gateup_down(xq, xs, cd, w13, s13, w2, s2)
+        runs.append(dict(args=(xq, xs, cd, w13, s13, w2, s2), alone=alone, cd=counts))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(device=dev) for _ in runs]
+    st = [torch.zeros(2, dtype=torch.int32, device=DEV) for _ in runs]
+    outs = [None, None]
+    for rep in range(3):
+        for i, (r, s) in enumerate(zip(runs, streams)):
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                outs[i] = api.moe_gemm_gateup_down(*r["args"], dev_status=st[i], stream=s)
+        torch.cuda.synchronize()
+        for i, r in enumerate(runs):
+            assert st[i].cpu().tolist() == [0, 0]
+            vd = (torch.arange(R).unsqueeze(0) < r["cd"].unsqueeze(1)).to(DEV)
+            assert torch.equal(outs[i][vd].view(torch.int16), r["alone"][vd].view(torch.int16))
+
+
 # ------------------------------------------------------------------ combine
 
 def test_combine_bit_exact():
