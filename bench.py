@@ -625,9 +625,16 @@ def run_ours(args, rank, local, world):
 
 
 def workload_config(wl, extra=None) -> dict:
+    x_mb = wl.T * wl.H * 2 / 1e6
+    w_gb = wl.E * 3 * wl.H * wl.I / 1e9
+    if x_mb > 129:
+        l2 = (f"inputs larger than L2 (no flush): x ({x_mb:.0f} MB) and the FP8 weights "
+              f"({w_gb:.1f} GB) exceed 129 MB")
+    else:
+        l2 = (f"no separate flush: every step streams the FP8 weights ({w_gb:.1f} GB, larger "
+              f"than the 129 MB L2) between two uses of x ({x_mb:.1f} MB), which evicts it")
     cfg = {"workload": f"{wl.name}: T={wl.T} E={wl.E} ({wl.W}x{wl.L}) top-{wl.K} H={wl.H} I={wl.I} R={wl.R}",
-           "global_batch": wl.T, "routings": N_ROUTINGS,
-           "l2": "inputs larger than L2 (no flush): x and the FP8 weights exceed 129 MB"}
+           "global_batch": wl.T, "routings": N_ROUTINGS, "l2": l2}
     if extra:
         cfg.update(extra)
     return cfg
