@@ -163,3 +163,20 @@ def test_gemm_gateup_down_sync_size_and_rejections(lib):
     assert f(*args(rows=-1)) == -1
     assert f(*args(out=None)) == -1
     assert f(*args(zq=ctypes.c_void_p(4096 + 8))) == -1   # TMA source must be 16-byte aligned
+
+
+def test_header_compiles_as_c(tmp_path):
+    """include/moe.h is plain C: the C layer driver compiles against it with
+    gcc in C11 mode, warnings as errors (compile only; it runs in the GPU
+    tests)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if gcc is None or not os.path.isdir(cuda_inc):
+        pytest.skip("gcc or the CUDA headers not found")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-c",
+                    "-I", os.path.join(root, "include"), "-I", cuda_inc,
+                    os.path.join(root, "tests", "capi", "layer_main.c"),
+                    "-o", str(tmp_path / "layer_main.o")], check=True)
