@@ -149,7 +149,9 @@ moe_status moe_dispatch_quant(const void* x, const int64_t* topk_idx, const floa
  * the gated-SiLU expert of "SGLang Expert Compute Backend", §1.1 and §3.5-3.7:
  * G = block-scaled FP8 GEMM of x with W13 (first I output columns gate, last
  * I up), Z = SiLU(gate) * up re-quantised per row per 128, out = block-scaled
- * FP8 GEMM of Z with W2, written at the original slot (e, s).
+ * FP8 GEMM of Z with W2, written at the original slot (e, s).  Both GEMMs run
+ * in one launch (see moe_gemm_gateup_down): the down tiles of a 128-row block
+ * start once that block's Z is written.
  *
  *   recv       device, BF16 [E, R, H]          rows >= counts[e] are never read
  *   counts     device, int32 [E]               valid rows per expert (values > R act as R)
@@ -160,7 +162,9 @@ moe_status moe_dispatch_quant(const void* x, const int64_t* topk_idx, const floa
  *   out        device, BF16 [E, R, H]          out: rows [0, counts[e]); others untouched
  *   dev_status device, int32 [2]               MOE_DEV_TIMEOUT may be ORed in
  *   workspace  device, >= moe_expert_compute_workspace_size(E, R, H, I) bytes,
- *              256-byte aligned; holds the FP8 activations and their scales
+ *              256-byte aligned; holds the FP8 activations and their scales, Z
+ *              and its scales, and the GEMM launch's tile ticket and block
+ *              counts; not shared with another call in flight
  *
  * Router weights never enter this call ("SGLang、NCCL 与 MoE EP", §1.1: the
  * weight multiplies the expert output, not its input).
