@@ -26,7 +26,8 @@
  *    FP8 tensors are e4m3 (OCP "float8_e4m3fn") codes, one byte each.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream): no host synchronisation, no allocation, no host reads of
- *    device data.  All calls can be captured into a CUDA graph.
+ *    device data.  Every call except moe_dispatch_noalloc can be captured
+ *    into a CUDA graph.
  *  - Host-detectable errors (null pointers, bad sizes, workspace too small,
  *    unsupported device) return a negative moe_status before anything is
  *    launched.  MOE_ERR_CUDA means a CUDA runtime call failed; the CUDA error
@@ -103,22 +104,23 @@ moe_status moe_dispatch(const void* x, const int64_t* topk_idx, const float* top
 /* ---------------------------------------------------------------------------
  * moe_dispatch_noalloc -- the pages have no counterpart; this is a convenience
  * of this library.  The same dispatch as moe_dispatch, for callers that cannot
- * allocate device memory: code running while a CUDA graph is captured (where
- * cudaMalloc is not allowed), runtimes that forbid device allocation after
- * start-up or hand this library no allocator, and latency-critical loops that
- * cannot afford cudaMalloc's implicit device synchronisation.
+ * allocate device memory: serving runtimes that reserve all device memory at
+ * start-up and forbid allocation afterwards, hosts (plain C programs, other
+ * language runtimes) that link this library without handing it an allocator,
+ * and latency-critical loops that cannot afford cudaMalloc's implicit device
+ * synchronisation.  It calls no allocating routine of CUDA or any library.
  *
  * Arguments and outputs are those of moe_dispatch, minus the workspace: the
  * scratch is a 1 MiB array inside the library (held by every GPU that loads
  * the library until the process exits), which limits the problem to
  * moe_dispatch_workspace_size(T, K, E) <= 1 MiB, i.e. E * ceil(T / (8*(32/K)))
  * <= 262144; larger problems return MOE_ERR_WORKSPACE without launching.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call shares the one array, and nothing in it needs to start
- * at zero (each call writes every entry it reads); calls whose kernels overlap
- * on the GPU (different streams without ordering) race on it and must not be
- * issued.
+ * The first call on a device (and the first after a cudaDeviceReset) looks up
+ * the array's device address with that device current and caches it per
+ * device and context; make that first call before any stream capture.  Every
+ * call shares the one array, and nothing in it needs to start at zero (each
+ * call writes every entry it reads); calls whose kernels overlap on the GPU
+ * (different streams without ordering) race on it and must not be issued.
  * ------------------------------------------------------------------------- */
 moe_status moe_dispatch_noalloc(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
                                 int H, int K, int E, int R, void* recv, int32_t* counts,

@@ -50,6 +50,9 @@ def test_workspace_sizes(lib):
     assert lib.moe_dispatch_workspace_size(0, 2, 8) == 256
     # one int32 per (expert, block of 8 warps x 32/K tokens)
     assert lib.moe_dispatch_workspace_size(16384, 8, 256) == 256 * (16384 // 32) * 4
+    # T near INT_MAX: the block count is computed in 64 bits (no overflow)
+    big = 2**31 - 1
+    assert lib.moe_dispatch_workspace_size(big, 1, 4) == -(-big // 256) * 4 * 4
     ws = lib.moe_expert_compute_workspace_size(2, 128, 256, 128)
     # xq, xs, zq, zs, then the fused GEMM's scratch: a tile ticket and one
     # count per 128-row block (ceil(rows/128) plus one per possible expert)

@@ -8,6 +8,8 @@ the oracle (on the CPU) fails it.
 import json
 import math
 import os
+import struct
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -397,6 +399,78 @@ def test_combine_identity_experts_return_input():
     assert np.array_equal(O.f32_to_bf16_rne(y64.astype(np.float32)), x)
 
 
+# A two-route token whose products nearly cancel: the fp32 rounding of each
+# product is then as large as the sum itself, so the three plausible readings
+# of "fp32 accumulation" -- product and sum each rounded, a fused multiply-add
+# for the second term, or fp64 accumulation rounded once -- land on three
+# different BF16 values.  Inputs as bit patterns: router weights fp32, expert
+# outputs BF16 (the dtype the combine reads).
+COMBINE_ROUNDING = {"w_bits": [0x3EE87226, 0x3EDA5BAF], "v_bits": [0x3F78, 0xBF84]}
+
+
+def _f32_round(x: Fraction) -> Fraction:
+    """Nearest fp32 to an exactly representable-in-double rational (ties to
+    even): ``struct`` packs a double into binary32 with IEEE rounding."""
+    d = float(x)
+    assert Fraction(d) == x, "value not exact in fp64"
+    return Fraction(struct.unpack("<f", struct.pack("<f", d))[0])
+
+
+def _bf16_round(x: Fraction) -> float:
+    """Nearest BF16 (ties to even) of an exact rational, by exact arithmetic."""
+    if x == 0:
+        return 0.0
+    e = math.floor(math.log2(abs(x)))
+    while Fraction(2) ** e > abs(x):
+        e -= 1
+    while Fraction(2) ** (e + 1) <= abs(x):
+        e += 1
+    q = Fraction(2) ** (e - 7)                     # 8 significant bits
+    n = abs(x) / q
+    f = math.floor(n)
+    r = n - f
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and f % 2 == 1):
+        f += 1
+    return float((1 if x > 0 else -1) * f * q)
+
+
+def _combine_rounding_readings():
+    w = [Fraction(struct.unpack("<f", struct.pack("<I", b))[0]) for b in COMBINE_ROUNDING["w_bits"]]
+    v = [Fraction(struct.unpack("<f", struct.pack("<I", b << 16))[0]) for b in COMBINE_ROUNDING["v_bits"]]
+    p0 = _f32_round(w[0] * v[0])
+    two = _f32_round(p0 + _f32_round(w[1] * v[1]))     # product and sum each rounded
+    fused = _f32_round(p0 + w[1] * v[1])               # fma for the second term
+    wide = w[0] * v[0] + w[1] * v[1]                   # fp64 (exact here), rounded once
+    return w, v, {"mul_add": _bf16_round(two), "fma": _bf16_round(fused), "fp64": _bf16_round(wide)}
+
+
+def pin_combine_rounding(combine):
+    """The combine's rounding sequence (fp32, product and sum each rounded,
+    ascending k from 0, one BF16 rounding at the end), checked on a case where
+    the other readings give other results."""
+    w, v, want = _combine_rounding_readings()
+    out = np.array([[float(v[0]), 0.0], [float(v[1]), 0.0]], np.float32)
+    src = np.array([[0, 1]], np.int32)
+    ww = np.array([[float(w[0]), float(w[1])]], np.float32)
+    y = combine(out, src, ww)
+    assert y[0, 0] == want["mul_add"] and y[0, 1] == 0.0
+
+
+def test_combine_rounding_sequence():
+    """"SGLang、NCCL 与 MoE EP", §3.2: each route's output is multiplied by its
+    weight once and summed into the token's row; the accumulation is fp32 in
+    ascending k (the reading this build takes where the pages do not fix the
+    rounding).  The three readings differ on this case, so the pin tells them
+    apart; the fp64 oracle combine agrees with the fp64 reading."""
+    _, _, want = _combine_rounding_readings()
+    assert len({want["mul_add"], want["fma"], want["fp64"]}) == 3
+    pin_combine_rounding(O.combine_f32_sequential)
+    w, v, _ = _combine_rounding_readings()
+    y64 = O.combine_fp64(np.array([[float(v[0])], [float(v[1])]], np.float32), np.array([[0, 1]], np.int32),
+                         np.array([[float(w[0]), float(w[1])]], np.float32))
+    assert float(O.f32_to_bf16_rne(y64.astype(np.float32))[0, 0]) == want["fp64"]
+
+
 def test_combine_empty_rank():
     y = O.combine_f32_sequential(np.zeros((8, 16), np.float32), np.zeros((0, 2), np.int32), np.zeros((0, 2), np.float32))
     assert y.shape == (0, 16)
@@ -552,6 +626,22 @@ def test_mutants_are_caught():
     def comb_noweight(out, src, w):
         return O.combine_fp64(out, src, np.ones_like(w))
     assert _fails(pin_combine_traced, comb_noweight)
+
+    # combine with a fused multiply-add per term (one rounding per term)
+    def comb_fma(out, src, w):
+        T, K = src.shape
+        acc = np.zeros((T, out.shape[1]), np.float64)
+        for k in range(K):
+            m = src[:, k] >= 0
+            prod = w[m, k].astype(np.float64)[:, None] * out[src[m, k]].astype(np.float64)
+            acc[m] = (acc[m].astype(np.float32).astype(np.float64) + prod).astype(np.float32)
+        return O.f32_to_bf16_rne(acc.astype(np.float32))
+    assert _fails(pin_combine_rounding, comb_fma)
+
+    # combine accumulated in fp64 and rounded once
+    def comb_wide(out, src, w):
+        return O.f32_to_bf16_rne(O.combine_fp64(out, src, w).astype(np.float32))
+    assert _fails(pin_combine_rounding, comb_wide)
 
 
 def test_packed_offsets_page_example():

@@ -1,6 +1,7 @@
 """moe_dispatch_noalloc, the dispatch entry point for callers that cannot
-allocate device memory (graph capture, allocation-free runtimes, loops that
-cannot pay cudaMalloc's implicit synchronisation): called through the C ABI,
+allocate device memory (runtimes that reserve all device memory at start-up,
+hosts that give the library no allocator, loops that cannot pay cudaMalloc's
+implicit synchronisation): called through the C ABI,
 it must give exactly what moe_dispatch gives with a caller-provided workspace,
 on two calls in a row that share its built-in scratch array.  This file is
 named so pytest collects it last."""
@@ -81,6 +82,8 @@ def test_noalloc_dispatch_rejects_problems_beyond_its_scratch():
     # E * ceil(T / 32) int32 = 1024 * 2048 * 4 bytes = 8 MiB > 1 MiB
     T, K, E = 65536, 8, 1024
     assert lib.moe_dispatch_workspace_size(T, K, E) > (1 << 20)
-    fake = ctypes.c_void_p(4096)
-    rc = lib.moe_dispatch_noalloc(fake, fake, None, T, 256, K, E, 16, fake, fake, fake, fake, None)
+    # Null pointers throughout: the size check must answer first; were it
+    # missing, the dispatch would reject the null pointers on the host and
+    # still launch nothing.
+    rc = lib.moe_dispatch_noalloc(None, None, None, T, 256, K, E, 16, None, None, None, None, None)
     assert rc == -3

@@ -1,12 +1,13 @@
 // moe_dispatch_noalloc: dispatch for callers that cannot allocate device
-// memory.  Some callers have no way to obtain a workspace: code that runs
-// while a CUDA graph is being captured (cudaMalloc is not allowed there),
-// runtimes that forbid device allocation after start-up or give this library
-// no allocator, and latency-critical loops that cannot pay for cudaMalloc's
-// implicit device synchronisation.  This entry point needs no workspace
-// argument: its scratch (the per-block route histograms) lives in a
+// memory.  Some callers have no way to obtain a workspace: serving runtimes
+// that reserve all device memory at start-up and forbid allocation afterwards,
+// hosts (plain C programs, other language runtimes) that link this library
+// without handing it an allocator, and latency-critical loops that cannot pay
+// for cudaMalloc's implicit device synchronisation.  This entry point needs no
+// workspace argument: its scratch (the per-block route histograms) lives in a
 // file-scope device array of fixed size that every GPU loading this library
 // holds until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -21,20 +22,51 @@ static __device__ __align__(256) unsigned char g_dispatch_scratch[kNoAllocScratc
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+// Per device: the context the address was looked up in, and the address.
+CUcontext g_scratch_ctx[kMaxDevices];
 void* g_scratch_ptr[kMaxDevices];
 
-// Device address of the scratch array on the current device.  In host code
-// the array's name is only a host-side stand-in, so the address is looked up
-// once per device with that device current and cached.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry point (no link-time
+// dependency on the driver library); nullptr if it cannot be resolved.
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  return fn;
+}
+
+// Device address of the scratch array in the current device's current
+// context.  In host code the array's name is only a host-side stand-in, so the
+// address is looked up with that device current and cached per device; the
+// cache is keyed by the context as well, because after cudaDeviceReset the
+// module is loaded again into a new context, possibly at another address.
 moe_status scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  CUcontext ctx = nullptr;
+  if (get_ctx == nullptr || get_ctx(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  if (ctx == nullptr) {
+    // No context current yet: cudaSetDevice initialises the device's primary
+    // context (the one the launches below use) and makes it current.
+    if (cudaSetDevice(dev) != cudaSuccess || get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+      return MOE_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || p == nullptr)
       return MOE_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return MOE_OK;

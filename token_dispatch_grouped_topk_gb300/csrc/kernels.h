@@ -35,10 +35,13 @@ inline RowLayout padded_rows(int E, int R) { return RowLayout{R, 0, static_cast<
 constexpr int kDispatchWarps = 8;
 inline int dispatch_tokens_per_warp(int K) { return 32 / K; }
 inline int dispatch_tokens_per_block(int K) { return kDispatchWarps * (32 / K); }
-inline int dispatch_blocks(int T, int K) {
-  const int tpb = dispatch_tokens_per_block(K);
+// Blocks of the routing kernels; computed in 64 bits so T near INT_MAX cannot
+// overflow (callers bound T * K below 2^31, so the result fits an int).
+inline int64_t dispatch_blocks64(int64_t T, int K) {
+  const int64_t tpb = dispatch_tokens_per_block(K);
   return (T + tpb - 1) / tpb;
 }
+inline int dispatch_blocks(int T, int K) { return static_cast<int>(dispatch_blocks64(T, K)); }
 // topk_idx holds int64 ids (idx_bits = 64) or int32 ids (idx_bits = 32).
 cudaError_t launch_dispatch(const void* x, const void* topk_idx, int idx_bits, int T, int H, int K,
                             int E, RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,

@@ -136,7 +136,7 @@ const char* moe_status_string(moe_status s) {
 
 size_t moe_dispatch_workspace_size(int T, int K, int E) {
   if (T < 0 || K < 1 || K > 32 || E < 1) return 0;
-  const size_t nb = static_cast<size_t>(dispatch_blocks(T, K));
+  const size_t nb = static_cast<size_t>(dispatch_blocks64(T, K));
   return align_up(std::max<size_t>(nb * E * sizeof(int32_t), 1), 256);
 }
 
