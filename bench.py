@@ -72,6 +72,49 @@ def load_peaks() -> dict:
                 "source": "fallback"}
 
 
+def measure_fp8_peak(device, n: int = 8192, sustained_s: float = 4.0) -> dict:
+    """Dense e4m3 GEMM throughput of this GPU through cuBLASLt
+    (torch._scaled_mm, per-tensor scales, BF16 output), n^3 with 2 n^3 FLOPs:
+    the best of 10 timed calls (burst) and the rate of calls back to back for
+    `sustained_s` seconds (sustained, under the power cap)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(0)
+    a = torch.randn(n, n, device=device, generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device=device, generator=g).to(torch.float8_e4m3fn).t()
+    one = torch.ones((), device=device, dtype=torch.float32)
+    mm = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    flops = 2.0 * n ** 3
+    best = float("inf")
+    for _ in range(10):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        mm()
+        e.record()
+        e.synchronize()
+        best = min(best, s.elapsed_time(e))
+    # sustained: batches of 20 calls until sustained_s has passed
+    calls, t0 = 0, time.perf_counter()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    while time.perf_counter() - t0 < sustained_s:
+        for _ in range(20):
+            mm()
+        calls += 20
+        torch.cuda.synchronize()
+    e.record()
+    e.synchronize()
+    sus_ms = s.elapsed_time(e) / calls
+    del a, b
+    torch.cuda.empty_cache()
+    return {"fp8_tflops": flops / (best * 1e-3) / 1e12, "fp8_tflops_sustained": flops / (sus_ms * 1e-3) / 1e12,
+            "how": f"torch._scaled_mm e4m3 {n}^3 (2n^3 FLOPs), per-tensor scales, bf16 out: best of 10 "
+                   f"(burst) and {calls} calls back to back over {sustained_s:.0f} s (sustained)"}
+
+
 def kernel_sources_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "token_dispatch_grouped_topk_gb300", "csrc")
