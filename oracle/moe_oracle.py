@@ -39,7 +39,7 @@ __all__ = [
     "QUANT_GROUP", "E4M3_MAX",
     "e4m3_decode", "e4m3_encode", "bf16_bits_to_f32", "f32_to_bf16_rne",
     "f32_to_bf16_bits", "expert_placement", "RouteResult", "route", "scatter",
-    "packed_row_offsets", "packed_src_map",
+    "packed_row_offsets", "packed_src_map", "SourceSlotResult", "route_source_slots",
     "route_stats", "quantize_rows", "gemm_block_scaled", "silu",
     "expert_forward", "combine_fp64", "combine_f32_sequential", "moe_layer",
     "m_blocks", "valid_tiles", "m_fill_rate", "align_index_capacity",
@@ -224,6 +224,57 @@ def packed_src_map(src_map: np.ndarray, counts, R: int) -> np.ndarray:
             e, s = divmod(int(q), R)
             out[idx] = off[e] + s
     return out
+
+
+@dataclass
+class SourceSlotResult:
+    counts: np.ndarray        # [E] int32, valid rows per expert (masked_m)
+    seg_counts: np.ndarray    # [E, W] int32, valid rows per (expert, source rank)
+    src_map: np.ndarray       # [T, K] int32, q = e*W*max_tokens + r*max_tokens + p, or -1
+    dropped: int              # routes past their source's slot range
+    bad_id: bool              # some id outside [-1, E)
+
+
+def route_source_slots(topk_idx: np.ndarray, E: int, L: int, max_tokens: int,
+                       src_rank: np.ndarray) -> SourceSlotResult:
+    """The low-latency receive layout of "DeepEP 架构与实现笔记", §9.5: the
+    receive buffer is [L, W*max_tokens, H] and every source rank owns a fixed
+    range of max_tokens slots inside every expert, so a route's row follows
+    from its source rank r and its position p among r's routes to that expert
+    -- row r*max_tokens + p -- with no layout agreed across ranks first.  Valid
+    rows are therefore not one prefix per expert: each (expert, source) range
+    holds its own valid count, and the rows between are padding.  Positions
+    are taken in ascending route id (the canonical order of ``route``); a route
+    whose position reaches max_tokens has no slot and is dropped.  Here the
+    experts of all ranks share one buffer [E, W*max_tokens, H], so the flat
+    row is q = e*W*max_tokens + r*max_tokens + p."""
+    topk_idx = np.asarray(topk_idx)
+    T, K = topk_idx.shape
+    W = E // L
+    R = W * max_tokens
+    fill = np.zeros((E, W), dtype=np.int64)
+    src_map = np.full((T, K), -1, dtype=np.int32)
+    dropped = 0
+    bad = False
+    ids = topk_idx.tolist()
+    for t in range(T):
+        r = int(src_rank[t])
+        for k in range(K):
+            e = int(ids[t][k])
+            if e == -1:
+                continue
+            if e < -1 or e >= E:
+                bad = True
+                continue
+            p = int(fill[e, r])
+            fill[e, r] += 1
+            if p < max_tokens:
+                src_map[t, k] = e * R + r * max_tokens + p
+            else:
+                dropped += 1
+    seg = np.minimum(fill, max_tokens).astype(np.int32)
+    return SourceSlotResult(counts=seg.sum(axis=1).astype(np.int32), seg_counts=seg,
+                            src_map=src_map, dropped=dropped, bad_id=bad)
 
 
 def route_stats(topk_idx: np.ndarray, L: int, src_rank: np.ndarray) -> dict:

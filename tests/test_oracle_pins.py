@@ -197,6 +197,64 @@ def test_replay_counts():
     assert [int(rr0.counts[e]) for e in TRACED["replay"]["experts"]] == TRACED["replay"]["before"]
 
 
+def pin_source_slots_traced(fn):
+    """The per-source fixed-slot layout ("DeepEP 架构与实现笔记", §9.5) on the
+    traced scenario with the pages' own per-rank slot count C = 64 (W = 4, so
+    each expert holds W*C = 256 rows): E0 receives 16, 31 and 64 routes from
+    source ranks 1, 2 and 3 ("SGLang、NCCL 与 MoE EP", §2.3.7), each group in
+    its own source's 64-row range; masked_m equals the global counts."""
+    idx, _ = traced_ids()
+    src = W.source_rank_of_tokens(W.WORKLOADS["traced"]).numpy()
+    C = TRACED["flat_row_e1"]["M"] // 4
+    res = fn(idx, 8, 2, C, src)
+    assert res.seg_counts[0].tolist() == [0] + TRACED["rank0_e0_sources"]["value"]
+    assert res.seg_counts[7].tolist() == [0] + TRACED["rank0_e0_sources"]["value"]
+    assert res.seg_counts[1].tolist() == [0, 0, 1, 0] == res.seg_counts[6].tolist()
+    assert res.counts.tolist() == TRACED["counts"]["global"]
+    # token (2, 5) = global 21: source rank 2's first slot of E1 and of E6
+    M = 4 * C
+    assert res.src_map[16 + 5].tolist() == [1 * M + 2 * C, 6 * M + 2 * C]
+    # the first token of rank 3 (global 48) opens rank 3's range of E0 and E7
+    assert res.src_map[48].tolist() == [0 * M + 3 * C, 7 * M + 3 * C]
+    assert res.dropped == 0 and not res.bad_id
+
+
+def test_source_slot_layout_pins():
+    pin_source_slots_traced(O.route_source_slots)
+
+
+def test_source_slot_layout_invariants():
+    """Every route sits in its source's fixed range of its expert; read in row
+    order, an expert's valid rows list the same routes as the canonical padded
+    layout (sources are concatenated in token order); a source with more
+    routes to one expert than its range holds drops the later ones."""
+    rng = np.random.default_rng(12)
+    E, L, K, T = 16, 4, 3, 90
+    W_ = E // L
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int64)
+    idx[rng.random((T, K)) < 0.1] = -1
+    src = np.minimum(np.arange(T) // -(-T // W_), W_ - 1)
+    mt = 40
+    res = O.route_source_slots(idx, E, L, mt, src)
+    R = W_ * mt
+    canon = O.route(idx, E, R)
+    assert res.dropped == 0 and canon.dropped == 0
+    assert res.counts.tolist() == canon.counts.tolist()
+    for e in range(E):
+        rows = {}
+        for t, k in np.argwhere(res.src_map // R == e):
+            q = int(res.src_map[t, k]) - e * R
+            r, p = divmod(q, mt)
+            assert r == src[t] and p < res.seg_counts[e, r]
+            rows[q] = (t, k)
+        in_row_order = [rows[q] for q in sorted(rows)]
+        by_slot = sorted((int(canon.src_map[t, k]), (t, k)) for t, k in np.argwhere(canon.src_map // R == e))
+        assert in_row_order == [tk for _, tk in by_slot]
+    small = O.route_source_slots(idx, E, L, 2, src)
+    assert small.dropped == int(np.maximum(res.seg_counts - 2, 0).sum())
+    assert small.seg_counts.max() <= 2
+
+
 def test_placement_and_byte_accounting():
     p = TRACED["placement"]
     for g, r, l in p["routes"]:
@@ -626,6 +684,18 @@ def test_mutants_are_caught():
     def comb_noweight(out, src, w):
         return O.combine_fp64(out, src, np.ones_like(w))
     assert _fails(pin_combine_traced, comb_noweight)
+
+    # per-source slots without the source's range offset (a packed prefix)
+    def slots_noseg(idx, E, L, mt, src):
+        res = O.route_source_slots(idx, E, L, mt, src)
+        rr = O.route(idx, E, (E // L) * mt)
+        return O.SourceSlotResult(res.counts, res.seg_counts, rr.src_map, res.dropped, res.bad_id)
+    assert _fails(pin_source_slots_traced, slots_noseg)
+
+    # slot range chosen by the destination rank instead of the source rank
+    def slots_dest(idx, E, L, mt, src):
+        return O.route_source_slots(idx, E, L, mt, np.asarray(idx)[:, 0] // L)
+    assert _fails(pin_source_slots_traced, slots_dest)
 
     # combine with a fused multiply-add per term (one rounding per term)
     def comb_fma(out, src, w):
