@@ -146,14 +146,30 @@ moe_status moe_dispatch_quant(const void* x, const int64_t* topk_idx, const floa
                               size_t workspace_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_dispatch_quant_ex -- the general fused dispatch: moe_dispatch_quant is
+ * its int64, padded case.  idx_bits (32 or 64) and rows (0: padded layout,
+ * xq [E, R, H] / xs [E, R, H/128]; > 0: packed layout, xq [rows, H] / xs
+ * [rows, H/128], rows as for moe_dispatch_packed) as for moe_dispatch_ex.
+ * Outputs equal moe_quantize_fp8's on moe_dispatch_ex's receive rows, bit for
+ * bit, with the src_map, counts and status of moe_dispatch_ex.
+ * ------------------------------------------------------------------------- */
+moe_status moe_dispatch_quant_ex(const void* x, const void* topk_idx, int idx_bits,
+                                 const float* topk_w, int T, int H, int K, int E, int R,
+                                 int64_t rows, uint8_t* xq, float* xs, int32_t* counts,
+                                 int32_t* src_map, int32_t* dev_status, void* workspace,
+                                 size_t workspace_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Expert compute -- per-token FP8 quantisation of the valid receive rows
  * ("SGLang、NCCL 与 MoE EP", §2.3.5; rule of "DeepEP 架构与实现笔记", §11), then
  * the gated-SiLU expert of "SGLang Expert Compute Backend", §1.1 and §3.5-3.7:
  * G = block-scaled FP8 GEMM of x with W13 (first I output columns gate, last
  * I up), Z = SiLU(gate) * up re-quantised per row per 128, out = block-scaled
- * FP8 GEMM of Z with W2, written at the original slot (e, s).  Both GEMMs run
- * in one launch (see moe_gemm_gateup_down): the down tiles of a 128-row block
- * start once that block's Z is written.
+ * FP8 GEMM of Z with W2, written at the original slot (e, s).  When the
+ * gate/up tiles fill only a few waves of CTAs (decode-sized layers) both GEMMs
+ * run in one launch (see moe_gemm_gateup_down: the down tiles of a 128-row
+ * block start once that block's Z is written); otherwise as two launches,
+ * which measured faster there.
  *
  *   recv       device, BF16 [E, R, H]          rows >= counts[e] are never read
  *   counts     device, int32 [E]               valid rows per expert (values > R act as R)
@@ -220,13 +236,15 @@ moe_status moe_gemm_down(const uint8_t* zq, const float* zs, const int32_t* coun
 
 /* ---------------------------------------------------------------------------
  * moe_gemm_gateup_down -- moe_gemm_gateup_silu followed by moe_gemm_down, in
- * one persistent launch.  The arithmetic is that of "SGLang Expert Compute
- * Backend", §3.5-3.7.  The scheduling applies the tile events of "XTuner
- * Domino EP" (HyperParallel-MoE section, from whole collectives to
- * destination tile events): a task waits on a per-tile counter reaching its
- * threshold rather than on the whole preceding operator.  Here a down tile of
- * a 128-row block starts once every gate/up tile of that block has written
- * its Z rows.  Results are bit-identical to the two calls.
+ * one persistent launch where that is the faster form, else as those two
+ * launches (the MOE_GEMM_* flags of moe_expert_compute_ex; MOE_GEMM_ONE_LAUNCH
+ * always takes the one launch).  The arithmetic is that of "SGLang Expert
+ * Compute Backend", §3.5-3.7.  The scheduling of the one launch applies the
+ * tile events of "XTuner Domino EP" (HyperParallel-MoE section, from whole
+ * collectives to destination tile events): a task waits on a per-tile counter
+ * reaching its threshold rather than on the whole preceding operator.  Here a
+ * down tile of a 128-row block starts once every gate/up tile of that block
+ * has written its Z rows.  Results are bit-identical to the two calls.
  *
  *   xq, xs     as for moe_gemm_gateup_silu, in the layout given by rows:
  *              rows = 0 padded [E, R, ...], rows > 0 packed [rows, ...]
@@ -236,11 +254,12 @@ moe_status moe_gemm_down(const uint8_t* zq, const float* zs, const int32_t* coun
  *   sync       device scratch of moe_gemm_gateup_down_sync_size(E, R, rows)
  *              bytes, 4-byte aligned, overwritten (zeroed) by the call;
  *              not shared with another call in flight
- *   flags      0 or MOE_W13_INTERLEAVED (see moe_expert_compute_ex)
+ *   flags      MOE_W13_INTERLEAVED, MOE_GEMM_ONE_LAUNCH, MOE_GEMM_TWO_LAUNCHES
+ *              (see moe_expert_compute_ex)
  * Returns MOE_ERR_INVALID_ARG for bad sizes, pointers or flags,
  * MOE_ERR_WORKSPACE if sync is too small.  Waits between tiles are bounded:
  * one that runs out raises MOE_DEV_TIMEOUT in dev_status.  moe_expert_compute
- * and its variants run this launch after their quantisation.
+ * and its variants run these GEMMs, in the same form, after their quantisation.
  * ------------------------------------------------------------------------- */
 size_t moe_gemm_gateup_down_sync_size(int E, int R, int64_t rows);
 moe_status moe_gemm_gateup_down(const uint8_t* xq, const float* xs, const int32_t* counts, int E,
@@ -313,16 +332,69 @@ moe_status moe_dispatch_ex(const void* x, const void* topk_idx, int idx_bits, co
  *          output columns of the first GEMM and multiplies by the odd ones.
  *          Default: the first I rows gate, the last I up ("SGLang Expert
  *          Compute Backend", §3.6).
+ *          MOE_GEMM_ONE_LAUNCH / MOE_GEMM_TWO_LAUNCHES: force the GEMMs' launch
+ *          form (see below); at most one of them.
  * Workspace: moe_expert_compute_ex_workspace_size(E, R, rows, H, I) bytes.
  * MOE_ERR_INVALID_ARG for unknown flag bits.
  * ------------------------------------------------------------------------- */
 #define MOE_W13_INTERLEAVED 1
+/* How the two GEMMs are launched (results are bit-identical either way): by
+ * default one launch (moe_gemm_gateup_down) when the gate/up tiles fill only a
+ * few waves of CTAs, else the gate/up launch followed by the down launch.
+ * These flags force one form or the other. */
+#define MOE_GEMM_ONE_LAUNCH 2
+#define MOE_GEMM_TWO_LAUNCHES 4
 size_t moe_expert_compute_ex_workspace_size(int E, int R, int64_t rows, int H, int I);
 moe_status moe_expert_compute_ex(const void* recv, const int32_t* counts, int E, int R, int64_t rows,
                                  int H, int I, const uint8_t* w13, const float* w13_scale,
                                  const uint8_t* w2, const float* w2_scale, void* out,
                                  int32_t* dev_status, void* workspace, size_t workspace_bytes,
                                  int flags, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_layer_stats -- the counts the pages account a layer by, for one routing:
+ * "SGLang、NCCL 与 MoE EP", §5.3 (each token sends one payload per distinct
+ * destination rank, D_t of them, §2.3.2; routes to an expert on another logical
+ * rank than the token's are cross-rank) and "SGLang Expert Compute Backend",
+ * §5.4 (M-row fill of the grouped GEMM's blocks).
+ *
+ *   topk_idx     device, [T, K] int32 (idx_bits = 32) or int64 router ids;
+ *                ids outside [0, E) do not count as routes
+ *   counts       device, int32 [E]: kept rows per expert (moe_dispatch's output)
+ *   L            local experts per logical rank (E % L == 0); expert g lives on
+ *                rank g / L
+ *   rank_offsets device, int32 [E/L + 1]: token t comes from the rank r with
+ *                rank_offsets[r] <= t < rank_offsets[r+1] (tokens concatenated
+ *                in rank order), or NULL: ceil(T / (E/L)) tokens per rank
+ *   stats        device, uint64 [7], 8-byte aligned, overwritten:
+ *                [0] valid routes  [1] kept routes (dropped = [0] - [1])
+ *                [2] messages, sum over tokens of D_t  [3] cross-rank routes
+ *                [4] 128-row blocks of the GEMM tile list, sum_e ceil(c_e/128)
+ *                    (M-row fill = [1] / (128 * [4]); a capacity-dense launch
+ *                    covers E * ceil(R/128) blocks)
+ *                [5] active experts  [6] the busiest expert's kept rows
+ * Asynchronous on `stream` like the other calls.
+ * ------------------------------------------------------------------------- */
+moe_status moe_layer_stats(const void* topk_idx, int idx_bits, const int32_t* counts, int T, int K,
+                           int E, int L, int R, const int32_t* rank_offsets, uint64_t* stats,
+                           moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_expert_compute_workspace_layout -- where moe_expert_compute_ex (and so
+ * moe_expert_compute and moe_expert_compute_packed) keeps its intermediate
+ * tensors inside the workspace, for callers that want to read them (FP8
+ * activations, Z) or to run moe_dispatch_quant + moe_gemm_gateup_down on the
+ * same workspace.  rows = 0: padded layout (E*R rows), else the packed row
+ * count.  Writes 7 byte counts to offsets:
+ *   [0] xq   e4m3 [rows, H]          [1] xs  fp32 [rows, H/128]
+ *   [2] zq   e4m3 [rows, I]          [3] zs  fp32 [rows, I/128]
+ *   [4] the GEMM launch's sync scratch, [5] its size in bytes
+ *   [6] the workspace size (= moe_expert_compute_ex_workspace_size)
+ * Every offset is a multiple of 256.  Returns MOE_ERR_INVALID_ARG for bad
+ * sizes or a null offsets pointer.  Host only; touches no device memory.
+ * ------------------------------------------------------------------------- */
+int moe_expert_compute_workspace_layout(int E, int R, int64_t rows, int H, int I,
+                                        size_t* offsets);
 
 /* ---------------------------------------------------------------------------
  * moe_selftest_bounded_wait -- exercises the device-side failure path: the

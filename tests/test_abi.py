@@ -62,6 +62,26 @@ def test_workspace_sizes(lib):
     assert lib.moe_expert_compute_workspace_size(2, 128, 200, 128) == 0   # H % 128 != 0
 
 
+@pytest.mark.parametrize("E,R,rows,H,I", [(2, 128, 0, 256, 128), (256, 4096, 0, 7168, 2048),
+                                          (128, 2048, 32768, 4096, 1536), (3, 5, 7, 128, 384)])
+def test_workspace_layout_is_the_carved_one(lib, E, R, rows, H, I):
+    """The workspace offsets the library exports (and api.MoeLayerBuffers'
+    views use) are ordered, 256-byte aligned, hold each part's bytes, and end
+    at the size the workspace-size query returns."""
+    off = (ctypes.c_size_t * 7)()
+    assert lib.moe_expert_compute_workspace_layout(E, R, rows, H, I, off) == 0
+    xq, xs, zq, zs, sync, sync_bytes, total = list(off)
+    n = rows or E * R
+    parts = [(xq, n * H), (xs, n * (H // 128) * 4), (zq, n * I), (zs, n * (I // 128) * 4),
+             (sync, sync_bytes)]
+    for (o, size), (o_next, _) in zip(parts, parts[1:] + [(total, 0)]):
+        assert o % 256 == 0 and o + size <= o_next
+    assert total == lib.moe_expert_compute_ex_workspace_size(E, R, rows, H, I)
+    assert sync_bytes >= lib.moe_gemm_gateup_down_sync_size(E, R, rows)
+    assert lib.moe_expert_compute_workspace_layout(E, R, rows, 200, I, off) == -1
+    assert lib.moe_expert_compute_workspace_layout(E, R, rows, H, I, None) == -1
+
+
 FAKE = ctypes.c_void_p(4096)   # aligned, never dereferenced: validation fails first
 
 
@@ -162,7 +182,8 @@ def test_gemm_gateup_down_sync_size_and_rejections(lib):
     assert f(*args(sync=None)) == -3
     assert f(*args(sync=ctypes.c_void_p(4096 + 2))) == -3  # counts are 4-byte words
     assert f(*args(H=200)) == -1
-    assert f(*args(flags=2)) == -1                        # unknown flag bit
+    assert f(*args(flags=8)) == -1                        # unknown flag bit
+    assert f(*args(flags=2 | 4)) == -1                    # one launch and two launches at once
     assert f(*args(rows=-1)) == -1
     assert f(*args(out=None)) == -1
     assert f(*args(zq=ctypes.c_void_p(4096 + 8))) == -1   # TMA source must be 16-byte aligned

@@ -247,3 +247,52 @@ def test_interleaved_w13_matches_oracle():
         ref, _, _, _ = O.expert_forward(xq, sx, u8(w13[e]), f32(s13[e]), u8(w2[e]), f32(s2[e]),
                                         interleaved=True)
         assert_rows_close(f32(out[e, :c]), ref, what=f"expert {e}")
+
+
+@pytest.mark.parametrize("bits,packed", [(32, False), (64, True), (32, True)])
+def test_dispatch_quant_ex_variants(bits, packed):
+    """moe_dispatch_quant_ex with int32 ids and/or the packed layout: the
+    source map is the oracle's (packed: its packed map), and every kept row
+    holds the oracle's e4m3 codes and scales of its token row."""
+    T, E, K, R, H = 700, 24, 6, 150, 512
+    g = torch.Generator().manual_seed(41 + bits + packed)
+    idx = torch.randint(-1, E, (T, K), generator=g)
+    idx[:, 0] = torch.randint(0, 3, (T,), generator=g)      # hot experts overflow R
+    idx[4, 1] = E + 2                                        # invalid id
+    x = (torch.randn(T, H, generator=g) * torch.rand(T, 1, generator=g) * 4).to(torch.bfloat16)
+    rows = api.packed_rows(T, K, E, R) if packed else 0
+    xd = x.to(DEV)
+    idd = idx.to(DEV).to(torch.int32 if bits == 32 else torch.int64)
+    xq, xs, counts, src, st = api.moe_dispatch_quant(xd, idd, None, E, R, rows=rows)
+    torch.cuda.synchronize()
+    rr = O.route(idx.numpy(), E, R)
+    want_map = O.packed_src_map(rr.src_map, rr.counts, R) if packed else rr.src_map
+    assert counts.cpu().numpy().tolist() == rr.counts.tolist()
+    assert np.array_equal(src.cpu().numpy(), want_map)
+    stv = st.cpu().tolist()
+    assert stv[1] == rr.dropped and bool(stv[0] & api.DEV_BAD_EXPERT_ID)
+    keep = want_map >= 0
+    q = torch.from_numpy(want_map[keep]).long()
+    tok = np.nonzero(keep)[0]
+    codes, scales = O.quantize_rows(x.float().numpy()[tok])
+    assert np.array_equal(xq.view(-1, H).cpu()[q].numpy(), codes)
+    assert np.array_equal(xs.view(-1, H // 128).cpu()[q].numpy(), scales)
+
+
+@pytest.mark.parametrize("name,packed,bits", [("traced", True, 64), ("decode", True, 32),
+                                              ("prefill", True, 64), ("decode", False, 32)])
+def test_layer_fused_path_every_variant(name, packed, bits):
+    """The fused dispatch+quant layer path on packed lanes and int32 ids is
+    bit-identical to the unfused padded path."""
+    d = W.make_layer_inputs(name, seed=8, device=DEV)
+    wl = d["wl"]
+    dev = torch.device(DEV)
+    ids = d["topk_idx"].to(torch.int32) if bits == 32 else d["topk_idx"]
+    wts = (d["w13"], d["s13"], d["w2"], d["s2"])
+    ref = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
+    y_ref = ref.forward(d["x"], d["topk_idx"], d["topk_w"], *wts).clone()
+    lane = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev, packed=packed)
+    y = lane.forward_fused(d["x"], ids, d["topk_w"], *wts)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y), _bits(y_ref))
+    assert lane.dev_status.cpu().tolist() == ref.dev_status.cpu().tolist()

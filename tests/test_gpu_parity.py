@@ -76,6 +76,29 @@ def test_dispatch_random_small(E, K):
             check_dispatch(xd, idd, E, R, recv, counts, src_map, st)
 
 
+@pytest.mark.parametrize("T,K", [(512, 8), (513, 8), (4096, 1), (4097, 1)])
+def test_dispatch_single_pass_threshold(T, K):
+    """Both sides of the single-kernel threshold (T*K <= 4096 routes: every
+    block counts the routes before its own; above it: histogram, scan,
+    scatter) give the oracle's canonical slots, counts and status, with
+    capacity drops and an invalid id, padded and packed, int64 and int32 ids."""
+    E, R, H = 40, 60, 256
+    g = torch.Generator().manual_seed(T * 7 + K)
+    idx = torch.randint(-1, E, (T, K), generator=g)
+    idx[:, 0] = torch.randint(0, 4, (T,), generator=g)
+    idx[T // 2, 0] = E + 1
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16)
+    xd, idd = x.to(DEV), idx.to(DEV)
+    recv, counts, src_map, st = api.moe_dispatch(xd, idd, None, E, R)
+    torch.cuda.synchronize()
+    rr = check_dispatch(xd, idd, E, R, recv, counts, src_map, st)
+    assert rr.dropped > 0 and rr.bad_id
+    precv, pc, pm, pst = api.moe_dispatch_packed(xd, idd.to(torch.int32), None, E, R)
+    torch.cuda.synchronize()
+    assert torch.equal(pc, counts) and torch.equal(pst, st)
+    assert np.array_equal(pm.cpu().numpy(), O.packed_src_map(rr.src_map, rr.counts, R))
+
+
 def test_dispatch_empty_rank_resets_counts():
     counts = torch.full((8,), 99, dtype=torch.int32, device=DEV)
     x = torch.empty(0, 256, dtype=torch.bfloat16, device=DEV)
@@ -273,7 +296,8 @@ def test_gemm_gateup_down_matches_stage_calls(E, R, H, I, seed):
     outs = []
     for _ in range(3):
         outs.append(api.moe_gemm_gateup_down(xq, xs, cd, w13, s13, w2, s2, zq=zq2, zs=zs2,
-                                             out=sentinel.clone(), sync=sync, dev_status=st))
+                                             out=sentinel.clone(), sync=sync, dev_status=st,
+                                             gemm_launch="one"))
     torch.cuda.synchronize()
     assert st.cpu().tolist() == [0, 0]
     valid = torch.arange(R).unsqueeze(0) < counts.unsqueeze(1)          # [E, R]
@@ -286,10 +310,12 @@ def test_gemm_gateup_down_matches_stage_calls(E, R, H, I, seed):
     xq_p, xs_p = xq[vd].contiguous(), xs[vd].contiguous()
     rows = xq_p.shape[0]
     if rows > 0:
-        out_p = api.moe_gemm_gateup_down(xq_p, xs_p, cd, w13, s13, w2, s2, R=R, dev_status=st)
-        torch.cuda.synchronize()
-        assert st.cpu().tolist() == [0, 0]
-        assert torch.equal(out_p.view(torch.int16), out1[vd].view(torch.int16))
+        for form in ("one", "two"):
+            out_p = api.moe_gemm_gateup_down(xq_p, xs_p, cd, w13, s13, w2, s2, R=R, dev_status=st,
+                                             gemm_launch=form)
+            torch.cuda.synchronize()
+            assert st.cpu().tolist() == [0, 0]
+            assert torch.equal(out_p.view(torch.int16), out1[vd].view(torch.int16)), form
 
 
 def test_gemm_gateup_down_two_streams_at_once():
@@ -308,7 +334,7 @@ def test_gemm_gateup_down_two_streams_at_once():
         cd = counts.to(torch.int32).to(DEV)
         w13, s13, w2, s2 = (t.to(DEV) for t in (w13, s13, w2, s2))
         xq, xs = api.moe_quantize_fp8(recv.to(DEV), cd)
-        alone = api.moe_gemm_gateup_down(xq, xs, cd, w13, s13, w2, s2)
+        alone = api.moe_gemm_gateup_down(xq, xs, cd, w13, s13, w2, s2, gemm_launch="one")
         runs.append(dict(args=(xq, xs, cd, w13, s13, w2, s2), alone=alone, cd=counts))
     torch.cuda.synchronize()
     streams = [torch.cuda.Stream(device=dev) for _ in runs]
@@ -318,12 +344,32 @@ def test_gemm_gateup_down_two_streams_at_once():
         for i, (r, s) in enumerate(zip(runs, streams)):
             s.wait_stream(torch.cuda.current_stream())
             with torch.cuda.stream(s):
-                outs[i] = api.moe_gemm_gateup_down(*r["args"], dev_status=st[i], stream=s)
+                outs[i] = api.moe_gemm_gateup_down(*r["args"], dev_status=st[i], stream=s,
+                                                   gemm_launch="one")
         torch.cuda.synchronize()
         for i, r in enumerate(runs):
             assert st[i].cpu().tolist() == [0, 0]
             vd = (torch.arange(R).unsqueeze(0) < r["cd"].unsqueeze(1)).to(DEV)
             assert torch.equal(outs[i][vd].view(torch.int16), r["alone"][vd].view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_layer_gemm_launch_forms_bit_identical(name):
+    """The layer with its GEMMs forced into one launch and into two launches
+    gives the same bytes (the default picks one of the two by tile count)."""
+    d = W.make_layer_inputs(name, seed=9, device=DEV)
+    wl = d["wl"]
+    args = (d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
+    ys = []
+    for form in ("one", "two", None):
+        buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV),
+                                  gemm_launch=form)
+        ys.append(buf.forward(*args).clone())
+        torch.cuda.synchronize()
+        assert buf.dev_status[0].item() & api.DEV_TIMEOUT == 0
+        del buf
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
+    assert torch.equal(ys[0].view(torch.int16), ys[2].view(torch.int16))
 
 
 # ------------------------------------------------------------------ combine

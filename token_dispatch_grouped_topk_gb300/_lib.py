@@ -28,6 +28,9 @@ SIGNATURES = {
     "moe_dispatch_quant": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                    c_size_t, c_void_p]),
+    "moe_dispatch_quant_ex": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
+                                      c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p,
+                                      c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_expert_compute_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
     "moe_expert_compute": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p,
                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -56,6 +59,9 @@ SIGNATURES = {
     "moe_expert_compute_ex": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int64, c_int, c_int,
                                       c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                       c_void_p, c_size_t, c_int, c_void_p]),
+    "moe_layer_stats": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                c_void_p, c_void_p, c_void_p]),
+    "moe_expert_compute_workspace_layout": (c_int, [c_int, c_int, c_int64, c_int, c_int, c_void_p]),
     "moe_gemm_gateup_down_sync_size": (c_size_t, [c_int, c_int, c_int64]),
     "moe_gemm_gateup_down": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int64, c_int,
                                      c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -63,6 +69,8 @@ SIGNATURES = {
                                      c_void_p]),
 }
 W13_INTERLEAVED = 1
+GEMM_ONE_LAUNCH = 2
+GEMM_TWO_LAUNCHES = 4
 
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED",
           -3: "MOE_ERR_WORKSPACE", -4: "MOE_ERR_CUDA"}

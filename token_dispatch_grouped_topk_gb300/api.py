@@ -6,6 +6,7 @@ passed in are allocated with torch on the input's device.
 """
 from __future__ import annotations
 
+import ctypes
 from dataclasses import dataclass
 
 import torch
@@ -13,11 +14,12 @@ import torch
 from . import _lib
 
 __all__ = [
-    "MoeError", "dispatch_workspace_size", "expert_compute_workspace_size", "moe_dispatch",
+    "MoeError", "dispatch_workspace_size", "expert_compute_workspace_size",
+    "expert_compute_workspace_layout", "moe_dispatch",
     "moe_dispatch_quant",
     "moe_expert_compute", "moe_combine", "moe_quantize_fp8", "moe_gemm_gateup_silu",
     "moe_gemm_down", "moe_gemm_gateup_down", "moe_dispatch_packed", "moe_expert_compute_packed",
-    "moe_combine_packed",
+    "moe_combine_packed", "moe_layer_stats", "layer_stats_dict", "LAYER_STATS",
     "packed_rows", "MoeLayerBuffers", "HostPipeline", "TwoBatchOverlap", "DEV_BAD_EXPERT_ID",
     "DEV_CAPACITY_DROPPED", "DEV_TIMEOUT",
 ]
@@ -57,8 +59,30 @@ def expert_compute_workspace_size(E: int, R: int, H: int, I: int) -> int:
     return int(_lib.load().moe_expert_compute_workspace_size(E, R, H, I))
 
 
+def expert_compute_workspace_layout(E: int, R: int, rows: int, H: int, I: int) -> list:
+    """Byte offsets [xq, xs, zq, zs, sync, sync bytes, total] of the expert
+    compute workspace, as the library carves it (rows = 0: padded layout)."""
+    off = (ctypes.c_size_t * 7)()
+    _lib.check("moe_expert_compute_workspace_layout",
+               _lib.load().moe_expert_compute_workspace_layout(E, R, rows, H, I, off))
+    return [int(v) for v in off]
+
+
 def _workspace(nbytes, device):
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _gemm_flags(w13_interleaved, gemm_launch):
+    """Flags of the GEMM launch form: None = the library's choice by tile
+    count, "one" = both GEMMs in one launch, "two" = gate/up then down."""
+    f = _lib.W13_INTERLEAVED if w13_interleaved else 0
+    if gemm_launch == "one":
+        return f | _lib.GEMM_ONE_LAUNCH
+    if gemm_launch == "two":
+        return f | _lib.GEMM_TWO_LAUNCHES
+    if gemm_launch is not None:
+        raise ValueError(f"gemm_launch: None, 'one' or 'two', not {gemm_launch!r}")
+    return f
 
 
 def _idx_bits(topk_idx):
@@ -100,19 +124,23 @@ def moe_dispatch(x, topk_idx, topk_w, E: int, R: int, *, recv=None, counts=None,
 
 
 def moe_dispatch_quant(x, topk_idx, topk_w, E: int, R: int, *, xq=None, xs=None, counts=None,
-                       src_map=None, dev_status=None, workspace=None, stream=None):
-    """Dispatch fused with the per-token FP8 quantisation.  Returns
-    ``(xq [E,R,H] uint8, xs [E,R,H/128] fp32, counts, src_map, dev_status)``."""
+                       src_map=None, dev_status=None, workspace=None, stream=None, rows=0):
+    """Dispatch fused with the per-token FP8 quantisation (moe_dispatch_quant_ex);
+    ``topk_idx`` int64 or int32.  ``rows = 0``: padded layout, ``xq [E,R,H]``;
+    ``rows > 0``: packed layout, ``xq [rows,H]``.  Returns ``(xq uint8, xs
+    fp32, counts, src_map, dev_status)``."""
     lib = _lib.load()
     T, H = x.shape
     K = topk_idx.shape[1]
     dev = x.device
     _need(x, torch.bfloat16, "x")
-    _need(topk_idx, torch.int64, "topk_idx")
+    bits = _idx_bits(topk_idx)
+    _need(topk_idx, topk_idx.dtype, "topk_idx")
+    lead = (rows,) if rows else (E, R)
     if xq is None:
-        xq = torch.empty(E, R, H, dtype=torch.uint8, device=dev)
+        xq = torch.empty(*lead, H, dtype=torch.uint8, device=dev)
     if xs is None:
-        xs = torch.empty(E, R, H // 128, dtype=torch.float32, device=dev)
+        xs = torch.empty(*lead, H // 128, dtype=torch.float32, device=dev)
     if counts is None:
         counts = torch.empty(E, dtype=torch.int32, device=dev)
     if src_map is None:
@@ -121,15 +149,15 @@ def moe_dispatch_quant(x, topk_idx, topk_w, E: int, R: int, *, xq=None, xs=None,
         dev_status = torch.empty(2, dtype=torch.int32, device=dev)
     if workspace is None:
         workspace = _workspace(lib.moe_dispatch_workspace_size(T, K, E), dev)
-    st = lib.moe_dispatch_quant(_p(x), _p(topk_idx), _p(topk_w), T, H, K, E, R, _p(xq), _p(xs),
-                                _p(counts), _p(src_map), _p(dev_status), _p(workspace),
-                                workspace.numel(), _s(stream))
-    _lib.check("moe_dispatch_quant", st)
+    st = lib.moe_dispatch_quant_ex(_p(x), _p(topk_idx), bits, _p(topk_w), T, H, K, E, R, rows,
+                                   _p(_u8(xq)), _p(xs), _p(counts), _p(src_map), _p(dev_status),
+                                   _p(workspace), workspace.numel(), _s(stream))
+    _lib.check("moe_dispatch_quant_ex", st)
     return xq, xs, counts, src_map, dev_status
 
 
 def moe_expert_compute(recv, counts, w13, w13_scale, w2, w2_scale, *, out=None, dev_status=None,
-                       workspace=None, stream=None, w13_interleaved=False):
+                       workspace=None, stream=None, w13_interleaved=False, gemm_launch=None):
     """Quantise the valid rows and run the grouped gated-SiLU FP8 expert MLP.
     Returns ``out [E,R,H] bf16`` (rows past counts[e] untouched).  With
     ``w13_interleaved`` the W13 rows alternate gate and up (moe_expert_compute_ex)."""
@@ -146,7 +174,7 @@ def moe_expert_compute(recv, counts, w13, w13_scale, w2, w2_scale, *, out=None, 
         workspace = _workspace(lib.moe_expert_compute_workspace_size(E, R, H, I), dev)
     st = lib.moe_expert_compute_ex(_p(recv), _p(counts), E, R, 0, H, I, _p(w13), _p(w13_scale),
                                    _p(w2), _p(w2_scale), _p(out), _p(dev_status), _p(workspace),
-                                   workspace.numel(), _lib.W13_INTERLEAVED if w13_interleaved else 0,
+                                   workspace.numel(), _gemm_flags(w13_interleaved, gemm_launch),
                                    _s(stream))
     _lib.check("moe_expert_compute_ex", st)
     return out
@@ -190,7 +218,8 @@ def moe_dispatch_packed(x, topk_idx, topk_w, E: int, R: int, *, rows=None, recv=
 
 
 def moe_expert_compute_packed(recv, counts, R: int, w13, w13_scale, w2, w2_scale, *, out=None,
-                              dev_status=None, workspace=None, stream=None, w13_interleaved=False):
+                              dev_status=None, workspace=None, stream=None, w13_interleaved=False,
+                              gemm_launch=None):
     """``moe_expert_compute`` on the packed layout: recv and out are [rows, H]."""
     lib = _lib.load()
     rows, H = recv.shape
@@ -206,10 +235,41 @@ def moe_expert_compute_packed(recv, counts, R: int, w13, w13_scale, w2, w2_scale
         workspace = _workspace(lib.moe_expert_compute_packed_workspace_size(rows, H, I), dev)
     st = lib.moe_expert_compute_ex(_p(recv), _p(counts), E, R, rows, H, I, _p(w13), _p(w13_scale),
                                    _p(w2), _p(w2_scale), _p(out), _p(dev_status), _p(workspace),
-                                   workspace.numel(), _lib.W13_INTERLEAVED if w13_interleaved else 0,
+                                   workspace.numel(), _gemm_flags(w13_interleaved, gemm_launch),
                                    _s(stream))
     _lib.check("moe_expert_compute_ex", st)
     return out
+
+
+LAYER_STATS = ("valid_routes", "kept_routes", "messages", "cross_rank_routes", "tile_blocks",
+               "active_experts", "busiest_expert_rows")
+
+
+def moe_layer_stats(topk_idx, counts, L: int, R: int, *, rank_offsets=None, stats=None,
+                    stream=None):
+    """Route, message and tile counts of one routing (moe_layer_stats); returns
+    the device ``stats`` tensor (int64 [7], in the order of ``LAYER_STATS``)."""
+    lib = _lib.load()
+    T, K = topk_idx.shape
+    E = counts.shape[0]
+    if stats is None:
+        stats = torch.empty(len(LAYER_STATS), dtype=torch.int64, device=counts.device)
+    st = lib.moe_layer_stats(_p(topk_idx), _idx_bits(topk_idx), _p(counts), T, K, E, L, R,
+                             _p(rank_offsets), _p(stats), _s(stream))
+    _lib.check("moe_layer_stats", st)
+    return stats
+
+
+def layer_stats_dict(stats, E: int, R: int) -> dict:
+    """Host view of moe_layer_stats' counters, with the derived figures:
+    dropped routes, M-row fill of the 128-row blocks, and the blocks a
+    capacity-dense launch would cover."""
+    v = [int(x) for x in stats.cpu().tolist()]
+    d = dict(zip(LAYER_STATS, v))
+    d["dropped_routes"] = d["valid_routes"] - d["kept_routes"]
+    d["m_fill_128"] = d["kept_routes"] / (128 * d["tile_blocks"]) if d["tile_blocks"] else None
+    d["capacity_blocks"] = E * -(-R // 128)
+    return d
 
 
 def moe_combine_packed(out, src_map, topk_w, *, y=None, stream=None):
@@ -289,7 +349,7 @@ def moe_gemm_down(zq, zs, counts, w2, w2_scale, *, out=None, dev_status=None, st
 
 def moe_gemm_gateup_down(xq, xs, counts, w13, w13_scale, w2, w2_scale, *, R=None, zq=None,
                          zs=None, out=None, sync=None, dev_status=None, stream=None,
-                         w13_interleaved=False):
+                         w13_interleaved=False, gemm_launch=None):
     """Both GEMMs in one launch (down tiles start per 128-row block as soon as
     that block's Z is written); bit-identical to ``moe_gemm_gateup_silu`` then
     ``moe_gemm_down``.  ``xq [E,R,H]`` is the padded layout; ``xq [rows,H]``
@@ -320,7 +380,7 @@ def moe_gemm_gateup_down(xq, xs, counts, w13, w13_scale, w2, w2_scale, *, R=None
     st = lib.moe_gemm_gateup_down(_p(_u8(xq)), _p(xs), _p(counts), E, R, rows, H, I, _p(w13),
                                   _p(w13_scale), _p(w2), _p(w2_scale), _p(zq), _p(zs), _p(out),
                                   _p(dev_status), _p(sync), sync.numel() * sync.element_size(),
-                                  _lib.W13_INTERLEAVED if w13_interleaved else 0, _s(stream))
+                                  _gemm_flags(w13_interleaved, gemm_launch), _s(stream))
     _lib.check("moe_gemm_gateup_down", st)
     return out
 
@@ -342,6 +402,7 @@ class MoeLayerBuffers:
     device: torch.device
     packed: bool = False   # packed layout (moe_*_packed): [rows, H] buffers, no capacity gaps
     w13_interleaved: bool = False   # W13 rows alternate gate and up
+    gemm_launch: str | None = None  # None: the library's choice; "one" / "two" launches
 
     def __post_init__(self):
         d, E, R, H, I, T, K = self.device, self.E, self.R, self.H, self.I, self.T, self.K
@@ -362,6 +423,13 @@ class MoeLayerBuffers:
         self.ws_dispatch = _workspace(dispatch_workspace_size(T, K, E), d)
         self.ws_compute = _workspace(ws, d)
 
+    def workspace_layout(self):
+        """Byte offsets of the expert compute workspace's parts, from the
+        library (moe_expert_compute_workspace_layout): xq, xs, zq, zs, sync,
+        sync bytes, total."""
+        return expert_compute_workspace_layout(self.E, self.R, self.rows if self.packed else 0,
+                                               self.H, self.I)
+
     def workspace_views(self):
         """(xq, xs, zq, zs): the FP8 activations and scales inside the expert
         compute workspace, in the layout moe_expert_compute(_packed) uses:
@@ -369,40 +437,39 @@ class MoeLayerBuffers:
         H, I, n = self.H, self.I, self.rows
         lead = (self.rows,) if self.packed else (self.E, self.R)
         G, GI = H // 128, I // 128
+        o = self.workspace_layout()
         ws = self.ws_compute
-        al = lambda v: (v + 255) // 256 * 256
-        o1 = al(n * H)
-        o2 = al(o1 + n * G * 4)
-        o3 = al(o2 + n * I)
-        xq = ws[:n * H].view(*lead, H)
-        xs = ws[o1:o1 + n * G * 4].view(torch.float32).view(*lead, G)
-        zq = ws[o2:o2 + n * I].view(*lead, I)
-        zs = ws[o3:o3 + n * GI * 4].view(torch.float32).view(*lead, GI)
+        xq = ws[o[0]:o[0] + n * H].view(*lead, H)
+        xs = ws[o[1]:o[1] + n * G * 4].view(torch.float32).view(*lead, G)
+        zq = ws[o[2]:o[2] + n * I].view(*lead, I)
+        zs = ws[o[3]:o[3] + n * GI * 4].view(torch.float32).view(*lead, GI)
         return xq, xs, zq, zs
 
     def sync_view(self):
         """The fused GEMM launch's scratch inside the expert compute workspace
         (a tile ticket and one count per 128-row block)."""
-        n, GI = self.rows, self.I // 128
-        al = lambda v: (v + 255) // 256 * 256
-        o4 = al(al(al(al(n * self.H) + n * (self.H // 128) * 4) + n * self.I) + n * GI * 4)
-        return self.ws_compute[o4:o4 + (1 + (n + 127) // 128 + 1024) * 4]
+        o = self.workspace_layout()
+        return self.ws_compute[o[4]:o[4] + o[5]]
 
-    def forward_fused(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None):
-        """The same layer with dispatch and quantisation fused (moe_dispatch_quant
+    def forward_fused(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None, y=None):
+        """The same layer with dispatch and quantisation fused (moe_dispatch_quant_ex
         -> both GEMMs in one launch -> combine); the BF16 receive buffer is not
-        used.  Returns ``y`` (bit-identical to ``forward``).  Padded lanes only."""
-        if self.packed:
-            raise ValueError("forward_fused runs on the padded layout")
+        used.  Returns ``y`` (bit-identical to ``forward``), padded or packed."""
+        y = self.y if y is None else y
+        rows = self.rows if self.packed else 0
         xq, xs, zq, zs = self.workspace_views()
         moe_dispatch_quant(x, topk_idx, topk_w, self.E, self.R, xq=xq, xs=xs, counts=self.counts,
                            src_map=self.src_map, dev_status=self.dev_status,
-                           workspace=self.ws_dispatch, stream=stream)
-        moe_gemm_gateup_down(xq, xs, self.counts, w13, w13_scale, w2, w2_scale, zq=zq, zs=zs,
-                             out=self.out, sync=self.sync_view(), dev_status=self.dev_status,
-                             stream=stream, w13_interleaved=self.w13_interleaved)
-        moe_combine(self.out, self.src_map, topk_w, y=self.y, stream=stream)
-        return self.y
+                           workspace=self.ws_dispatch, stream=stream, rows=rows)
+        moe_gemm_gateup_down(xq, xs, self.counts, w13, w13_scale, w2, w2_scale, R=self.R, zq=zq,
+                             zs=zs, out=self.out, sync=self.sync_view(), dev_status=self.dev_status,
+                             stream=stream, w13_interleaved=self.w13_interleaved,
+                             gemm_launch=self.gemm_launch)
+        if self.packed:
+            moe_combine_packed(self.out, self.src_map, topk_w, y=y, stream=stream)
+        else:
+            moe_combine(self.out, self.src_map, topk_w, y=y, stream=stream)
+        return y
 
     def forward(self, x, topk_idx, topk_w, w13, w13_scale, w2, w2_scale, stream=None, y=None):
         """dispatch -> expert compute -> combine on one stream; returns ``y``
@@ -416,7 +483,8 @@ class MoeLayerBuffers:
             moe_expert_compute_packed(self.recv, self.counts, self.R, w13, w13_scale, w2,
                                       w2_scale, out=self.out, dev_status=self.dev_status,
                                       workspace=self.ws_compute, stream=stream,
-                                      w13_interleaved=self.w13_interleaved)
+                                      w13_interleaved=self.w13_interleaved,
+                                      gemm_launch=self.gemm_launch)
             moe_combine_packed(self.out, self.src_map, topk_w, y=y, stream=stream)
             return y
         moe_dispatch(x, topk_idx, topk_w, self.E, self.R, recv=self.recv, counts=self.counts,
@@ -424,7 +492,7 @@ class MoeLayerBuffers:
                      stream=stream)
         moe_expert_compute(self.recv, self.counts, w13, w13_scale, w2, w2_scale, out=self.out,
                            dev_status=self.dev_status, workspace=self.ws_compute, stream=stream,
-                           w13_interleaved=self.w13_interleaved)
+                           w13_interleaved=self.w13_interleaved, gemm_launch=self.gemm_launch)
         moe_combine(self.out, self.src_map, topk_w, y=y, stream=stream)
         return y
 

@@ -118,19 +118,70 @@ __global__ void __launch_bounds__(kScanThreads)
   }
 }
 
+// Single-pass slot bases for small route counts (T*K <= kSinglePassRoutes):
+// instead of the histogram and scan kernels, every block counts in shared
+// memory, straight from topk_idx, the routes to each expert before its own
+// first route (s_prev) and in all (s_tot).  The slots are then the ones the
+// scanned histograms give.  Block (0, 0) writes counts[e] = min(s_tot[e], R)
+// and both status words (bad-id bit, drop bit and count), so the launch needs
+// no status reset either.  With the packed layout the row bases are the
+// prefix of the clamped totals (s_rows).  Every thread of the block calls it.
 template <typename IdT>
+__device__ void single_pass_bases(const IdT* __restrict__ topk_idx, int T, int K, int E,
+                                  RowLayout rl, int* s_prev, int* s_tot, int* s_rows,
+                                  int32_t* __restrict__ counts, int32_t* dev_status) {
+  __shared__ int s_dropped;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_prev[e] = s_tot[e] = 0;
+  if (threadIdx.x == 0) s_dropped = 0;
+  __syncthreads();
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kDispatchWarps * (32 / K) * K;
+  const int64_t n = static_cast<int64_t>(T) * K;
+  int bad = 0;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const int64_t id = static_cast<int64_t>(topk_idx[i]);
+    if (id >= 0 && id < E) {
+      atomicAdd(&s_tot[id], 1);
+      if (i < first) atomicAdd(&s_prev[id], 1);
+    } else if (id != -1) {
+      bad = 1;
+    }
+  }
+  bad = __syncthreads_or(bad);
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    int dropped = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      counts[e] = min(s_tot[e], rl.R);
+      dropped += max(s_tot[e] - rl.R, 0);
+    }
+    if (dropped) atomicAdd(&s_dropped, dropped);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      dev_status[0] = (bad ? kDevBadExpertId : 0) | (s_dropped > 0 ? kDevCapacityDropped : 0);
+      dev_status[1] = s_dropped;
+    }
+  }
+  if (rl.packed) expert_prefix(s_tot, E, rl.R, 1, 1, s_rows, nullptr);
+  __syncthreads();
+}
+
+template <typename IdT, bool kSingle>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
     route_scatter_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx, int T,
                          int H, int K, int E, RowLayout rl, int nblocks,
-                         const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
+                         const int32_t* __restrict__ base, int32_t* __restrict__ counts,
                          uint4* __restrict__ recv, int32_t* __restrict__ src_map,
-                         int vec_per_slice) {
+                         int32_t* dev_status, int vec_per_slice) {
   extern __shared__ int smem[];
   int* s_cnt = smem;                           // [kDispatchWarps][E]
   int* s_dest = smem + kDispatchWarps * E;     // [kDispatchWarps][32]
   int* s_rows = s_dest + kDispatchWarps * 32;  // [E + 1] packed row bases
+  int* s_prev = s_rows + E + 1;                // single pass: [E] routes before this block
+  int* s_tot = s_prev + E;                     //              [E] all routes
   for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) s_cnt[i] = 0;
-  if (rl.packed) expert_prefix(counts, E, rl.R, 1, 1, s_rows, nullptr);
+  if (kSingle)
+    single_pass_bases(topk_idx, T, K, E, rl, s_prev, s_tot, s_rows, counts, dev_status);
+  else if (rl.packed)
+    expert_prefix(counts, E, rl.R, 1, 1, s_rows, nullptr);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kDispatchWarps + warp;
@@ -141,7 +192,8 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   __syncthreads();
   int q = -1;
   if (r.e >= 0) {
-    int s = base[static_cast<size_t>(r.e) * nblocks + blockIdx.x] + lane_rank;
+    int s = (kSingle ? s_prev[r.e] : base[static_cast<size_t>(r.e) * nblocks + blockIdx.x]) +
+            lane_rank;
     for (int w = 0; w < warp; ++w) s += s_cnt[w * E + r.e];
     if (s < rl.R) q = (rl.packed ? s_rows[r.e] : r.e * rl.R) + s;
   }
@@ -190,20 +242,26 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
 // fp32 scales are written to every kept destination row; the BF16 receive
 // buffer is never formed.  Rank derivation is the one of route_scatter_kernel.
 // Each block takes a slice of whole 128-groups of its tokens' rows.
-template <typename IdT>
+template <typename IdT, bool kSingle>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
     route_scatter_fp8_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx,
                              int T, int H, int K, int E, RowLayout rl, int nblocks,
-                             const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
+                             const int32_t* __restrict__ base, int32_t* __restrict__ counts,
                              uint2* __restrict__ xq, float* __restrict__ xs,
-                             int32_t* __restrict__ src_map, int groups_per_slice) {
+                             int32_t* __restrict__ src_map, int32_t* dev_status,
+                             int groups_per_slice) {
   extern __shared__ int smem[];
   int* s_cnt = smem;                                               // [kDispatchWarps][E]
   int* s_dest = smem + kDispatchWarps * E;                         // [kDispatchWarps][32]
   int* s_rows = s_dest + kDispatchWarps * 32;                       // [E + 1] packed row bases
-  float* s_sc = reinterpret_cast<float*>(s_rows + E + 1);          // [warps][groups_per_slice]
+  int* s_prev = s_rows + E + 1;                                    // single pass: [E]
+  int* s_tot = s_prev + E;                                         //              [E]
+  float* s_sc = reinterpret_cast<float*>(s_tot + E);               // [warps][groups_per_slice]
   for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) s_cnt[i] = 0;
-  if (rl.packed) expert_prefix(counts, E, rl.R, 1, 1, s_rows, nullptr);
+  if (kSingle)
+    single_pass_bases(topk_idx, T, K, E, rl, s_prev, s_tot, s_rows, counts, dev_status);
+  else if (rl.packed)
+    expert_prefix(counts, E, rl.R, 1, 1, s_rows, nullptr);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
@@ -215,7 +273,8 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   __syncthreads();
   int q = -1;
   if (r.e >= 0) {
-    int sl = base[static_cast<size_t>(r.e) * nblocks + blockIdx.x] + lane_rank;
+    int sl = (kSingle ? s_prev[r.e] : base[static_cast<size_t>(r.e) * nblocks + blockIdx.x]) +
+             lane_rank;
     for (int w = 0; w < warp; ++w) sl += s_cnt[w * E + r.e];
     if (sl < rl.R) q = (rl.packed ? s_rows[r.e] : r.e * rl.R) + sl;
   }
@@ -290,37 +349,172 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   }
 }
 
+// Per-source fixed-slot dispatch ("DeepEP 架构与实现笔记", §9.5): expert e's
+// R = W * mt rows are W ranges of mt slots, one per source rank, and route
+// (t, k) of source rank r goes to slot r * mt + p, p its position among r's
+// routes to e in ascending route id.  A slot follows from the source's own
+// routes alone, so each block takes one source rank's tokens (blockIdx.x = r,
+// blockIdx.y = column slice) and walks them in chunks of kDispatchWarps *
+// (32 / K) tokens, with running per-expert positions in shared memory: no
+// histogram or scan across blocks.  Routes whose position reaches mt are
+// dropped.  Each (y = 0) block adds its clamped positions to counts[e] (the
+// per-expert valid rows, zeroed by the launcher) and writes its column of
+// seg_counts [E, W].
+template <typename IdT>
+__global__ void __launch_bounds__(kDispatchWarps * 32)
+    route_source_slots_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx,
+                              int T, int H, int K, int E, int W, int mt,
+                              const int32_t* __restrict__ rank_offsets, uint4* __restrict__ recv,
+                              int32_t* __restrict__ counts, int32_t* __restrict__ seg_counts,
+                              int32_t* __restrict__ src_map, int32_t* dev_status,
+                              int vec_per_slice) {
+  extern __shared__ int smem[];
+  int* s_cnt = smem;                        // [kDispatchWarps][E] routes per warp of a chunk
+  int* s_dest = smem + kDispatchWarps * E;  // [kDispatchWarps][32]
+  int* s_pos = s_dest + kDispatchWarps * 32;  // [E] next position of this source per expert
+  const int r = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tpw = 32 / K;
+  const int per = (T + W - 1) / W;
+  const int t0 = rank_offsets ? rank_offsets[r] : min(T, r * per);
+  const int t1 = rank_offsets ? rank_offsets[r + 1] : min(T, (r + 1) * per);
+  const int64_t R = static_cast<int64_t>(W) * mt;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_pos[e] = 0;
+  const int nvec = H / 8;
+  const int v0 = blockIdx.y * vec_per_slice;
+  const int v1 = min(nvec, v0 + vec_per_slice);
+  int bad = 0;
+  for (int c0 = t0; c0 < t1; c0 += kDispatchWarps * tpw) {
+    for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) s_cnt[i] = 0;
+    __syncthreads();
+    const int t = c0 + warp * tpw + lane / K;
+    const int k = lane % K;
+    const bool active = lane < tpw * K && t < t1;
+    int e = -1;
+    if (active) {
+      const int64_t id = static_cast<int64_t>(topk_idx[static_cast<int64_t>(t) * K + k]);
+      if (id >= 0 && id < E) e = static_cast<int>(id);
+      else if (id != -1) bad = 1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int lane_rank = __popc(peers & ((1u << lane) - 1u));
+    const bool leader = e >= 0 && lane == __ffs(peers) - 1;
+    if (leader) s_cnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    int q = -1;
+    if (e >= 0) {
+      int p = s_pos[e] + lane_rank;
+      for (int w = 0; w < warp; ++w) p += s_cnt[w * E + e];
+      if (p < mt) q = static_cast<int>(e * R + static_cast<int64_t>(r) * mt + p);
+    }
+    if (blockIdx.y == 0 && active) src_map[static_cast<int64_t>(t) * K + k] = q;
+    s_dest[warp * 32 + lane] = q;
+    __syncthreads();
+    if (leader) atomicAdd(&s_pos[e], __popc(peers));   // positions for the next chunk
+    // payload: this warp's tokens, this block's column slice
+    const int* wdest = s_dest + warp * 32;
+    for (int tt = 0; tt < tpw; ++tt) {
+      const int tok = c0 + warp * tpw + tt;
+      if (tok >= t1) break;
+      const int* dq = wdest + tt * K;
+      bool any = false;
+      for (int kk = 0; kk < K; ++kk) any |= dq[kk] >= 0;
+      if (!any) continue;
+      const uint4* src = x + static_cast<size_t>(tok) * nvec;
+      for (int v = v0 + lane; v < v1; v += 32 * 8) {
+        uint4 a[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (v + 32 * u < v1) a[u] = ld_stream(src + v + 32 * u);
+        for (int kk = 0; kk < K; ++kk) {
+          const int qq = dq[kk];
+          if (qq < 0) continue;
+          uint4* dst = recv + static_cast<size_t>(qq) * nvec;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (v + 32 * u < v1) dst[v + 32 * u] = a[u];
+        }
+      }
+    }
+  }
+  bad = __syncthreads_or(bad);
+  if (blockIdx.y != 0) return;
+  int dropped = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int n = s_pos[e];
+    const int kept = min(n, mt);
+    seg_counts[static_cast<size_t>(e) * W + r] = kept;
+    if (kept) atomicAdd(&counts[e], kept);
+    dropped += n - kept;
+  }
+  if (dropped) {
+    atomicAdd(dev_status + 1, dropped);
+    atomicOr(dev_status, kDevCapacityDropped);
+  }
+  if (bad && threadIdx.x == 0) atomicOr(dev_status, kDevBadExpertId);
+}
+
 }  // namespace
 
 namespace {
+
+// Column slices per token row when there are too few tokens to keep enough
+// warps in flight; a slice keeps at least `min_units` units.
+int row_slices(int nblocks, int units, int min_units, int sm_count) {
+  const int target_warps = sm_count * 48;
+  int hsplit = (target_warps + nblocks * kDispatchWarps - 1) / (nblocks * kDispatchWarps);
+  return max(1, min(hsplit, units / min_units));
+}
+
+// Dynamic shared memory above the 48 KB default needs an opt-in per kernel.
+template <typename Kernel>
+cudaError_t allow_smem(Kernel k, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(bytes));
+}
+
+bool single_pass(int T, int K) {
+  return T > 0 && static_cast<int64_t>(T) * K <= kSinglePassRoutes;
+}
+
 template <typename IdT>
 cudaError_t dispatch_impl(const void* x, const IdT* topk_idx, int T, int H, int K, int E,
                           RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
                           int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s) {
   const int R = rl.R;
-  cudaError_t err = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
-  if (err != cudaSuccess) return err;
   const int nblocks = dispatch_blocks(T, K);
-  if (nblocks > 0) {
-    route_hist_kernel<IdT><<<nblocks, kDispatchWarps * 32, E * sizeof(int), s>>>(
-        topk_idx, T, K, E, nblocks, hist, dev_status);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  }
-  route_scan_kernel<<<E, kScanThreads, 0, s>>>(hist, nblocks, R, counts, dev_status);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  if (nblocks == 0) return cudaSuccess;
-  // Split each row into column slices when there are too few tokens to keep
-  // enough warps in flight; a slice keeps at least 32 vectors (512 bytes).
   const int nvec = H / 8;
-  const int target_warps = sm_count * 48;
-  int hsplit = (target_warps + nblocks * kDispatchWarps - 1) / (nblocks * kDispatchWarps);
-  hsplit = max(1, min(hsplit, nvec / 32));
+  const bool one = single_pass(T, K);
+  cudaError_t err;
+  if (!one) {
+    err = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
+    if (err != cudaSuccess) return err;
+    if (nblocks > 0) {
+      route_hist_kernel<IdT><<<nblocks, kDispatchWarps * 32, E * sizeof(int), s>>>(
+          topk_idx, T, K, E, nblocks, hist, dev_status);
+      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    route_scan_kernel<<<E, kScanThreads, 0, s>>>(hist, nblocks, R, counts, dev_status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (nblocks == 0) return cudaSuccess;
+  }
+  int hsplit = row_slices(nblocks, nvec, 32, sm_count);
   const int vec_per_slice = (nvec + hsplit - 1) / hsplit;
   hsplit = (nvec + vec_per_slice - 1) / vec_per_slice;
-  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + E + 1) * sizeof(int);
-  route_scatter_kernel<IdT><<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
-      static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
-      static_cast<uint4*>(recv), src_map, vec_per_slice);
+  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + 3 * E + 1) * sizeof(int);
+  const dim3 grid(nblocks, hsplit);
+  if ((err = allow_smem(one ? route_scatter_kernel<IdT, true> : route_scatter_kernel<IdT, false>,
+                        smem)) != cudaSuccess)
+    return err;
+  if (one)
+    route_scatter_kernel<IdT, true><<<grid, kDispatchWarps * 32, smem, s>>>(
+        static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
+        static_cast<uint4*>(recv), src_map, dev_status, vec_per_slice);
+  else
+    route_scatter_kernel<IdT, false><<<grid, kDispatchWarps * 32, smem, s>>>(
+        static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
+        static_cast<uint4*>(recv), src_map, dev_status, vec_per_slice);
   return cudaGetLastError();
 }
 }  // namespace
@@ -339,33 +533,60 @@ cudaError_t launch_dispatch(const void* x, const void* topk_idx, int idx_bits, i
 
 namespace moe {
 
-cudaError_t launch_dispatch_quant(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
-                                  int R, uint8_t* xq, float* xs, int32_t* counts, int32_t* src_map,
-                                  int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s) {
-  cudaError_t err = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
-  if (err != cudaSuccess) return err;
+namespace {
+template <typename IdT>
+cudaError_t dispatch_quant_impl(const void* x, const IdT* topk_idx, int T, int H, int K, int E,
+                                RowLayout rl, uint8_t* xq, float* xs, int32_t* counts,
+                                int32_t* src_map, int32_t* dev_status, int32_t* hist,
+                                int sm_count, cudaStream_t s) {
   const int nblocks = dispatch_blocks(T, K);
-  if (nblocks > 0) {
-    route_hist_kernel<int64_t><<<nblocks, kDispatchWarps * 32, E * sizeof(int), s>>>(
-        topk_idx, T, K, E, nblocks, hist, dev_status);
+  const bool one = single_pass(T, K);
+  cudaError_t err;
+  if (!one) {
+    err = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
+    if (err != cudaSuccess) return err;
+    if (nblocks > 0) {
+      route_hist_kernel<IdT><<<nblocks, kDispatchWarps * 32, E * sizeof(int), s>>>(
+          topk_idx, T, K, E, nblocks, hist, dev_status);
+      if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    route_scan_kernel<<<E, kScanThreads, 0, s>>>(hist, nblocks, rl.R, counts, dev_status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (nblocks == 0) return cudaSuccess;
   }
-  route_scan_kernel<<<E, kScanThreads, 0, s>>>(hist, nblocks, R, counts, dev_status);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  if (nblocks == 0) return cudaSuccess;
   // Slices of whole 128-groups when there are too few tokens to fill the GPU.
   const int G = H / kGroup;
-  const int target_warps = sm_count * 48;
-  int hsplit = (target_warps + nblocks * kDispatchWarps - 1) / (nblocks * kDispatchWarps);
-  hsplit = max(1, min(hsplit, G / 4));
+  int hsplit = row_slices(nblocks, G, 4, sm_count);
   const int gps = (G + hsplit - 1) / hsplit;
   hsplit = (G + gps - 1) / gps;
-  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + E + 1) * sizeof(int) +
+  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + 3 * E + 1) * sizeof(int) +
                       kDispatchWarps * gps * sizeof(float);
-  route_scatter_fp8_kernel<int64_t><<<dim3(nblocks, hsplit), kDispatchWarps * 32, smem, s>>>(
-      static_cast<const uint4*>(x), topk_idx, T, H, K, E, padded_rows(E, R), nblocks, hist, counts,
-      reinterpret_cast<uint2*>(xq), xs, src_map, gps);
+  const dim3 grid(nblocks, hsplit);
+  if ((err = allow_smem(one ? route_scatter_fp8_kernel<IdT, true>
+                            : route_scatter_fp8_kernel<IdT, false>,
+                        smem)) != cudaSuccess)
+    return err;
+  if (one)
+    route_scatter_fp8_kernel<IdT, true><<<grid, kDispatchWarps * 32, smem, s>>>(
+        static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
+        reinterpret_cast<uint2*>(xq), xs, src_map, dev_status, gps);
+  else
+    route_scatter_fp8_kernel<IdT, false><<<grid, kDispatchWarps * 32, smem, s>>>(
+        static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
+        reinterpret_cast<uint2*>(xq), xs, src_map, dev_status, gps);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_dispatch_quant(const void* x, const void* topk_idx, int idx_bits, int T, int H,
+                                  int K, int E, RowLayout rl, uint8_t* xq, float* xs,
+                                  int32_t* counts, int32_t* src_map, int32_t* dev_status,
+                                  int32_t* hist, int sm_count, cudaStream_t s) {
+  if (idx_bits == 32)
+    return dispatch_quant_impl(x, static_cast<const int32_t*>(topk_idx), T, H, K, E, rl, xq, xs,
+                               counts, src_map, dev_status, hist, sm_count, s);
+  return dispatch_quant_impl(x, static_cast<const int64_t*>(topk_idx), T, H, K, E, rl, xq, xs,
+                             counts, src_map, dev_status, hist, sm_count, s);
 }
 
 }  // namespace moe

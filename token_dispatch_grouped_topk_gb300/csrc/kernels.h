@@ -42,16 +42,21 @@ inline int64_t dispatch_blocks64(int64_t T, int K) {
   return (T + tpb - 1) / tpb;
 }
 inline int dispatch_blocks(int T, int K) { return static_cast<int>(dispatch_blocks64(T, K)); }
+// Up to this many routes (T * K) the dispatch runs as one kernel: every block
+// counts the routes before its own straight from topk_idx instead of the
+// histogram and scan kernels (same slots, counts and status).
+constexpr int kSinglePassRoutes = 4096;
 // topk_idx holds int64 ids (idx_bits = 64) or int32 ids (idx_bits = 32).
 cudaError_t launch_dispatch(const void* x, const void* topk_idx, int idx_bits, int T, int H, int K,
                             int E, RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
                             int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s);
 
-// ----- dispatch fused with the per-token FP8 quantisation: xq [E, R, H]
-// e4m3 and xs [E, R, H/128] instead of the BF16 receive buffer
-cudaError_t launch_dispatch_quant(const void* x, const int64_t* topk_idx, int T, int H, int K, int E,
-                                  int R, uint8_t* xq, float* xs, int32_t* counts, int32_t* src_map,
-                                  int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s);
+// ----- dispatch fused with the per-token FP8 quantisation: xq e4m3 and xs
+// (row layout rl, int32 or int64 ids) instead of the BF16 receive buffer
+cudaError_t launch_dispatch_quant(const void* x, const void* topk_idx, int idx_bits, int T, int H,
+                                  int K, int E, RowLayout rl, uint8_t* xq, float* xs,
+                                  int32_t* counts, int32_t* src_map, int32_t* dev_status,
+                                  int32_t* hist, int sm_count, cudaStream_t s);
 
 // ----- per-token FP8 quantisation of the valid rows; xs is [E, R, H/128]
 cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, RowLayout rl, int H,
@@ -73,6 +78,10 @@ cudaError_t launch_gemm_down(const uint8_t* zq, const float* zs, const int32_t* 
 // gemm_sync_ints(E, rl) ints of device scratch (zeroed by the launch).  With
 // H % 256 != 0 it runs the two launches above instead.
 size_t gemm_sync_ints(int E, RowLayout rl);
+// Whether moe_expert_compute runs both GEMMs as one launch (true) or as the
+// gate/up launch followed by the down launch, from the largest possible tile
+// count of the layout.
+bool gemm_prefer_one_launch(int E, RowLayout rl, int I, int sm_count);
 cudaError_t launch_gemm_gateup_down(const uint8_t* xq, const float* xs, const int32_t* counts,
                                     int E, RowLayout rl, int H, int I, const uint8_t* w13,
                                     const float* w13_scale, const uint8_t* w2,
@@ -85,5 +94,14 @@ cudaError_t launch_gemm_gateup_down(const uint8_t* xq, const float* xs, const in
 // a src_map entry outside [0, rows) is treated like -1.
 cudaError_t launch_combine(const void* out, const int32_t* src_map, const float* topk_w, int T,
                            int H, int K, int64_t rows, void* y, int sm_count, cudaStream_t s);
+
+// ----- layer statistics of one routing (kLayerStats 64-bit counters):
+// [0] valid routes, [1] kept routes, [2] messages (sum over tokens of the
+// distinct destination ranks), [3] cross-rank routes, [4] 128-row blocks of
+// the GEMM tile list, [5] active experts, [6] the busiest expert's kept rows
+constexpr int kLayerStats = 7;
+cudaError_t launch_layer_stats(const void* topk_idx, int idx_bits, const int32_t* counts, int T,
+                               int K, int E, int L, int R, const int32_t* rank_offsets,
+                               unsigned long long* stats, cudaStream_t s);
 
 }  // namespace moe

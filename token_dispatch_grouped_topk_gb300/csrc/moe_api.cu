@@ -91,6 +91,32 @@ ComputeWorkspace compute_workspace(int E, int R, int H, int I) {
 
 moe_status from_cuda(cudaError_t e);
 
+// Both GEMMs, as one launch or as the gate/up launch then the down launch
+// (MOE_GEMM_ONE_LAUNCH / MOE_GEMM_TWO_LAUNCHES, else by the tile count).
+cudaError_t run_gemms(const uint8_t* xq, const float* xs, const int32_t* counts, int E, RowLayout rl,
+                      int H, int I, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                      const float* w2_scale, uint8_t* zq, float* zs, void* out, int* sync,
+                      size_t sync_ints, int32_t* dev_status, int sm_count, cudaStream_t s,
+                      int flags) {
+  const int inter = (flags & MOE_W13_INTERLEAVED) ? 1 : 0;
+  const bool one = (flags & MOE_GEMM_ONE_LAUNCH)     ? true
+                   : (flags & MOE_GEMM_TWO_LAUNCHES) ? false
+                                                     : gemm_prefer_one_launch(E, rl, I, sm_count);
+  if (one)
+    return launch_gemm_gateup_down(xq, xs, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, zq,
+                                   zs, out, sync, sync_ints, dev_status, sm_count, s, inter);
+  cudaError_t err = launch_gemm_gateup(xq, xs, counts, E, rl, H, I, w13, w13_scale, zq, zs,
+                                       dev_status, sm_count, s, inter);
+  if (err != cudaSuccess) return err;
+  return launch_gemm_down(zq, zs, counts, E, rl, H, I, w2, w2_scale, out, dev_status, sm_count, s);
+}
+
+bool valid_gemm_flags(int flags) {
+  return (flags & ~(MOE_W13_INTERLEAVED | MOE_GEMM_ONE_LAUNCH | MOE_GEMM_TWO_LAUNCHES)) == 0 &&
+         !((flags & MOE_GEMM_ONE_LAUNCH) && (flags & MOE_GEMM_TWO_LAUNCHES));
+}
+
+
 // The expert compute on a carved workspace: quantisation, then both GEMMs in
 // one launch.
 moe_status expert_compute_impl(const void* recv, const int32_t* counts, int E, RowLayout rl, int H,
@@ -106,9 +132,8 @@ moe_status expert_compute_impl(const void* recv, const int32_t* counts, int E, R
   int* sync = reinterpret_cast<int*>(ws + w.sync);
   cudaError_t err = launch_quantize(recv, counts, E, rl, H, xq, xs, sm_count, s);
   if (err == cudaSuccess)
-    err = launch_gemm_gateup_down(xq, xs, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, zq,
-                                  zs, out, sync, w.sync_ints, dev_status, sm_count, s,
-                                  (flags & MOE_W13_INTERLEAVED) ? 1 : 0);
+    err = run_gemms(xq, xs, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, zq, zs, out, sync,
+                    w.sync_ints, dev_status, sm_count, s, flags);
   return from_cuda(err);
 }
 
@@ -187,13 +212,15 @@ moe_status moe_dispatch_packed(const void* x, const int64_t* topk_idx, const flo
                          dev_status, workspace, workspace_bytes, stream);
 }
 
-moe_status moe_dispatch_quant(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
-                              int H, int K, int E, int R, uint8_t* xq, float* xs, int32_t* counts,
-                              int32_t* src_map, int32_t* dev_status, void* workspace,
-                              size_t workspace_bytes, moe_stream_t stream) {
+moe_status moe_dispatch_quant_ex(const void* x, const void* topk_idx, int idx_bits,
+                                 const float* topk_w, int T, int H, int K, int E, int R,
+                                 int64_t rows, uint8_t* xq, float* xs, int32_t* counts,
+                                 int32_t* src_map, int32_t* dev_status, void* workspace,
+                                 size_t workspace_bytes, moe_stream_t stream) {
   (void)topk_w;
   if (T < 0 || !valid_hidden(H) || !valid_experts(E, R) || K < 1 || K > 32 || K > E)
     return MOE_ERR_INVALID_ARG;
+  if (idx_bits != 32 && idx_bits != 64) return MOE_ERR_INVALID_ARG;
   if (counts == nullptr || dev_status == nullptr) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (x == nullptr || topk_idx == nullptr || xq == nullptr || xs == nullptr ||
                 src_map == nullptr))
@@ -201,13 +228,28 @@ moe_status moe_dispatch_quant(const void* x, const int64_t* topk_idx, const floa
   if (T > 0 && (!aligned16(x) || (reinterpret_cast<uintptr_t>(xq) & 7u) != 0))
     return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(T) * K > (int64_t{1} << 31) - 1) return MOE_ERR_INVALID_ARG;
+  RowLayout rl = padded_rows(E, R);
+  if (rows != 0) {
+    const int64_t need_rows =
+        std::min<int64_t>(static_cast<int64_t>(T) * K, static_cast<int64_t>(E) * R);
+    if (!valid_rows(rows) || rows < need_rows) return MOE_ERR_INVALID_ARG;
+    rl = RowLayout{R, 1, rows};
+  }
   const size_t need = moe_dispatch_workspace_size(T, K, E);
   if (workspace == nullptr || workspace_bytes < need) return MOE_ERR_WORKSPACE;
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
-  return from_cuda(launch_dispatch_quant(x, topk_idx, T, H, K, E, R, xq, xs, counts, src_map,
-                                         dev_status, static_cast<int32_t*>(workspace),
+  return from_cuda(launch_dispatch_quant(x, topk_idx, idx_bits, T, H, K, E, rl, xq, xs, counts,
+                                         src_map, dev_status, static_cast<int32_t*>(workspace),
                                          dev->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch_quant(const void* x, const int64_t* topk_idx, const float* topk_w, int T,
+                              int H, int K, int E, int R, uint8_t* xq, float* xs, int32_t* counts,
+                              int32_t* src_map, int32_t* dev_status, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream) {
+  return moe_dispatch_quant_ex(x, topk_idx, 64, topk_w, T, H, K, E, R, 0, xq, xs, counts, src_map,
+                               dev_status, workspace, workspace_bytes, stream);
 }
 
 size_t moe_expert_compute_workspace_size(int E, int R, int H, int I) {
@@ -269,7 +311,7 @@ moe_status moe_gemm_gateup_down(const uint8_t* xq, const float* xs, const int32_
                                 uint8_t* zq, float* zs, void* out, int32_t* dev_status, void* sync,
                                 size_t sync_bytes, int flags, moe_stream_t stream) {
   if (!valid_experts(E, R) || !valid_hidden(H) || !valid_hidden(I)) return MOE_ERR_INVALID_ARG;
-  if ((flags & ~MOE_W13_INTERLEAVED) != 0) return MOE_ERR_INVALID_ARG;
+  if (!valid_gemm_flags(flags)) return MOE_ERR_INVALID_ARG;
   if (rows != 0 && !valid_rows(rows)) return MOE_ERR_INVALID_ARG;
   if (xq == nullptr || xs == nullptr || counts == nullptr || w13 == nullptr ||
       w13_scale == nullptr || w2 == nullptr || w2_scale == nullptr || zq == nullptr ||
@@ -284,10 +326,9 @@ moe_status moe_gemm_gateup_down(const uint8_t* xq, const float* xs, const int32_
     return MOE_ERR_WORKSPACE;
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
-  return from_cuda(launch_gemm_gateup_down(
-      xq, xs, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, zq, zs, out,
-      static_cast<int*>(sync), sync_bytes / sizeof(int), dev_status, dev->sm_count,
-      reinterpret_cast<cudaStream_t>(stream), (flags & MOE_W13_INTERLEAVED) ? 1 : 0));
+  return from_cuda(run_gemms(xq, xs, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, zq, zs,
+                             out, static_cast<int*>(sync), sync_bytes / sizeof(int), dev_status,
+                             dev->sm_count, reinterpret_cast<cudaStream_t>(stream), flags));
 }
 
 moe_status moe_expert_compute(const void* recv, const int32_t* counts, int E, int R, int H, int I,
@@ -344,13 +385,29 @@ size_t moe_expert_compute_ex_workspace_size(int E, int R, int64_t rows, int H, i
   return moe_expert_compute_packed_workspace_size(rows, H, I);
 }
 
+int moe_expert_compute_workspace_layout(int E, int R, int64_t rows, int H, int I,
+                                        size_t* offsets) {
+  if (offsets == nullptr || !valid_hidden(H) || !valid_hidden(I)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0 ? !valid_experts(E, R) : !valid_rows(rows)) return MOE_ERR_INVALID_ARG;
+  const ComputeWorkspace w =
+      compute_workspace_rows(rows == 0 ? static_cast<int64_t>(E) * R : rows, H, I);
+  offsets[0] = w.xq;
+  offsets[1] = w.xs;
+  offsets[2] = w.zq;
+  offsets[3] = w.zs;
+  offsets[4] = w.sync;
+  offsets[5] = w.sync_ints * sizeof(int);
+  offsets[6] = w.total;
+  return MOE_OK;
+}
+
 moe_status moe_expert_compute_ex(const void* recv, const int32_t* counts, int E, int R, int64_t rows,
                                  int H, int I, const uint8_t* w13, const float* w13_scale,
                                  const uint8_t* w2, const float* w2_scale, void* out,
                                  int32_t* dev_status, void* workspace, size_t workspace_bytes,
                                  int flags, moe_stream_t stream) {
   if (!valid_experts(E, R) || !valid_hidden(H) || !valid_hidden(I)) return MOE_ERR_INVALID_ARG;
-  if ((flags & ~MOE_W13_INTERLEAVED) != 0) return MOE_ERR_INVALID_ARG;
+  if (!valid_gemm_flags(flags)) return MOE_ERR_INVALID_ARG;
   if (rows != 0 && !valid_rows(rows)) return MOE_ERR_INVALID_ARG;
   if (recv == nullptr || counts == nullptr || w13 == nullptr || w13_scale == nullptr ||
       w2 == nullptr || w2_scale == nullptr || out == nullptr || dev_status == nullptr)
@@ -367,6 +424,23 @@ moe_status moe_expert_compute_ex(const void* recv, const int32_t* counts, int E,
   return expert_compute_impl(recv, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, out,
                              dev_status, workspace, w, dev->sm_count,
                              reinterpret_cast<cudaStream_t>(stream), flags);
+}
+
+moe_status moe_layer_stats(const void* topk_idx, int idx_bits, const int32_t* counts, int T, int K,
+                           int E, int L, int R, const int32_t* rank_offsets, uint64_t* stats,
+                           moe_stream_t stream) {
+  if (T < 0 || K < 1 || K > 32 || E < 1 || E > 1024 || R < 1 || L < 1 || E % L != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (idx_bits != 32 && idx_bits != 64) return MOE_ERR_INVALID_ARG;
+  if (counts == nullptr || stats == nullptr || (T > 0 && topk_idx == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(stats) & 7u) != 0) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * K > (int64_t{1} << 31) - 1) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_layer_stats(topk_idx, idx_bits, counts, T, K, E, L, R, rank_offsets,
+                                      reinterpret_cast<unsigned long long*>(stats),
+                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_combine(const void* out, const int32_t* src_map, const float* topk_w, int T, int H,
