@@ -306,6 +306,57 @@ moe_status moe_combine_packed(const void* out, int64_t rows, const int32_t* src_
                               moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Per-source fixed slots -- the low-latency receive layout of "DeepEP 架构与实现笔记",
+ * §9.5: the receive buffer is [L, W*max_tokens, H] per rank and every source
+ * rank owns a fixed range of max_tokens slots inside every expert, so a route's
+ * row follows from its source rank and its position among that source's routes
+ * to the expert, with no layout agreed across ranks first (no global count or
+ * scan).  The cost, as the page says: a larger buffer whose padding rows lie
+ * between the source ranges, which the expert GEMM must skip.  On one GPU the
+ * W = E / L logical ranks' experts share one buffer:
+ *
+ * moe_dispatch_source_slots
+ *   x, topk_idx, idx_bits, topk_w, T, H, K as for moe_dispatch_ex
+ *   L            local experts per logical rank (E % L == 0, W = E / L ranks)
+ *   max_tokens   slots per source range (the page's max tokens per rank)
+ *   rank_offsets device, int32 [W + 1]: source rank r's tokens are
+ *                [rank_offsets[r], rank_offsets[r+1]), or NULL for
+ *                ceil(T / W) tokens per rank (the last ones fewer)
+ *   recv         device, BF16 [E, W*max_tokens, H]: route (t, k) of source rank
+ *                r to expert e, the p-th of r's routes to e in ascending route
+ *                id, lands at row r*max_tokens + p of expert e; other rows
+ *                untouched
+ *   counts       device, int32 [E]: valid rows per expert (the page's masked_m)
+ *   seg_counts   device, int32 [E, W]: valid rows of each (expert, source) range
+ *   src_map      device, int32 [T, K]: q = e*W*max_tokens + r*max_tokens + p, or -1
+ *   dev_status   as for moe_dispatch; a route with p >= max_tokens is dropped
+ *                (MOE_DEV_CAPACITY_DROPPED, counted in dev_status[1])
+ * No workspace: each source rank's slots are computed by its own blocks.
+ *
+ * moe_expert_compute_source_slots -- moe_expert_compute on that layout: the
+ *   tiles of expert e cover its rows up to its last valid row, the gaps
+ *   between source ranges are skipped by quantisation and never stored.
+ *   recv/out device BF16 [E, W*max_tokens, H]; counts may be NULL (not read);
+ *   seg_counts from moe_dispatch_source_slots; workspace of
+ *   moe_expert_compute_workspace_size(E, W*max_tokens, H, I) bytes; flags as
+ *   for moe_expert_compute_ex.  Output rows equal those of the padded layout
+ *   for the same routes, bit for bit.  Combine with moe_combine(out, src_map,
+ *   topk_w, T, H, K, E, W*max_tokens, y).
+ * ------------------------------------------------------------------------- */
+moe_status moe_dispatch_source_slots(const void* x, const void* topk_idx, int idx_bits,
+                                     const float* topk_w, int T, int H, int K, int E, int L,
+                                     int max_tokens, const int32_t* rank_offsets, void* recv,
+                                     int32_t* counts, int32_t* seg_counts, int32_t* src_map,
+                                     int32_t* dev_status, moe_stream_t stream);
+moe_status moe_expert_compute_source_slots(const void* recv, const int32_t* counts,
+                                           const int32_t* seg_counts, int E, int L,
+                                           int max_tokens, int H, int I, const uint8_t* w13,
+                                           const float* w13_scale, const uint8_t* w2,
+                                           const float* w2_scale, void* out, int32_t* dev_status,
+                                           void* workspace, size_t workspace_bytes, int flags,
+                                           moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * moe_dispatch_ex -- the general dispatch: moe_dispatch and moe_dispatch_packed
  * are its two common cases.
  *   topk_idx   device, [T, K] router ids, int32 (idx_bits = 32) or int64
@@ -333,7 +384,8 @@ moe_status moe_dispatch_ex(const void* x, const void* topk_idx, int idx_bits, co
  *          Default: the first I rows gate, the last I up ("SGLang Expert
  *          Compute Backend", §3.6).
  *          MOE_GEMM_ONE_LAUNCH / MOE_GEMM_TWO_LAUNCHES: force the GEMMs' launch
- *          form (see below); at most one of them.
+ *          form (see below); at most one of them.  MOE_GEMM_MAX_CTAS(n): cap
+ *          the GEMMs' grid at n SMs.
  * Workspace: moe_expert_compute_ex_workspace_size(E, R, rows, H, I) bytes.
  * MOE_ERR_INVALID_ARG for unknown flag bits.
  * ------------------------------------------------------------------------- */
@@ -344,6 +396,11 @@ moe_status moe_dispatch_ex(const void* x, const void* topk_idx, int idx_bits, co
  * These flags force one form or the other. */
 #define MOE_GEMM_ONE_LAUNCH 2
 #define MOE_GEMM_TWO_LAUNCHES 4
+/* At most n CTAs (SMs) for the GEMMs' persistent grids, 1 <= n <= 32767; the
+ * default (n = 0) takes one CTA per SM.  Leaves SMs to kernels of other
+ * streams, e.g. the other micro-batch's dispatch and combine in a two-batch
+ * overlap ("SGLang、NCCL 与 MoE EP", §2.4).  Combine with | into flags. */
+#define MOE_GEMM_MAX_CTAS(n) ((int)(((unsigned)(n) & 0x7FFFu) << 16))
 size_t moe_expert_compute_ex_workspace_size(int E, int R, int64_t rows, int H, int I);
 moe_status moe_expert_compute_ex(const void* recv, const int32_t* counts, int E, int R, int64_t rows,
                                  int H, int I, const uint8_t* w13, const float* w13_scale,
@@ -378,6 +435,15 @@ moe_status moe_expert_compute_ex(const void* recv, const int32_t* counts, int E,
 moe_status moe_layer_stats(const void* topk_idx, int idx_bits, const int32_t* counts, int T, int K,
                            int E, int L, int R, const int32_t* rank_offsets, uint64_t* stats,
                            moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_expert_compute_gemm_launches -- how many launches the GEMMs of
+ * moe_expert_compute_ex take on this device for these sizes and flags: 1 (both
+ * GEMMs in one launch) or 2 (gate/up, then down); rows as for
+ * moe_expert_compute_ex.  A negative moe_status for bad arguments or an
+ * unsupported device.  Host only.
+ * ------------------------------------------------------------------------- */
+int moe_expert_compute_gemm_launches(int E, int R, int64_t rows, int I, int flags);
 
 /* ---------------------------------------------------------------------------
  * moe_expert_compute_workspace_layout -- where moe_expert_compute_ex (and so

@@ -82,6 +82,16 @@ def test_workspace_layout_is_the_carved_one(lib, E, R, rows, H, I):
     assert lib.moe_expert_compute_workspace_layout(E, R, rows, H, I, None) == -1
 
 
+def test_gemm_launch_form_query(lib):
+    """Forced forms answer without a device; bad sizes and flag bits are
+    rejected; MOE_GEMM_MAX_CTAS(n) is a known flag."""
+    assert lib.moe_expert_compute_gemm_launches(8, 128, 0, 256, 2) == 1
+    assert lib.moe_expert_compute_gemm_launches(8, 128, 0, 256, 4 | (100 << 16)) == 2
+    assert lib.moe_expert_compute_gemm_launches(8, 128, 0, 200, 2) == -1
+    assert lib.moe_expert_compute_gemm_launches(8, 128, 0, 256, 2 | 4) == -1
+    assert lib.moe_expert_compute_gemm_launches(8, 128, 0, 256, 8) == -1
+
+
 FAKE = ctypes.c_void_p(4096)   # aligned, never dereferenced: validation fails first
 
 

@@ -31,6 +31,13 @@ SIGNATURES = {
     "moe_dispatch_quant_ex": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
                                       c_int, c_int, c_int64, c_void_p, c_void_p, c_void_p,
                                       c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_dispatch_source_slots": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_int,
+                                          c_int, c_int, c_int, c_void_p, c_void_p, c_void_p,
+                                          c_void_p, c_void_p, c_void_p, c_void_p]),
+    "moe_expert_compute_source_slots": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                                c_int, c_int, c_void_p, c_void_p, c_void_p,
+                                                c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                                c_int, c_void_p]),
     "moe_expert_compute_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
     "moe_expert_compute": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p,
                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -61,6 +68,7 @@ SIGNATURES = {
                                       c_void_p, c_size_t, c_int, c_void_p]),
     "moe_layer_stats": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                 c_void_p, c_void_p, c_void_p]),
+    "moe_expert_compute_gemm_launches": (c_int, [c_int, c_int, c_int64, c_int, c_int]),
     "moe_expert_compute_workspace_layout": (c_int, [c_int, c_int, c_int64, c_int, c_int, c_void_p]),
     "moe_gemm_gateup_down_sync_size": (c_size_t, [c_int, c_int, c_int64]),
     "moe_gemm_gateup_down": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int64, c_int,

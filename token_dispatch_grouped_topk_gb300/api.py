@@ -19,7 +19,8 @@ __all__ = [
     "moe_dispatch_quant",
     "moe_expert_compute", "moe_combine", "moe_quantize_fp8", "moe_gemm_gateup_silu",
     "moe_gemm_down", "moe_gemm_gateup_down", "moe_dispatch_packed", "moe_expert_compute_packed",
-    "moe_combine_packed", "moe_layer_stats", "layer_stats_dict", "LAYER_STATS",
+    "moe_combine_packed", "moe_dispatch_source_slots", "moe_expert_compute_source_slots",
+    "moe_layer_stats", "layer_stats_dict", "LAYER_STATS",
     "packed_rows", "MoeLayerBuffers", "HostPipeline", "TwoBatchOverlap", "DEV_BAD_EXPERT_ID",
     "DEV_CAPACITY_DROPPED", "DEV_TIMEOUT",
 ]
@@ -72,10 +73,14 @@ def _workspace(nbytes, device):
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
-def _gemm_flags(w13_interleaved, gemm_launch):
+def _gemm_flags(w13_interleaved, gemm_launch, max_ctas=0):
     """Flags of the GEMM launch form: None = the library's choice by tile
-    count, "one" = both GEMMs in one launch, "two" = gate/up then down."""
+    count, "one" = both GEMMs in one launch, "two" = gate/up then down;
+    max_ctas > 0 caps the GEMMs' persistent grid (MOE_GEMM_MAX_CTAS)."""
     f = _lib.W13_INTERLEAVED if w13_interleaved else 0
+    if not 0 <= max_ctas <= 0x7FFF:
+        raise ValueError("max_ctas must be in [0, 32767]")
+    f |= max_ctas << 16
     if gemm_launch == "one":
         return f | _lib.GEMM_ONE_LAUNCH
     if gemm_launch == "two":
@@ -157,7 +162,8 @@ def moe_dispatch_quant(x, topk_idx, topk_w, E: int, R: int, *, xq=None, xs=None,
 
 
 def moe_expert_compute(recv, counts, w13, w13_scale, w2, w2_scale, *, out=None, dev_status=None,
-                       workspace=None, stream=None, w13_interleaved=False, gemm_launch=None):
+                       workspace=None, stream=None, w13_interleaved=False, gemm_launch=None,
+                       max_ctas=0):
     """Quantise the valid rows and run the grouped gated-SiLU FP8 expert MLP.
     Returns ``out [E,R,H] bf16`` (rows past counts[e] untouched).  With
     ``w13_interleaved`` the W13 rows alternate gate and up (moe_expert_compute_ex)."""
@@ -174,9 +180,67 @@ def moe_expert_compute(recv, counts, w13, w13_scale, w2, w2_scale, *, out=None, 
         workspace = _workspace(lib.moe_expert_compute_workspace_size(E, R, H, I), dev)
     st = lib.moe_expert_compute_ex(_p(recv), _p(counts), E, R, 0, H, I, _p(w13), _p(w13_scale),
                                    _p(w2), _p(w2_scale), _p(out), _p(dev_status), _p(workspace),
-                                   workspace.numel(), _gemm_flags(w13_interleaved, gemm_launch),
-                                   _s(stream))
+                                   workspace.numel(),
+                                   _gemm_flags(w13_interleaved, gemm_launch, max_ctas), _s(stream))
     _lib.check("moe_expert_compute_ex", st)
+    return out
+
+
+def moe_dispatch_source_slots(x, topk_idx, topk_w, E: int, L: int, max_tokens: int, *,
+                              rank_offsets=None, recv=None, counts=None, seg_counts=None,
+                              src_map=None, dev_status=None, stream=None):
+    """Dispatch into the per-source fixed-slot layout (moe_dispatch_source_slots):
+    expert e's W*max_tokens rows hold one range of max_tokens slots per source
+    rank.  Returns ``(recv [E, W*max_tokens, H] bf16, counts [E], seg_counts
+    [E, W], src_map [T, K], dev_status)``."""
+    lib = _lib.load()
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    W = E // L
+    dev = x.device
+    _need(x, torch.bfloat16, "x")
+    bits = _idx_bits(topk_idx)
+    _need(topk_idx, topk_idx.dtype, "topk_idx")
+    if recv is None:
+        recv = torch.empty(E, W * max_tokens, H, dtype=torch.bfloat16, device=dev)
+    if counts is None:
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+    if seg_counts is None:
+        seg_counts = torch.empty(E, W, dtype=torch.int32, device=dev)
+    if src_map is None:
+        src_map = torch.empty(T, K, dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.empty(2, dtype=torch.int32, device=dev)
+    st = lib.moe_dispatch_source_slots(_p(x), _p(topk_idx), bits, _p(topk_w), T, H, K, E, L,
+                                       max_tokens, _p(rank_offsets), _p(recv), _p(counts),
+                                       _p(seg_counts), _p(src_map), _p(dev_status), _s(stream))
+    _lib.check("moe_dispatch_source_slots", st)
+    return recv, counts, seg_counts, src_map, dev_status
+
+
+def moe_expert_compute_source_slots(recv, counts, seg_counts, L: int, max_tokens: int, w13,
+                                    w13_scale, w2, w2_scale, *, out=None, dev_status=None,
+                                    workspace=None, stream=None, w13_interleaved=False,
+                                    gemm_launch=None):
+    """``moe_expert_compute`` on the per-source fixed-slot layout: only the rows
+    that hold a route are quantised and stored.  Returns ``out [E, W*max_tokens,
+    H] bf16`` (other rows untouched)."""
+    lib = _lib.load()
+    E, R, H = recv.shape
+    w13, w2 = _u8(w13), _u8(w2)
+    I = w13.shape[1] // 2
+    dev = recv.device
+    if out is None:
+        out = torch.empty(E, R, H, dtype=torch.bfloat16, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(2, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _workspace(lib.moe_expert_compute_workspace_size(E, R, H, I), dev)
+    st = lib.moe_expert_compute_source_slots(
+        _p(recv), _p(counts), _p(seg_counts), E, L, max_tokens, H, I, _p(w13), _p(w13_scale),
+        _p(w2), _p(w2_scale), _p(out), _p(dev_status), _p(workspace), workspace.numel(),
+        _gemm_flags(w13_interleaved, gemm_launch), _s(stream))
+    _lib.check("moe_expert_compute_source_slots", st)
     return out
 
 
@@ -403,9 +467,18 @@ class MoeLayerBuffers:
     packed: bool = False   # packed layout (moe_*_packed): [rows, H] buffers, no capacity gaps
     w13_interleaved: bool = False   # W13 rows alternate gate and up
     gemm_launch: str | None = None  # None: the library's choice; "one" / "two" launches
+    # per-source fixed slots (moe_*_source_slots): max tokens per source rank
+    # (0: off); then R must be (E / L) * source_slots, rank_offsets optional
+    source_slots: int = 0
+    L: int = 1
+    rank_offsets: torch.Tensor | None = None
 
     def __post_init__(self):
         d, E, R, H, I, T, K = self.device, self.E, self.R, self.H, self.I, self.T, self.K
+        if self.source_slots:
+            if self.packed or E % self.L or R != (E // self.L) * self.source_slots:
+                raise ValueError("source slots: padded lane with R = (E / L) * max_tokens")
+            self.seg_counts = torch.zeros(E, E // self.L, dtype=torch.int32, device=d)
         if self.packed:
             self.rows = packed_rows(T, K, E, R)
             shape = (self.rows, H)
@@ -455,6 +528,8 @@ class MoeLayerBuffers:
         """The same layer with dispatch and quantisation fused (moe_dispatch_quant_ex
         -> both GEMMs in one launch -> combine); the BF16 receive buffer is not
         used.  Returns ``y`` (bit-identical to ``forward``), padded or packed."""
+        if self.source_slots:
+            raise ValueError("forward_fused runs on the padded and packed layouts")
         y = self.y if y is None else y
         rows = self.rows if self.packed else 0
         xq, xs, zq, zs = self.workspace_views()
@@ -475,6 +550,20 @@ class MoeLayerBuffers:
         """dispatch -> expert compute -> combine on one stream; returns ``y``
         (the lane's own output buffer unless ``y`` [T, H] BF16 is given)."""
         y = self.y if y is None else y
+        if self.source_slots:
+            moe_dispatch_source_slots(x, topk_idx, topk_w, self.E, self.L, self.source_slots,
+                                      rank_offsets=self.rank_offsets, recv=self.recv,
+                                      counts=self.counts, seg_counts=self.seg_counts,
+                                      src_map=self.src_map, dev_status=self.dev_status,
+                                      stream=stream)
+            moe_expert_compute_source_slots(self.recv, self.counts, self.seg_counts, self.L,
+                                            self.source_slots, w13, w13_scale, w2, w2_scale,
+                                            out=self.out, dev_status=self.dev_status,
+                                            workspace=self.ws_compute, stream=stream,
+                                            w13_interleaved=self.w13_interleaved,
+                                            gemm_launch=self.gemm_launch)
+            moe_combine(self.out, self.src_map, topk_w, y=y, stream=stream)
+            return y
         if self.packed:
             moe_dispatch_packed(x, topk_idx, topk_w, self.E, self.R, recv=self.recv,
                                 counts=self.counts, src_map=self.src_map,
@@ -565,7 +654,8 @@ class TwoBatchOverlap:
     one stream (the "serial split" of "SGLang Expert Compute Backend", §5.6).
     Both produce the same bytes."""
 
-    def __init__(self, T: int, E: int, K: int, H: int, I: int, R: int, device):
+    def __init__(self, T: int, E: int, K: int, H: int, I: int, R: int, device, gemm_ctas: int = 0):
+        self.gemm_ctas = gemm_ctas   # > 0: the expert compute's GEMMs take at most this many SMs
         self.half = T // 2
         self.sizes = (self.half, T - self.half)
         self.lanes = [MoeLayerBuffers(n, E, K, H, I, R, device) for n in self.sizes]
@@ -588,7 +678,8 @@ class TwoBatchOverlap:
                          workspace=lane.ws_dispatch, stream=stream)
         elif name == "compute":
             moe_expert_compute(lane.recv, lane.counts, *weights, out=lane.out,
-                               dev_status=lane.dev_status, workspace=lane.ws_compute, stream=stream)
+                               dev_status=lane.dev_status, workspace=lane.ws_compute, stream=stream,
+                               max_ctas=self.gemm_ctas)
         else:
             moe_combine(lane.out, lane.src_map, w, y=lane.y, stream=stream)
 

@@ -376,8 +376,9 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tpw = 32 / K;
   const int per = (T + W - 1) / W;
-  const int t0 = rank_offsets ? rank_offsets[r] : min(T, r * per);
-  const int t1 = rank_offsets ? rank_offsets[r + 1] : min(T, (r + 1) * per);
+  // this source rank's tokens, clamped to [0, T] whatever the offsets say
+  const int t0 = max(0, min(T, rank_offsets ? rank_offsets[r] : r * per));
+  const int t1 = max(t0, min(T, rank_offsets ? rank_offsets[r + 1] : (r + 1) * per));
   const int64_t R = static_cast<int64_t>(W) * mt;
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_pos[e] = 0;
   const int nvec = H / 8;
@@ -518,6 +519,42 @@ cudaError_t dispatch_impl(const void* x, const IdT* topk_idx, int T, int H, int 
   return cudaGetLastError();
 }
 }  // namespace
+
+namespace {
+template <typename IdT>
+cudaError_t source_slots_impl(const void* x, const IdT* topk_idx, int T, int H, int K, int E,
+                              int W, int mt, const int32_t* rank_offsets, void* recv,
+                              int32_t* counts, int32_t* seg_counts, int32_t* src_map,
+                              int32_t* dev_status, int sm_count, cudaStream_t s) {
+  cudaError_t err = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
+  if (err == cudaSuccess) err = cudaMemsetAsync(counts, 0, E * sizeof(int32_t), s);
+  if (err != cudaSuccess) return err;
+  const int nvec = H / 8;
+  int hsplit = row_slices(W, nvec, 32, sm_count);
+  const int vec_per_slice = (nvec + hsplit - 1) / hsplit;
+  hsplit = (nvec + vec_per_slice - 1) / vec_per_slice;
+  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + E) * sizeof(int);
+  if ((err = allow_smem(route_source_slots_kernel<IdT>, smem)) != cudaSuccess) return err;
+  route_source_slots_kernel<IdT><<<dim3(W, hsplit), kDispatchWarps * 32, smem, s>>>(
+      static_cast<const uint4*>(x), topk_idx, T, H, K, E, W, mt, rank_offsets,
+      static_cast<uint4*>(recv), counts, seg_counts, src_map, dev_status, vec_per_slice);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_dispatch_source_slots(const void* x, const void* topk_idx, int idx_bits, int T,
+                                         int H, int K, int E, int W, int mt,
+                                         const int32_t* rank_offsets, void* recv, int32_t* counts,
+                                         int32_t* seg_counts, int32_t* src_map,
+                                         int32_t* dev_status, int sm_count, cudaStream_t s) {
+  if (idx_bits == 32)
+    return source_slots_impl(x, static_cast<const int32_t*>(topk_idx), T, H, K, E, W, mt,
+                             rank_offsets, recv, counts, seg_counts, src_map, dev_status,
+                             sm_count, s);
+  return source_slots_impl(x, static_cast<const int64_t*>(topk_idx), T, H, K, E, W, mt,
+                           rank_offsets, recv, counts, seg_counts, src_map, dev_status, sm_count,
+                           s);
+}
 
 cudaError_t launch_dispatch(const void* x, const void* topk_idx, int idx_bits, int T, int H, int K,
                             int E, RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,

@@ -109,6 +109,8 @@ struct GemmArgs {
   int inter;               // W13 rows interleaved (2j gate, 2j+1 up) instead of the
                            // first I gate and the last I up
   long long rows;          // their row count
+  int seg;                 // per-source slots: rows per source range (0: none)
+  const int32_t* seg_counts;  // [E, R / seg] valid rows per range
   int32_t* dev_status;
 };
 
@@ -336,7 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Block prefix per expert (ends with __syncthreads, which also publishes the
   // barrier initialisation and the TMEM address).
-  expert_prefix(args.counts, args.E, args.R, kBM, 1, ctl->blk_start, ctl->cnt);
+  // per-source slots: each expert's tiles cover its rows up to its last valid one
+  if (args.seg) source_slot_extents(args.seg_counts, args.E, args.R, args.seg, ctl->cnt);
+  expert_prefix(args.seg ? ctl->cnt : args.counts, args.E, args.R, kBM, 1, ctl->blk_start,
+                ctl->cnt);
   if (args.packed) expert_prefix(args.counts, args.E, args.R, 1, 1, ctl->cnt, nullptr);
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
@@ -568,7 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         nxt.t = t_next;
         if (t_next >= 0) epi_prepare<BN, kMode>(&nxt, ctl, args, row, ch);
       }
-      const bool valid = row < tl.rows && grow < args.rows;
+      // rows stored: inside the tile's valid range and the buffer, and (per-source
+      // slots) a row that holds a route; bit r of vmask is the warp's row r
+      const bool valid = row < tl.rows && grow < args.rows &&
+                         (!args.seg || source_slot_valid(args.seg_counts, args.R, args.seg, tl.e,
+                                                         tl.m_blk * kBM + row));
+      const unsigned vmask = __ballot_sync(0xffffffffu, valid);
       if (kMode != kModeDown && tl.gu) {
         // Z = SiLU(gate) * up on this thread's 64 columns (written over the
         // gate half of acc2), then the row amax over the tile's 128 Z columns
@@ -633,13 +643,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
           const long long grow0 = static_cast<long long>(tl.base) + lq * 32;  // warp's first row
-          const int nvalid = static_cast<int>(                   // rows of this warp to store
-              min(static_cast<long long>(min(32, tl.rows - lq * 32)), args.rows - grow0));
           const int c = lane & 3;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int r = 8 * i + (lane >> 2);
-            if (r < nvalid) {
+            if ((vmask >> r) & 1u) {
               const uint4 v = *reinterpret_cast<const uint4*>(stage + r * kStageRowBytes + 16 * c);
               *reinterpret_cast<uint4*>(args.zq + (grow0 + r) * args.I + tl.n_blk * 128 + ch * 64 +
                                         16 * c) = v;
@@ -665,8 +673,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 8 rows x 64 bytes per store instruction.
         uint8_t* stage = out_stage + ew * kStageWarpBytes;
         const long long grow0 = static_cast<long long>(tl.base) + lq * 32;  // warp's first row
-        const int nvalid = static_cast<int>(                   // rows of this warp to store
-            min(static_cast<long long>(min(32, tl.rows - lq * 32)), args.rows - grow0));
         __nv_bfloat16* gbase = args.out + grow0 * args.H + tl.n_blk * BN + ch * kCols;
         // lane -> (row 8i + lane/4, 16-byte chunk lane%4) of each store instruction i
         const int c = lane & 3;
@@ -689,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            if (8 * i + (lane >> 2) < nvalid) {
+            if ((vmask >> (8 * i + (lane >> 2))) & 1u) {
               const uint4 v = *reinterpret_cast<const uint4*>(stage + sidx + i * 8 * kStageRowBytes);
               *reinterpret_cast<uint4*>(gbase + goff + i * gstep + 32 * r) = v;
             }
@@ -806,6 +812,8 @@ GemmArgs common_args(const int32_t* counts, int E, RowLayout rl, int H, int I,
   a.nt_dn = H % 256 == 0 ? H / 256 : H / 128;
   a.packed = rl.packed;
   a.rows = rl.rows;
+  a.seg = rl.seg;
+  a.seg_counts = rl.seg_counts;
   a.dev_status = dev_status;
   return a;
 }

@@ -23,13 +23,21 @@ const DeviceInfo* current_device_info();
 // clamped counts c_e = min(counts[e], R), so the valid rows are contiguous
 // ("SGLang Expert Compute Backend", §2.6, compact storage).  `rows` is the
 // row count of those buffers: E*R when padded, at least the largest possible
-// sum of counts when packed.
+// sum of counts when packed.  Per-source fixed slots ("DeepEP 架构与实现笔记",
+// §9.5; padded only): expert e's R rows are R / seg ranges of seg rows, one
+// per source rank, and row m is valid iff m % seg < seg_counts[e * (R / seg) +
+// m / seg]; the rows an expert's tiles cover run to its last valid row.
 struct RowLayout {
   int R;
   int packed;
   int64_t rows;
+  int seg = 0;                          // rows per source range, 0: not segmented
+  const int32_t* seg_counts = nullptr;  // [E, R / seg] valid rows per range
 };
 inline RowLayout padded_rows(int E, int R) { return RowLayout{R, 0, static_cast<int64_t>(E) * R}; }
+inline RowLayout source_slot_rows(int E, int R, int seg, const int32_t* seg_counts) {
+  return RowLayout{R, 0, static_cast<int64_t>(E) * R, seg, seg_counts};
+}
 
 // ----- dispatch (route validation, histogram, scan, stable scatter)
 constexpr int kDispatchWarps = 8;
@@ -50,6 +58,15 @@ constexpr int kSinglePassRoutes = 4096;
 cudaError_t launch_dispatch(const void* x, const void* topk_idx, int idx_bits, int T, int H, int K,
                             int E, RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
                             int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s);
+
+// ----- per-source fixed-slot dispatch: recv [E, W * mt, H]; counts [E] valid
+// rows per expert, seg_counts [E, W] per (expert, source rank); rank_offsets
+// [W + 1] token offsets of the source ranks, or null for ceil(T / W) each
+cudaError_t launch_dispatch_source_slots(const void* x, const void* topk_idx, int idx_bits, int T,
+                                         int H, int K, int E, int W, int mt,
+                                         const int32_t* rank_offsets, void* recv, int32_t* counts,
+                                         int32_t* seg_counts, int32_t* src_map,
+                                         int32_t* dev_status, int sm_count, cudaStream_t s);
 
 // ----- dispatch fused with the per-token FP8 quantisation: xq e4m3 and xs
 // (row layout rl, int32 or int64 ids) instead of the BF16 receive buffer

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <mutex>
 
@@ -102,17 +103,22 @@ cudaError_t run_gemms(const uint8_t* xq, const float* xs, const int32_t* counts,
   const bool one = (flags & MOE_GEMM_ONE_LAUNCH)     ? true
                    : (flags & MOE_GEMM_TWO_LAUNCHES) ? false
                                                      : gemm_prefer_one_launch(E, rl, I, sm_count);
+  // MOE_GEMM_MAX_CTAS(n): the persistent grids take at most n SMs
+  const int cap = (flags >> 16) & 0x7FFF;
+  const int grid = cap > 0 ? std::min(cap, sm_count) : sm_count;
   if (one)
     return launch_gemm_gateup_down(xq, xs, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, zq,
-                                   zs, out, sync, sync_ints, dev_status, sm_count, s, inter);
+                                   zs, out, sync, sync_ints, dev_status, grid, s, inter);
   cudaError_t err = launch_gemm_gateup(xq, xs, counts, E, rl, H, I, w13, w13_scale, zq, zs,
-                                       dev_status, sm_count, s, inter);
+                                       dev_status, grid, s, inter);
   if (err != cudaSuccess) return err;
-  return launch_gemm_down(zq, zs, counts, E, rl, H, I, w2, w2_scale, out, dev_status, sm_count, s);
+  return launch_gemm_down(zq, zs, counts, E, rl, H, I, w2, w2_scale, out, dev_status, grid, s);
 }
 
 bool valid_gemm_flags(int flags) {
-  return (flags & ~(MOE_W13_INTERLEAVED | MOE_GEMM_ONE_LAUNCH | MOE_GEMM_TWO_LAUNCHES)) == 0 &&
+  const int known = MOE_W13_INTERLEAVED | MOE_GEMM_ONE_LAUNCH | MOE_GEMM_TWO_LAUNCHES |
+                    MOE_GEMM_MAX_CTAS(0x7FFF);
+  return (flags & ~known) == 0 &&
          !((flags & MOE_GEMM_ONE_LAUNCH) && (flags & MOE_GEMM_TWO_LAUNCHES));
 }
 
@@ -210,6 +216,65 @@ moe_status moe_dispatch_packed(const void* x, const int64_t* topk_idx, const flo
   if (rows == 0) return MOE_ERR_INVALID_ARG;
   return moe_dispatch_ex(x, topk_idx, 64, topk_w, T, H, K, E, R, rows, recv, counts, src_map,
                          dev_status, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_dispatch_source_slots(const void* x, const void* topk_idx, int idx_bits,
+                                     const float* topk_w, int T, int H, int K, int E, int L,
+                                     int max_tokens, const int32_t* rank_offsets, void* recv,
+                                     int32_t* counts, int32_t* seg_counts, int32_t* src_map,
+                                     int32_t* dev_status, moe_stream_t stream) {
+  (void)topk_w;
+  if (T < 0 || !valid_hidden(H) || K < 1 || K > 32 || L < 1 || E % L != 0 || K > E ||
+      max_tokens < 1)
+    return MOE_ERR_INVALID_ARG;
+  const int W = E / L;
+  if (!valid_experts(E, static_cast<int>(std::min<int64_t>(int64_t{W} * max_tokens, INT32_MAX))) ||
+      int64_t{W} * max_tokens > (int64_t{1} << 30))
+    return MOE_ERR_INVALID_ARG;
+  if (idx_bits != 32 && idx_bits != 64) return MOE_ERR_INVALID_ARG;
+  if (counts == nullptr || seg_counts == nullptr || dev_status == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || topk_idx == nullptr || recv == nullptr || src_map == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(x) || !aligned16(recv))) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * K > (int64_t{1} << 31) - 1) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_dispatch_source_slots(
+      x, topk_idx, idx_bits, T, H, K, E, W, max_tokens, rank_offsets, recv, counts, seg_counts,
+      src_map, dev_status, dev->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_compute_source_slots(const void* recv, const int32_t* counts,
+                                           const int32_t* seg_counts, int E, int L,
+                                           int max_tokens, int H, int I, const uint8_t* w13,
+                                           const float* w13_scale, const uint8_t* w2,
+                                           const float* w2_scale, void* out, int32_t* dev_status,
+                                           void* workspace, size_t workspace_bytes, int flags,
+                                           moe_stream_t stream) {
+  (void)counts;  // the tile list follows seg_counts
+  if (L < 1 || E % L != 0 || max_tokens < 1 || !valid_hidden(H) || !valid_hidden(I))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t R64 = int64_t{E / L} * max_tokens;
+  if (R64 > (int64_t{1} << 30) || !valid_experts(E, static_cast<int>(R64)))
+    return MOE_ERR_INVALID_ARG;
+  const int R = static_cast<int>(R64);
+  if (!valid_gemm_flags(flags)) return MOE_ERR_INVALID_ARG;
+  if (recv == nullptr || seg_counts == nullptr || w13 == nullptr || w13_scale == nullptr ||
+      w2 == nullptr || w2_scale == nullptr || out == nullptr || dev_status == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(recv) || !aligned16(w13) || !aligned16(w2) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  const ComputeWorkspace w = compute_workspace(E, R, H, I);
+  if (workspace == nullptr || workspace_bytes < w.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  // the tile list and the stored rows come from seg_counts; counts is not read
+  return expert_compute_impl(recv, seg_counts, E, source_slot_rows(E, R, max_tokens, seg_counts),
+                             H, I, w13, w13_scale, w2, w2_scale, out, dev_status, workspace, w,
+                             dev->sm_count, reinterpret_cast<cudaStream_t>(stream), flags);
 }
 
 moe_status moe_dispatch_quant_ex(const void* x, const void* topk_idx, int idx_bits,
@@ -383,6 +448,18 @@ moe_status moe_expert_compute_packed(const void* recv, const int32_t* counts, in
 size_t moe_expert_compute_ex_workspace_size(int E, int R, int64_t rows, int H, int I) {
   if (rows == 0) return moe_expert_compute_workspace_size(E, R, H, I);
   return moe_expert_compute_packed_workspace_size(rows, H, I);
+}
+
+int moe_expert_compute_gemm_launches(int E, int R, int64_t rows, int I, int flags) {
+  if (!valid_hidden(I) || !valid_gemm_flags(flags)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0 ? !valid_experts(E, R) : (!valid_experts(E, R) || !valid_rows(rows)))
+    return MOE_ERR_INVALID_ARG;
+  if (flags & MOE_GEMM_ONE_LAUNCH) return 1;
+  if (flags & MOE_GEMM_TWO_LAUNCHES) return 2;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  const RowLayout rl = rows == 0 ? padded_rows(E, R) : RowLayout{R, 1, rows};
+  return gemm_prefer_one_launch(E, rl, I, dev->sm_count) ? 1 : 2;
 }
 
 int moe_expert_compute_workspace_layout(int E, int R, int64_t rows, int H, int I,

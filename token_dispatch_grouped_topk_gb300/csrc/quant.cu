@@ -36,7 +36,9 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   int* s_rows = smem + 2 * E + 1;    // [E + 1] packed row bases
   float* s_scale = reinterpret_cast<float*>(smem + 3 * E + 2);  // [G][kRowsPerBlock]
   const int R = rl.R;
-  expert_prefix(counts, E, R, kRowsPerBlock, 1, s_start, s_cnt);
+  // per-source slots: rows up to each expert's last valid row, gaps skipped
+  if (rl.seg) source_slot_extents(rl.seg_counts, E, R, rl.seg, s_cnt);
+  expert_prefix(rl.seg ? s_cnt : counts, E, R, kRowsPerBlock, 1, s_start, s_cnt);
   if (rl.packed) expert_prefix(counts, E, R, 1, 1, s_rows, nullptr);
   const int G = H / kGroup;
   const int nvec = H / 8;
@@ -52,6 +54,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
         min(static_cast<int64_t>(min(kRowsPerBlock, s_cnt[e] - row0)), rl.rows - base));
     if (nrows <= 0) continue;
     for (int r = warp; r < nrows; r += kQuantWarps) {
+      if (rl.seg && !source_slot_valid(rl.seg_counts, R, rl.seg, e, row0 + r)) continue;
       const size_t row = static_cast<size_t>(base) + r;
       const uint4* src = recv + row * nvec;
       uint2* dst = xq + row * (H / 8);
