@@ -234,6 +234,24 @@ def barrier(world: int):
 
 # ------------------------------------------------------------------ CPU oracle
 
+def host_description() -> dict:
+    """CPU model and core count of this host (the oracle baseline's hardware)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True,
+                             timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"cpu_model": model, "nproc": os.cpu_count()}
+
+
 def cpu_oracle_sample(wl, n_experts: int, rows_per_expert: int, seed: int = 0) -> dict:
     """Times the oracle, as it stands, on a bounded sample of the workload:
     the routing pass over the whole batch (charged pro rata to the sampled
@@ -266,133 +284,251 @@ def cpu_oracle_sample(wl, n_experts: int, rows_per_expert: int, seed: int = 0) -
     return {"value": rows / total, "unit": UNIT, "seconds": t_route + t_exp, "rows": rows,
             "sample": (f"{rows} kept routes of the {wl.name} layer on its {n_experts} busiest experts "
                        f"({rows_per_expert} rows each): quant, gate/up GEMM, SiLU*up, requant, down GEMM, "
-                       f"combine; plus the full routing pass over {wl.T * wl.K} routes charged pro rata"),
-            "cores": int(torch.get_num_threads())}
+                       f"combine; plus the full routing pass over {wl.T * wl.K} routes charged pro rata")}
+
+
+def cpu_oracle_sample_single_thread(wl, n_experts: int, rows_per_expert: int) -> dict | None:
+    """The same sample in a child process whose BLAS and OpenMP pools are
+    limited to one thread; None if the child fails."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample", wl.name,
+           "--cpu-experts", str(n_experts), "--cpu-rows", str(rows_per_expert)]
+    try:
+        p = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, env=env,
+                           timeout=600)
+        return json.loads(p.stdout.strip().splitlines()[-1]) if p.returncode == 0 else None
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
+
+
+def cpu_small_kernels_full(wl, seed: int = 0) -> dict:
+    """The oracle's routing, scatter, quantisation and combine over the whole
+    batch of a workload (every token, every kept route), timed as they stand;
+    the expert MLP is not part of this figure."""
+    import oracle as O
+    from token_dispatch_grouped_topk_gb300 import workloads as W
+
+    idx, w = W.router(wl.T, wl.E, wl.K, W.router_bias(wl, seed, "cpu"), seed + 1, "cpu")
+    x = W.activations(wl.T, wl.H, seed + 2, "cpu").float().numpy()
+    idx_np, w_np = idx.numpy(), w.numpy()
+    t = {}
+    t0 = time.perf_counter()
+    rr = O.route(idx_np, wl.E, wl.R)
+    t["route"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    recv = O.scatter(x, rr.src_map, wl.E, wl.R).reshape(wl.E * wl.R, wl.H)
+    t["scatter"] = time.perf_counter() - t0
+    rows = rr.src_map[rr.src_map >= 0]
+    t0 = time.perf_counter()
+    O.quantize_rows(recv[np.sort(rows)])
+    t["quant"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    O.combine_f32_sequential(recv, rr.src_map, w_np)   # reads only the kept (written) rows
+    t["combine"] = time.perf_counter() - t0
+    n = int(rr.counts.sum())
+    total = sum(t.values())
+    return {"rows": n, "seconds": {k: round(v, 4) for k, v in t.items()}, "rows_per_s": n / total,
+            "note": f"{wl.name}: T={wl.T} E={wl.E} top-{wl.K} H={wl.H}, every kept route"}
 
 
 # ------------------------------------------------------------------ GPU arm
+
+def measure_write_bandwidth(device, nbytes: int = 4 << 30) -> float:
+    """Write-only HBM bandwidth (GB/s): the best of 10 fills of a buffer much
+    larger than L2 (context for kernels that write far more than they read)."""
+    buf = torch.empty(nbytes // 2, dtype=torch.bfloat16, device=device)
+    for _ in range(3):
+        buf.fill_(1.0)
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        buf.fill_(0.5)
+        e.record()
+        e.synchronize()
+        best = min(best, s.elapsed_time(e))
+    del buf
+    torch.cuda.empty_cache()
+    return nbytes / (best * 1e-3) / 1e9
+
+
+def graph_ms(graphs, steps, stream, warmup, world, device, sampler=None, load_s=0.0):
+    """Times `steps` CUDA-graph replays (one per routing, cycled) with events
+    on the launching stream, barriers and a sync on both sides; returns the
+    slowest rank's elapsed ms.  With a clock sampler, `load_s` seconds of the
+    same replays run before and after the timed region inside its window."""
+    n = len(graphs)
+    for i in range(warmup):
+        graphs[i % n].replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def load():
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < load_s:
+            for i in range(n):
+                graphs[i].replay()
+            torch.cuda.synchronize()
+
+    def timed():
+        barrier(world)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(steps):
+            graphs[(warmup + i) % n].replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+
+    if sampler is None:
+        timed()
+    else:
+        with sampler:
+            load()
+            timed()
+            load()
+    return reduce_max(a.elapsed_time(b), world, device)
+
+
+def capture(fn, n):
+    """One CUDA graph per routing r of fn(r)."""
+    gs = []
+    for r in range(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(r)
+        gs.append(g)
+    return gs
+
 
 def run_ours(args, rank, local, world):
     from token_dispatch_grouped_topk_gb300 import _lib, api
     from token_dispatch_grouped_topk_gb300 import workloads as W
 
-    _lib.load()
+    lib = _lib.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = W.WORKLOADS[args.workload]
+    peaks = load_peaks()
+    fp8 = measure_fp8_peak(dev)
+    write_gbs = measure_write_bandwidth(dev)
     seed = 1000 * rank
     x = W.activations(wl.T, wl.H, seed + 2, dev)
     w13, s13, w2, s2 = W.expert_weights(wl.E, wl.H, wl.I, seed + 3, dev)
     routings = [W.router(wl.T, wl.E, wl.K, W.router_bias(wl, seed + r, dev), seed + r + 1, dev)
                 for r in range(N_ROUTINGS)]
     buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
-    E, R, H, I = wl.E, wl.R, wl.H, wl.I
+    E, R, H, I, K, T = wl.E, wl.R, wl.H, wl.I, wl.K, wl.T
     xq, xs, zq, zs = buf.workspace_views()
+    sync = buf.sync_view()
     stream = torch.cuda.current_stream()
+    n_gemm = int(lib.moe_expert_compute_gemm_launches(E, R, 0, I, 0))
+    form = "one" if n_gemm == 1 else "two"
+    rank_offsets = None
+    if wl.tokens_per_rank:
+        rank_offsets = torch.tensor(np.concatenate([[0], np.cumsum(wl.tokens_per_rank)]),
+                                    dtype=torch.int32, device=dev)
 
-    n_valid, n_active = [], []
+    # routing figures of each of the four routings (moe_layer_stats)
+    n_valid, n_active, stats = [], [], []
     for idx, w in routings:
         api.moe_dispatch(x, idx, w, E, R, recv=buf.recv, counts=buf.counts, src_map=buf.src_map,
                          dev_status=buf.dev_status, workspace=buf.ws_dispatch)
-        c = buf.counts.cpu()
-        n_valid.append(int(c.sum()))
-        n_active.append(int((c > 0).sum()))
-    dropped = int(buf.dev_status[1].item())
+        st = api.layer_stats_dict(api.moe_layer_stats(idx, buf.counts, wl.L, R, rank_offsets=rank_offsets),
+                                  E, R)
+        stats.append(st)
+        n_valid.append(st["kept_routes"])
+        n_active.append(st["active_experts"])
 
-    # One step = dispatch -> quantisation -> both GEMMs in one launch ->
-    # combine (the kernels moe_dispatch, moe_expert_compute and moe_combine
-    # run), each stage bracketed by events on the launching stream so every
-    # launch's duration is measured in place.
-    stage_names = ["dispatch", "quant", "gemm_gateup_down", "combine"]
-    n_stage = len(stage_names)
-    sync = buf.sync_view()
+    # One step = the layer as moe_dispatch, moe_expert_compute and moe_combine
+    # run it: dispatch -> quantisation -> the GEMMs in the library's launch
+    # form for this shape -> combine, with events between the launches (eager
+    # loop) for each kernel's time.
+    gemm_names = ["gemm_gateup_down"] if form == "one" else ["gemm_gateup", "gemm_down"]
+    stage_names = ["dispatch", "quant"] + gemm_names + ["combine"]
 
     def step(i, evs=None):
         idx, w = routings[i % N_ROUTINGS]
-        if evs: evs[0].record(stream)
+        rec = (lambda j: evs[j].record(stream)) if evs else (lambda j: None)
+        rec(0)
         api.moe_dispatch(x, idx, w, E, R, recv=buf.recv, counts=buf.counts, src_map=buf.src_map,
                          dev_status=buf.dev_status, workspace=buf.ws_dispatch)
-        if evs: evs[1].record(stream)
+        rec(1)
         api.moe_quantize_fp8(buf.recv, buf.counts, xq=xq, xs=xs)
-        if evs: evs[2].record(stream)
-        api.moe_gemm_gateup_down(xq, xs, buf.counts, w13, s13, w2, s2, zq=zq, zs=zs, out=buf.out,
-                                 sync=sync, dev_status=buf.dev_status)
-        if evs: evs[3].record(stream)
+        rec(2)
+        if form == "one":
+            api.moe_gemm_gateup_down(xq, xs, buf.counts, w13, s13, w2, s2, zq=zq, zs=zs, out=buf.out,
+                                     sync=sync, dev_status=buf.dev_status, gemm_launch="one")
+            k = 3
+        else:
+            api.moe_gemm_gateup_silu(xq, xs, buf.counts, w13, s13, zq=zq, zs=zs, dev_status=buf.dev_status)
+            rec(3)
+            api.moe_gemm_down(zq, zs, buf.counts, w2, s2, out=buf.out, dev_status=buf.dev_status)
+            k = 4
+        rec(k)
         api.moe_combine(buf.out, buf.src_map, w, y=buf.y)
-        if evs: evs[4].record(stream)
+        rec(k + 1)
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    # The headline timing replays one captured CUDA graph per routing (the
-    # layer's launches recorded once; the device work is identical).
-    graphs = []
-    for r in range(N_ROUTINGS):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            step(r)
-        graphs.append(g)
-    for i in range(args.warmup):
-        graphs[i % N_ROUTINGS].replay()
-    torch.cuda.synchronize()
-    gs, ge = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        gs.record(stream)
-        for i in range(args.steps):
-            graphs[(args.warmup + i) % N_ROUTINGS].replay()
-        ge.record(stream)
-        torch.cuda.synchronize()
-    barrier(world)
-    elapsed_ms = gs.elapsed_time(ge)
+    graphs = capture(step, N_ROUTINGS)
+    clk = ClockSampler(local)
+    elapsed_ms = graph_ms(graphs, args.steps, stream, args.warmup, world, dev, sampler=clk, load_s=0.6)
     del graphs
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_stage + 1)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
+           for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
-    start.record(stream)
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0e.record(stream)
     for i in range(args.steps):
         step(args.warmup + i, evs[i])
-    end.record(stream)
+    t1e.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    eager_ms = start.elapsed_time(end)
-
+    eager_ms = t0e.elapsed_time(t1e)
     status = buf.dev_status.cpu().tolist()
     if status[0] & api.DEV_TIMEOUT:
         raise RuntimeError("device timeout during the timed region")
     stage_ms = {n: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]))
                 for j, n in enumerate(stage_names)}
+    rows_steps = [n_valid[(args.warmup + i) % N_ROUTINGS] for i in range(args.steps)]
+    rows_local = float(sum(rows_steps))
+    rows_total = reduce_sum(rows_local, world, dev)
+    value = rows_total / (elapsed_ms / 1e3)
+    mean_rows = rows_total / args.steps / world
 
-    # ---- the two GEMMs as separate launches (moe_gemm_gateup_silu, then
-    # moe_gemm_down), for the rate of each GEMM on its own
-    def split_step(i, se):
+    # ---- both launch forms of the GEMMs, same routings, eager with events
+    def forms_step(i, fe):
         idx, w = routings[i % N_ROUTINGS]
         api.moe_dispatch(x, idx, w, E, R, recv=buf.recv, counts=buf.counts, src_map=buf.src_map,
                          dev_status=buf.dev_status, workspace=buf.ws_dispatch)
         api.moe_quantize_fp8(buf.recv, buf.counts, xq=xq, xs=xs)
-        se[0].record(stream)
+        fe[0].record(stream)
+        api.moe_gemm_gateup_down(xq, xs, buf.counts, w13, s13, w2, s2, zq=zq, zs=zs, out=buf.out,
+                                 sync=sync, dev_status=buf.dev_status, gemm_launch="one")
+        fe[1].record(stream)
         api.moe_gemm_gateup_silu(xq, xs, buf.counts, w13, s13, zq=zq, zs=zs, dev_status=buf.dev_status)
-        se[1].record(stream)
+        fe[2].record(stream)
         api.moe_gemm_down(zq, zs, buf.counts, w2, s2, out=buf.out, dev_status=buf.dev_status)
-        se[2].record(stream)
-        api.moe_combine(buf.out, buf.src_map, w, y=buf.y)
+        fe[3].record(stream)
 
-    split_steps = max(3, min(args.steps, 30))
-    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(split_steps)]
+    form_steps = max(3, min(args.steps, 20))
+    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(form_steps)]
     for i in range(args.warmup):
-        split_step(i, sevs[0])
+        forms_step(i, fevs[0])
     torch.cuda.synchronize()
-    for i in range(split_steps):
-        split_step(args.warmup + i, sevs[i])
+    for i in range(form_steps):
+        forms_step(args.warmup + i, fevs[i])
     torch.cuda.synchronize()
-    split_ms = {n: float(np.mean([sevs[i][j].elapsed_time(sevs[i][j + 1]) for i in range(split_steps)]))
-                for j, n in enumerate(["gemm_gateup", "gemm_down"])}
-    split_rows = float(np.mean([n_valid[(args.warmup + i) % N_ROUTINGS] for i in range(split_steps)]))
+    f_ms = {n: float(np.mean([fevs[i][j].elapsed_time(fevs[i][j + 1]) for i in range(form_steps)]))
+            for j, n in enumerate(["one_launch", "gate_up", "down"])}
+    f_rows = float(np.mean([n_valid[(args.warmup + i) % N_ROUTINGS] for i in range(form_steps)]))
 
-    # ---- the same layer with dispatch and quantisation fused (moe_dispatch_quant)
-    fused_names = ["dispatch_quant", "gemm_gateup_down", "combine"]
+    # ---- dispatch fused with quantisation (moe_dispatch_quant), graph replay
+    fused_names = ["dispatch_quant", "gemms", "combine"]
 
     def fused_step(i, fe=None):
         idx, w = routings[i % N_ROUTINGS]
@@ -409,72 +545,20 @@ def run_ours(args, rank, local, world):
     for i in range(args.warmup):
         fused_step(i)
     torch.cuda.synchronize()
-    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fused_names) + 1)]
-            for _ in range(args.steps)]
-    fs, fe_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
+    fgev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(form_steps)]
+    for i in range(form_steps):
+        fused_step(args.warmup + i, fgev[i])
     torch.cuda.synchronize()
-    fs.record(stream)
-    for i in range(args.steps):
-        fused_step(args.warmup + i, fevs[i])
-    fe_.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    fused_eager_ms = fs.elapsed_time(fe_)
-    fgraphs = []
-    for r in range(N_ROUTINGS):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            fused_step(r)
-        fgraphs.append(g)
-    for i in range(args.warmup):
-        fgraphs[i % N_ROUTINGS].replay()
-    torch.cuda.synchronize()
-    barrier(world)
-    fs.record(stream)
-    for i in range(args.steps):
-        fgraphs[(args.warmup + i) % N_ROUTINGS].replay()
-    fe_.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    fused_ms = reduce_max(fs.elapsed_time(fe_), world, dev)
-    del fgraphs
-    fused_stage_ms = {n: float(np.mean([fevs[i][j].elapsed_time(fevs[i][j + 1]) for i in range(args.steps)]))
+    fused_stage_ms = {n: float(np.mean([fgev[i][j].elapsed_time(fgev[i][j + 1]) for i in range(form_steps)]))
                       for j, n in enumerate(fused_names)}
-    rows_steps = [n_valid[(args.warmup + i) % N_ROUTINGS] for i in range(args.steps)]
-    rows_local = float(sum(rows_steps))
-    max_ms = reduce_max(elapsed_ms, world, dev)
-    rows_total = reduce_sum(rows_local, world, dev)
-    value = rows_total / (max_ms / 1e3)
+    fgraphs = capture(fused_step, N_ROUTINGS)
+    fused_ms = graph_ms(fgraphs, args.steps, stream, args.warmup, world, dev)
+    del fgraphs
 
-    # ---- packed layout (moe_*_packed): the same step with the experts' rows
-    # back to back instead of one capacity block per expert
-    pbuf = api.MoeLayerBuffers(wl.T, E, wl.K, H, I, R, dev, packed=True)
-
-    def packed_step(i):
-        idx, w = routings[i % N_ROUTINGS]
-        pbuf.forward(x, idx, w, w13, s13, w2, s2)
-
-    for i in range(args.warmup):
-        packed_step(i)
-    torch.cuda.synchronize()
-    pgraphs = []
-    for r in range(N_ROUTINGS):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            packed_step(r)
-        pgraphs.append(g)
-    for i in range(args.warmup):
-        pgraphs[i % N_ROUTINGS].replay()
-    torch.cuda.synchronize()
-    barrier(world)
-    fs.record(stream)
-    for i in range(args.steps):
-        pgraphs[(args.warmup + i) % N_ROUTINGS].replay()
-    fe_.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    packed_ms = reduce_max(fs.elapsed_time(fe_), world, dev)
+    # ---- packed layout (moe_*_packed), graph replay
+    pbuf = api.MoeLayerBuffers(T, E, K, H, I, R, dev, packed=True)
+    pgraphs = capture(lambda r: pbuf.forward(x, *routings[r], w13, s13, w2, s2), N_ROUTINGS)
+    packed_ms = graph_ms(pgraphs, args.steps, stream, args.warmup, world, dev)
 
     def lane_bytes(b):
         return int(sum(t.numel() * t.element_size()
@@ -487,45 +571,68 @@ def run_ours(args, rank, local, world):
     del pgraphs, pbuf
     torch.cuda.empty_cache()
 
-    # ---- two micro-batches: serial split and overlapped on two streams
-    tbo = api.TwoBatchOverlap(wl.T, E, wl.K, H, I, R, dev)
+    # ---- per-source fixed slots (moe_*_source_slots), the decode-path layout:
+    # max_tokens = the largest source rank's token count; skipped when its
+    # receive buffer would exceed 16 GB
+    mt = max(wl.tokens_per_rank) if wl.tokens_per_rank else -(-T // wl.W)
+    ss_bytes = E * wl.W * mt * H * 2
+    if ss_bytes <= (16 << 30):
+        sbuf = api.MoeLayerBuffers(T, E, K, H, I, wl.W * mt, dev, source_slots=mt, L=wl.L,
+                                   rank_offsets=rank_offsets)
+        sgraphs = capture(lambda r: sbuf.forward(x, *routings[r], w13, s13, w2, s2), N_ROUTINGS)
+        ss_ms = graph_ms(sgraphs, args.steps, stream, args.warmup, world, dev)
+        ss_rows = []
+        for r in range(N_ROUTINGS):
+            sbuf.forward(x, *routings[r], w13, s13, w2, s2)
+            ss_rows.append(int(sbuf.counts.sum().item()))
+        ss_total = reduce_sum(float(sum(ss_rows[(args.warmup + i) % N_ROUTINGS] for i in range(args.steps))),
+                              world, dev)
+        source_slots = {"value": ss_total / (ss_ms / 1e3), "unit": UNIT, "ms_per_step": ss_ms / args.steps,
+                        "max_tokens": mt, "rows_per_expert": wl.W * mt, "lane_bytes": lane_bytes(sbuf),
+                        "note": "moe_dispatch_source_slots / moe_expert_compute_source_slots / moe_combine: "
+                                "each source rank owns max_tokens slots in every expert (CUDA-graph replay)"}
+        del sgraphs, sbuf
+        torch.cuda.empty_cache()
+    else:
+        source_slots = {"skipped": f"receive buffer would be {ss_bytes / 1e9:.0f} GB (W*max_tokens = "
+                                   f"{wl.W * mt} rows per expert); the layout is the decode path's"}
+
+    # ---- two micro-batches: serial split, and overlapped on two streams with
+    # the GEMMs' grid capped at several SM counts (the rest left to the other
+    # stream's dispatch and combine)
     tbo_steps = max(3, min(args.steps, 20))
 
-    def tbo_ms(overlap):
-        # one CUDA graph per routing holds the whole split step (both lanes and,
-        # when overlapped, both side streams forked from the capturing stream)
+    def tbo_ms(overlap, ctas):
+        tbo = api.TwoBatchOverlap(T, E, K, H, I, R, dev, gemm_ctas=ctas)
         for i in range(args.warmup):
-            idx, w = routings[i % N_ROUTINGS]
-            tbo.forward(x, idx, w, w13, s13, w2, s2, overlap=overlap)
+            tbo.forward(x, *routings[i % N_ROUTINGS], w13, s13, w2, s2, overlap=overlap)
         torch.cuda.synchronize()
-        tgraphs = []
-        for r in range(N_ROUTINGS):
-            idx, w = routings[r]
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                tbo.forward(x, idx, w, w13, s13, w2, s2, overlap=overlap)
-            tgraphs.append(g)
-        for i in range(args.warmup):
-            tgraphs[i % N_ROUTINGS].replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for i in range(tbo_steps):
-            tgraphs[(args.warmup + i) % N_ROUTINGS].replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        del tgraphs
-        return a.elapsed_time(b) / tbo_steps
+        tg = capture(lambda r: tbo.forward(x, *routings[r], w13, s13, w2, s2, overlap=overlap), N_ROUTINGS)
+        ms = graph_ms(tg, tbo_steps, stream, args.warmup, world, dev) / tbo_steps
+        del tg, tbo
+        torch.cuda.empty_cache()
+        return ms
 
-    split_serial_ms = tbo_ms(False)
-    split_overlap_ms = tbo_ms(True)
-    del tbo
-    torch.cuda.empty_cache()
+    sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    tbo_modes = {"no_split": elapsed_ms / args.steps, "serial_split": tbo_ms(False, 0)}
+    caps = {}
+    for ctas in (0, sm - 8, sm - 24, sm - 40):
+        caps[str(ctas or sm)] = tbo_ms(True, ctas)
+    tbo_modes["overlapped_split"] = caps[str(sm)]
+    best_cap = min(caps, key=caps.get)
+    tbo_res = {
+        "modes_ms_per_step": tbo_modes,
+        "overlapped_by_gemm_ctas_ms": caps, "best_gemm_ctas": int(best_cap),
+        "rows_per_s": {k: mean_rows / (v / 1e3) for k, v in tbo_modes.items()},
+        "note": "two token halves, one buffer lane each; overlapped = B's dispatch beside A's expert "
+                "compute and B's expert compute beside A's combine on two streams; the GEMMs' grid "
+                "capped at each listed SM count; every mode timed as CUDA-graph replays",
+    }
 
     # ---- end to end through the public API with host buffers
     x_h = x.cpu().pin_memory()
     r_h = [(i.cpu().pin_memory(), w.cpu().pin_memory()) for i, w in routings]
-    y_h = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+    y_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
     x_d = torch.empty_like(x)
     idx_d = torch.empty_like(routings[0][0])
     w_d = torch.empty_like(routings[0][1])
@@ -569,101 +676,93 @@ def run_ours(args, rank, local, world):
     del pipe
     e2e_rows = reduce_sum(float(sum(n_valid[(args.warmup + i) % N_ROUTINGS] for i in range(e2e_steps))), world, dev)
     h2d = x.numel() * 2 + routings[0][0].numel() * 8 + routings[0][1].numel() * 4
-    d2h = wl.T * wl.H * 2
+    d2h = T * H * 2
 
-    # ---- roofline of the dominant kernel (the two-GEMM launch) and per-kernel rates
-    peaks = load_peaks()
+    # ---- rates and the roofline of the dominant kernel
     nv = float(np.mean(rows_steps))
     na = int(round(np.mean([n_active[(args.warmup + i) % N_ROUTINGS] for i in range(args.steps)])))
-
     acct = layer_bytes_flops(wl, int(nv), na)
-    fp8_peak = 2.0 * peaks["bf16_tflops"]        # nominal fp8 : bf16 dense ratio 4.5 / 2.25
+    fp8_peak = max(fp8["fp8_tflops"], fp8["fp8_tflops_sustained"])
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
     tfs = lambda f, ms: f / (ms * 1e-3) / 1e12
-    gemm_flops = acct["gemm_gateup_flops"] + acct["gemm_down_flops"]
-    gemm_bytes = acct["gemm_gateup_bytes"] + acct["gemm_down_bytes"]
-    g12 = tfs(gemm_flops, stage_ms["gemm_gateup_down"])
-    # the separate-launch GEMM rates, on the rows of the steps they ran
-    sacct = layer_bytes_flops(wl, int(split_rows), na)
-    g1 = tfs(sacct["gemm_gateup_flops"], split_ms["gemm_gateup"])
-    g2 = tfs(sacct["gemm_down_flops"], split_ms["gemm_down"])
-    kernels = {
-        "dispatch": {"ms": stage_ms["dispatch"], "GB/s": gbs(acct["dispatch_bytes"], stage_ms["dispatch"]),
-                     "frac_hbm": gbs(acct["dispatch_bytes"], stage_ms["dispatch"]) / peaks["hbm_gbs"]},
-        "quant": {"ms": stage_ms["quant"], "GB/s": gbs(acct["quant_bytes"], stage_ms["quant"]),
-                  "frac_hbm": gbs(acct["quant_bytes"], stage_ms["quant"]) / peaks["hbm_gbs"]},
-        "gemm_gateup_down": {"ms": stage_ms["gemm_gateup_down"], "TFLOP/s": g12, "frac_fp8": g12 / fp8_peak,
-                             "GB/s": gbs(gemm_bytes, stage_ms["gemm_gateup_down"]),
-                             "note": "both GEMMs in one launch (moe_gemm_gateup_down)"},
-        "combine": {"ms": stage_ms["combine"], "GB/s": gbs(acct["combine_bytes"], stage_ms["combine"]),
-                    "frac_hbm": gbs(acct["combine_bytes"], stage_ms["combine"]) / peaks["hbm_gbs"]},
-        "separate_launches": {
-            "gemm_gateup": {"ms": split_ms["gemm_gateup"], "TFLOP/s": g1, "frac_fp8": g1 / fp8_peak,
-                            "GB/s": gbs(sacct["gemm_gateup_bytes"], split_ms["gemm_gateup"])},
-            "gemm_down": {"ms": split_ms["gemm_down"], "TFLOP/s": g2, "frac_fp8": g2 / fp8_peak,
-                          "GB/s": gbs(sacct["gemm_down_bytes"], split_ms["gemm_down"])},
-            "steps": split_steps,
-            "note": "moe_gemm_gateup_silu then moe_gemm_down (eager, events around each)"},
+    flops = {"gemm_gateup": acct["gemm_gateup_flops"], "gemm_down": acct["gemm_down_flops"],
+             "gemm_gateup_down": acct["gemm_gateup_flops"] + acct["gemm_down_flops"]}
+    gbytes = {"gemm_gateup": acct["gemm_gateup_bytes"], "gemm_down": acct["gemm_down_bytes"],
+              "gemm_gateup_down": acct["gemm_gateup_bytes"] + acct["gemm_down_bytes"]}
+    kernels = {}
+    for n in ("dispatch", "quant", "combine"):
+        b = acct[f"{n}_bytes"]
+        kernels[n] = {"ms": stage_ms[n], "GB/s": gbs(b, stage_ms[n]), "frac_hbm": gbs(b, stage_ms[n]) / peaks["hbm_gbs"],
+                      "bytes": b}
+    for n in gemm_names:
+        kernels[n] = {"ms": stage_ms[n], "TFLOP/s": tfs(flops[n], stage_ms[n]),
+                      "frac_fp8": tfs(flops[n], stage_ms[n]) / fp8_peak,
+                      "GB/s": gbs(gbytes[n], stage_ms[n]), "frac_hbm": gbs(gbytes[n], stage_ms[n]) / peaks["hbm_gbs"]}
+    kernels["dispatch"]["frac_write_only_hbm"] = kernels["dispatch"]["GB/s"] / write_gbs
+    f_acct = layer_bytes_flops(wl, int(f_rows), na)
+    f_fl = f_acct["gemm_gateup_flops"] + f_acct["gemm_down_flops"]
+    gemm_forms = {
+        "one_launch_ms": f_ms["one_launch"], "two_launches_ms": f_ms["gate_up"] + f_ms["down"],
+        "one_launch_TFLOP/s": tfs(f_fl, f_ms["one_launch"]),
+        "two_launches_TFLOP/s": tfs(f_fl, f_ms["gate_up"] + f_ms["down"]),
+        "gate_up_TFLOP/s": tfs(f_acct["gemm_gateup_flops"], f_ms["gate_up"]),
+        "down_TFLOP/s": tfs(f_acct["gemm_down_flops"], f_ms["down"]),
+        "chosen": form, "steps": form_steps,
+        "note": "both GEMMs in one launch (moe_gemm_gateup_down, tile events) against the gate/up "
+                "launch then the down launch, on the same routings; moe_expert_compute picks by "
+                "tile count (one launch when the gate/up tiles fill at most 16 waves of SMs)",
     }
-    mean_rows = rows_total / args.steps / world
-    tbo_res = {
-        "modes_ms_per_step": {"no_split": max_ms / args.steps, "serial_split": split_serial_ms,
-                              "overlapped_split": split_overlap_ms},
-        "rows_per_s": {"no_split": value, "serial_split": mean_rows / (split_serial_ms / 1e3),
-                       "overlapped_split": mean_rows / (split_overlap_ms / 1e3)},
-        "note": "two token halves, one buffer lane each; overlapped = B's dispatch beside A's expert "
-                "compute and B's expert compute beside A's combine on two streams; every mode "
-                "timed as CUDA-graph replays",
-    }
+    dom = max(gemm_names + ["dispatch", "quant", "combine"], key=lambda n: stage_ms[n])
+    if dom in flops:
+        t_tensor = flops[dom] / (fp8_peak * 1e12)
+        t_hbm = gbytes[dom] / (peaks["hbm_gbs"] * 1e9)
+        if t_tensor >= t_hbm:
+            ach = kernels[dom]["TFLOP/s"]
+            roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
+                    "frac": ach / fp8_peak,
+                    "peak_note": (f"of measured: dense e4m3 cuBLASLt GEMM on this GPU, the larger of burst "
+                                  f"{fp8['fp8_tflops']:.0f} and sustained {fp8['fp8_tflops_sustained']:.0f} "
+                                  f"TFLOP/s; 2 x the measured bf16 burst would be {2 * peaks['bf16_tflops']:.0f}")}
+        else:
+            ach = kernels[dom]["GB/s"]
+            roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / peaks["hbm_gbs"],
+                    "peak_note": (f"of {peaks['source']} HBM copy bandwidth; tensor frac "
+                                  f"{kernels[dom]['frac_fp8']:.3f} of the measured fp8 peak {fp8_peak:.0f}")}
+        roof["roofline_ms"] = {"tensor": t_tensor * 1e3, "hbm": t_hbm * 1e3}
+        roof["algorithmic"] = {"flops_per_launch": flops[dom], "bytes_per_launch": gbytes[dom]}
+    else:
+        ach = kernels[dom]["GB/s"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "peak_note": f"of {peaks['source']} HBM copy bandwidth",
+                "algorithmic": {"bytes_per_launch": acct[f"{dom}_bytes"]}}
+    roof["traffic"] = recorded_traffic(dom, wl.name)
     fused = {
         "value": rows_total / (fused_ms / 1e3), "unit": UNIT, "ms_per_step": fused_ms / args.steps,
         "note": "moe_dispatch_quant (each token row quantised once, FP8 scattered) replaces dispatch + quant",
-        "kernels": {
-            "dispatch_quant": {"ms": fused_stage_ms["dispatch_quant"],
-                               "GB/s": gbs(acct["dispatch_quant_bytes"], fused_stage_ms["dispatch_quant"]),
-                               "frac_hbm": gbs(acct["dispatch_quant_bytes"], fused_stage_ms["dispatch_quant"]) / peaks["hbm_gbs"]},
-            "gemm_gateup_down": {"ms": fused_stage_ms["gemm_gateup_down"]},
-            "combine": {"ms": fused_stage_ms["combine"]},
-        },
-        "gpu_launches": 5 * args.steps,
+        "kernels": {"dispatch_quant": {"ms": fused_stage_ms["dispatch_quant"],
+                                       "GB/s": gbs(acct["dispatch_quant_bytes"], fused_stage_ms["dispatch_quant"]),
+                                       "frac_hbm": gbs(acct["dispatch_quant_bytes"],
+                                                       fused_stage_ms["dispatch_quant"]) / peaks["hbm_gbs"]},
+                    "gemms": {"ms": fused_stage_ms["gemms"]}, "combine": {"ms": fused_stage_ms["combine"]}},
     }
-    dom = max(stage_ms, key=stage_ms.get)
-    if dom == "gemm_gateup_down":
-        # The GEMM launch's bound is whichever roofline time is longer: its
-        # FLOPs at the FP8 peak or its bytes at the HBM peak (decode-shaped
-        # layers stream the weights for few rows and sit below the ridge).
-        t_tensor = gemm_flops / (fp8_peak * 1e12)
-        t_hbm = gemm_bytes / (peaks["hbm_gbs"] * 1e9)
-        if t_tensor >= t_hbm:
-            achieved = kernels[dom]["TFLOP/s"]
-            roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": fp8_peak,
-                    "unit": "TFLOP/s", "frac": achieved / fp8_peak,
-                    "peak_note": f"fp8 dense = 2 x bf16 burst of {peaks['source']} peaks"}
-        else:
-            achieved = kernels[dom]["GB/s"]
-            roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "peak_note": f"{peaks['source']} HBM copy bandwidth; tensor frac "
-                                 f"{kernels[dom]['frac_fp8']:.3f} of the fp8 dense peak"}
-        roof["roofline_ms"] = {"tensor": t_tensor * 1e3, "hbm": t_hbm * 1e3}
-        roof["traffic"] = recorded_traffic(dom, wl.name)
-    else:
-        achieved = kernels[dom]["GB/s"]
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "peak_note": f"{peaks['source']} HBM copy bandwidth",
-                "traffic": recorded_traffic(dom, wl.name)}
+    dispatch_kernels = 1 if T * K <= 4096 else 3
+    launches_per_step = dispatch_kernels + 1 + n_gemm + 1
     return {
-        "value": value, "ms_per_step": max_ms / args.steps, "eager_ms_per_step": eager_ms / args.steps,
-        "kernels": kernels, "roofline": roof,
+        "value": value, "ms_per_step": elapsed_ms / args.steps, "eager_ms_per_step": eager_ms / args.steps,
+        "kernels": kernels, "gemm_forms": gemm_forms, "roofline": roof,
+        "peaks": {"fp8": fp8, "hbm_copy_gbs": peaks["hbm_gbs"], "hbm_write_only_gbs": write_gbs,
+                  "bf16_tflops": peaks["bf16_tflops"], "source": peaks["source"]},
         "e2e": {"value": e2e_rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
                 "path": "api.HostPipeline: pinned host in/out every step; step i+1's copy-in and "
                         "step i-1's copy-out run on two copy streams beside step i's compute",
                 "serial_value": e2e_rows / (e2e_serial_ms / 1e3),
                 "serial_note": "copy in, compute, copy out back to back on one stream"},
-        "gpu_launches": 6 * args.steps, "clocks": clk.summary(), "fused": fused, "tbo": tbo_res,
-        "packed": packed,
-        "rows_per_step": nv, "dropped_routes_last_routing": dropped, "wl": wl,
+        "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
+        "clocks": clk.summary(), "fused": fused, "tbo": tbo_res, "packed": packed,
+        "source_slots": source_slots, "layer_stats": stats,
+        "rows_per_step": nv, "wl": wl,
     }
 
 
@@ -683,6 +782,23 @@ def workload_config(wl, extra=None) -> dict:
     return cfg
 
 
+def cpu_baseline(wl) -> dict:
+    """The oracle as it stands on this host: the bounded expert sample with
+    all threads and with one, plus the routing/scatter/quant/combine passes in
+    full on the decode- and prefill-shaped layers."""
+    from token_dispatch_grouped_topk_gb300 import workloads as W
+    host = host_description()
+    allt = cpu_oracle_sample(wl, n_experts=8, rows_per_expert=128)
+    one = cpu_oracle_sample_single_thread(wl, n_experts=8, rows_per_expert=128)
+    small = {n: cpu_small_kernels_full(W.WORKLOADS[n]) for n in ("decode", "prefill")}
+    return {"value": allt["value"], "unit": UNIT, "cores": host["nproc"], "threads": host["nproc"],
+            "cpu_model": host["cpu_model"], "kind": "oracle", "sample": allt["sample"],
+            "single_thread": None if one is None else {"value": one["value"], "unit": UNIT, "threads": 1},
+            "routing_scatter_quant_combine_full": small,
+            "note": "numpy's BLAS pool takes every core (threads); the single-thread figure runs the "
+                    "same sample in a child process with the BLAS/OpenMP pools at one thread"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -690,10 +806,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large", choices=["large", "prefill", "decode", "traced"])
+    # internal: one oracle sample as a JSON line (the single-thread baseline's child process)
+    ap.add_argument("--cpu-sample", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-experts", type=int, default=8, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-rows", type=int, default=128, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    from token_dispatch_grouped_topk_gb300 import workloads as W
+    if args.cpu_sample:
+        print(json.dumps(cpu_oracle_sample(W.WORKLOADS[args.cpu_sample], args.cpu_experts, args.cpu_rows)))
+        return
     if args.warmup < 3:
         args.warmup = 3
-    from token_dispatch_grouped_topk_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
 
     rank, local, world = dist_setup(args.gpus)
@@ -715,16 +838,15 @@ def main():
                                            "rows_per_step": res["rows_per_step"],
                                            "timing": "CUDA-graph replay of each step (per-kernel "
                                                      "times from an eager loop with events)",
-                                           "eager_ms_per_step": res["eager_ms_per_step"]}),
-            "kernels": res["kernels"], "roofline": res["roofline"], "e2e": res["e2e"],
-            "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
-            "fused_dispatch_quant": res["fused"],
-            "packed_layout": res["packed"],
-            "two_batch_overlap": res["tbo"],
+                                           "eager_ms_per_step": res["eager_ms_per_step"],
+                                           "launches_per_step": res["launches_per_step"]}),
+            "kernels": res["kernels"], "gemm_forms": res["gemm_forms"], "roofline": res["roofline"],
+            "peaks": res["peaks"], "e2e": res["e2e"], "gpu_launches": res["gpu_launches"],
+            "clocks": res["clocks"], "layer_stats": res["layer_stats"],
+            "fused_dispatch_quant": res["fused"], "packed_layout": res["packed"],
+            "source_slots_layout": res["source_slots"], "two_batch_overlap": res["tbo"],
         }
-        sample = cpu_oracle_sample(wl, n_experts=8, rows_per_expert=128)
-        line["cpu_baseline"] = {"value": sample["value"], "unit": UNIT, "cores": sample["cores"],
-                                "kind": "oracle", "sample": sample["sample"]}
+        line["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -739,13 +861,14 @@ def run_reference(args, wl, world):
             vals.append(s)
     secs = sum(v["seconds"] for v in vals)
     value = float(np.mean([v["value"] for v in vals]))
+    host = host_description()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / len(vals),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "config": workload_config(wl),
-        "cpu_baseline": {"kind": "oracle", "cores": vals[0]["cores"], "sample": vals[0]["sample"], "value": value,
-                         "unit": UNIT},
+        "cpu_baseline": {"kind": "oracle", "cores": host["nproc"], "cpu_model": host["cpu_model"],
+                         "sample": vals[0]["sample"], "value": value, "unit": UNIT},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
