@@ -208,6 +208,29 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   const int v0 = blockIdx.y * vec_per_slice;
   const int v1 = min(nvec, v0 + vec_per_slice);
   const int* wdest = s_dest + warp * 32;
+  if (v1 - v0 <= 32 && tpw <= 8) {
+    // Short slices (few tokens, many column slices, as at decode): one vector
+    // per lane per token, so the loads of all the warp's tokens are issued
+    // before the first store -- one memory round trip instead of one per token.
+    const int v = v0 + lane;
+    uint4 a[8];
+#pragma unroll
+    for (int tt = 0; tt < 8; ++tt) {
+      const int t = gw * tpw + tt;
+      if (tt < tpw && t < T && v < v1) a[tt] = ld_stream(x + static_cast<size_t>(t) * nvec + v);
+    }
+#pragma unroll
+    for (int tt = 0; tt < 8; ++tt) {
+      const int t = gw * tpw + tt;
+      if (tt >= tpw || t >= T || v >= v1) continue;
+      const int* dq = wdest + tt * K;
+      for (int k = 0; k < K; ++k) {
+        const int qq = dq[k];
+        if (qq >= 0) recv[static_cast<size_t>(qq) * nvec + v] = a[tt];
+      }
+    }
+    return;
+  }
   for (int tt = 0; tt < tpw; ++tt) {
     const int t = gw * tpw + tt;
     if (t >= T) break;
