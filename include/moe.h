@@ -463,6 +463,68 @@ int moe_expert_compute_workspace_layout(int E, int R, int64_t rows, int H, int I
                                         size_t* offsets);
 
 /* ---------------------------------------------------------------------------
+ * Expert parallelism across ranks (one GPU each, W = E / L ranks, rank r holding
+ * experts [r*L, r*L + L)) -- "SGLang、NCCL 与 MoE EP": §2.3.2 (a token sends one
+ * payload to each distinct destination rank among its routes, with a header
+ * carrying its route list), §2.3.4 (the destination writes one expert input per
+ * route) and §3.2 (合对: every route's expert output goes back into that route's
+ * result slot at the source, which applies the router weight and sums).  The
+ * exchanges themselves are the caller's all-to-all (e.g. NCCL through
+ * torch.distributed); these calls are each rank's data path around them:
+ *
+ * source      moe_ep_pack           -> send_x, send_ids, send_counts per rank
+ *             (all-to-all of send_counts, then of send_x rows and send_ids rows)
+ * destination moe_dispatch_ex(recv_x, recv_ids as int32 ids, E = L, R) and
+ *             moe_expert_compute on the received rows; moe_ep_route_offsets on
+ *             recv_ids; moe_ep_return -> one returned row per route
+ *             (all-to-all of the returned rows and flags back)
+ * source      moe_ep_route_offsets on send_ids; moe_ep_result_map;
+ *             moe_combine_packed(returned rows, result_map, topk_w) -> y
+ * Rows reach a destination grouped by source rank in ascending token order, so
+ * with tokens numbered rank after rank the slots, capacity drops and y equal
+ * those of moe_dispatch / moe_expert_compute / moe_combine on all ranks' tokens
+ * on one GPU, bit for bit.
+ *
+ * moe_ep_pack
+ *   x, topk_idx, idx_bits, T, H, K as for moe_dispatch_ex (global expert ids)
+ *   send_x      device BF16 [T*min(K, W), H]: one row per (token, destination
+ *               rank), rows for rank d back to back (d ascending), tokens
+ *               ascending; send_counts device int32 [W]: rows for each rank
+ *   send_ids    device int32 [T*min(K, W), K]: row u's destination-local
+ *               expert id (global id % L) at each top-k position routed to
+ *               that rank, -1 at the others
+ *   route_msg, route_pos  device int32 [T, K]: the send row carrying route
+ *               (t, k) and its position among that row's routes (-1 if none)
+ *   dev_status  as for moe_dispatch (bad ids reported and ignored)
+ *   workspace   moe_ep_pack_workspace_size(T, K, E, L) bytes, 256-byte aligned
+ * moe_ep_route_offsets  offsets device int32 [S + 1]: offsets[j] = number of
+ *               entries >= 0 in rows [0, j) of ids [S, K]; offsets[S] = all;
+ *               workspace moe_ep_offsets_workspace_size(S) bytes
+ * moe_ep_return  for each row j of ids [S, K] (the received send_ids) and each
+ *               of its routes in k order: ret row offsets[j] + position = out
+ *               row src_map[j, k] (the local layer's output and source map), or
+ *               zeros with flag 0 if src_map is -1 (dropped for capacity).
+ *               ret device BF16 [offsets[S], H]; flag device int32 [offsets[S]]
+ * moe_ep_result_map  result_map device int32 [T, K]: for route (t, k) with
+ *               message u = route_msg and position p, offsets[u] + p (offsets of
+ *               the source's send_ids) if that returned row's flag is 1, else -1
+ * ------------------------------------------------------------------------- */
+size_t moe_ep_pack_workspace_size(int T, int K, int E, int L);
+moe_status moe_ep_pack(const void* x, const void* topk_idx, int idx_bits, int T, int H, int K,
+                       int E, int L, void* send_x, int32_t* send_ids, int32_t* send_counts,
+                       int32_t* route_msg, int32_t* route_pos, int32_t* dev_status,
+                       void* workspace, size_t workspace_bytes, moe_stream_t stream);
+size_t moe_ep_offsets_workspace_size(int64_t S);
+moe_status moe_ep_route_offsets(const int32_t* ids, int64_t S, int K, int32_t* offsets,
+                                void* workspace, size_t workspace_bytes, moe_stream_t stream);
+moe_status moe_ep_return(const void* out, int64_t out_rows, const int32_t* src_map,
+                         const int32_t* ids, const int32_t* offsets, int64_t S, int K, int H,
+                         void* ret, int32_t* flag, moe_stream_t stream);
+moe_status moe_ep_result_map(const int32_t* route_msg, const int32_t* route_pos,
+                             const int32_t* offsets, const int32_t* flag, int64_t n_ret, int T,
+                             int K, int32_t* result_map, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * moe_selftest_bounded_wait -- exercises the device-side failure path: the
  * kernels' two bounded waits run on things nothing completes, at the same
  * time (an mbarrier wait, and the acquire wait on a global completion counter

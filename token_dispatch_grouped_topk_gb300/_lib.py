@@ -69,6 +69,16 @@ SIGNATURES = {
     "moe_layer_stats": (c_int, [c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                 c_void_p, c_void_p, c_void_p]),
     "moe_expert_compute_gemm_launches": (c_int, [c_int, c_int, c_int64, c_int, c_int]),
+    "moe_ep_pack_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
+    "moe_ep_pack": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p,
+                            c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                            c_void_p]),
+    "moe_ep_offsets_workspace_size": (c_size_t, [c_int64]),
+    "moe_ep_route_offsets": (c_int, [c_void_p, c_int64, c_int, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_ep_return": (c_int, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int,
+                              c_void_p, c_void_p, c_void_p]),
+    "moe_ep_result_map": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_int, c_int,
+                                  c_void_p, c_void_p]),
     "moe_expert_compute_workspace_layout": (c_int, [c_int, c_int, c_int64, c_int, c_int, c_void_p]),
     "moe_gemm_gateup_down_sync_size": (c_size_t, [c_int, c_int, c_int64]),
     "moe_gemm_gateup_down": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int64, c_int,

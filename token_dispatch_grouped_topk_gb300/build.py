@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libmoe_gb300.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 SOURCES = ["moe_api.cu", "dispatch.cu", "quant.cu", "gemm.cu", "combine.cu", "dispatch_noalloc.cu",
-           "selftest.cu", "stats.cu"]
+           "selftest.cu", "stats.cu", "ep.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]

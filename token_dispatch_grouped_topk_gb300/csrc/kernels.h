@@ -112,6 +112,33 @@ cudaError_t launch_gemm_gateup_down(const uint8_t* xq, const float* xs, const in
 cudaError_t launch_combine(const void* out, const int32_t* src_map, const float* topk_w, int T,
                            int H, int K, int64_t rows, void* y, int sm_count, cudaStream_t s);
 
+// ----- expert parallelism across ranks (ep.cu)
+// Send plan of one source rank: send_x [T * min(K, W), H] one payload row per
+// (token, destination rank), packed by destination in ascending token order;
+// send_ids [same rows, K] the destination-local expert id of each top-k
+// position (-1 elsewhere); send_counts [W]; route_msg / route_pos [T, K] the
+// message of each route and its position among the message's routes.  dest,
+// msg [T, K] int32 and hist (dispatch workspace) are scratch.
+cudaError_t launch_ep_pack(const void* x, const void* topk_idx, int idx_bits, int T, int H, int K,
+                           int E, int L, void* send_x, int32_t* send_ids, int32_t* send_counts,
+                           int32_t* route_msg, int32_t* route_pos, int32_t* dev_status,
+                           int32_t* dest, int32_t* msg, int32_t* hist, int sm_count,
+                           cudaStream_t s);
+// offsets [S + 1]: exclusive prefix over rows of ids [S, K] of their valid
+// (>= 0) entries; scratch of ep_offsets_scratch_ints(S) ints.
+size_t ep_offsets_scratch_ints(int64_t S);
+cudaError_t launch_ep_offsets(const int32_t* ids, int64_t S, int K, int32_t* offsets,
+                              int32_t* scratch, cudaStream_t s);
+// One returned row per route of the received rows (expert output or zeros),
+// at offsets[j] + position; flag 1 where the layer kept the route.
+cudaError_t launch_ep_return(const void* out, int64_t out_rows, const int32_t* src_map,
+                             const int32_t* ids, const int32_t* offsets, int64_t S, int K, int H,
+                             void* ret, int32_t* flag, cudaStream_t s);
+// result_map [T, K]: the returned row of each route at the source, or -1.
+cudaError_t launch_ep_result(const int32_t* route_msg, const int32_t* route_pos,
+                             const int32_t* offsets, const int32_t* flag, int64_t n_ret, int T,
+                             int K, int32_t* result_map, cudaStream_t s);
+
 // ----- layer statistics of one routing (kLayerStats 64-bit counters):
 // [0] valid routes, [1] kept routes, [2] messages (sum over tokens of the
 // distinct destination ranks), [3] cross-rank routes, [4] 128-row blocks of

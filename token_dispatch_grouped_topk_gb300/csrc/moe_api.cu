@@ -520,6 +520,86 @@ moe_status moe_layer_stats(const void* topk_idx, int idx_bits, const int32_t* co
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_ep_pack_workspace_size(int T, int K, int E, int L) {
+  if (T < 0 || K < 1 || K > 32 || L < 1 || E < 1 || E % L != 0) return 0;
+  const size_t tk = align_up(static_cast<size_t>(T) * K * sizeof(int32_t) + 1, 256);
+  return 2 * tk + moe_dispatch_workspace_size(T, K, E / L);
+}
+
+moe_status moe_ep_pack(const void* x, const void* topk_idx, int idx_bits, int T, int H, int K,
+                       int E, int L, void* send_x, int32_t* send_ids, int32_t* send_counts,
+                       int32_t* route_msg, int32_t* route_pos, int32_t* dev_status,
+                       void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (T < 0 || !valid_hidden(H) || K < 1 || K > 32 || L < 1 || E < 1 || E > 1024 || E % L != 0 ||
+      K > E)
+    return MOE_ERR_INVALID_ARG;
+  if (idx_bits != 32 && idx_bits != 64) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * K > (int64_t{1} << 30)) return MOE_ERR_INVALID_ARG;
+  if (send_counts == nullptr || dev_status == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || topk_idx == nullptr || send_x == nullptr || send_ids == nullptr ||
+                route_msg == nullptr || route_pos == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(x) || !aligned16(send_x))) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_ep_pack_workspace_size(T, K, E, L);
+  if (workspace == nullptr || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  const size_t tk = align_up(static_cast<size_t>(T) * K * sizeof(int32_t) + 1, 256);
+  auto* ws = static_cast<uint8_t*>(workspace);
+  return from_cuda(launch_ep_pack(x, topk_idx, idx_bits, T, H, K, E, L, send_x, send_ids,
+                                  send_counts, route_msg, route_pos, dev_status,
+                                  reinterpret_cast<int32_t*>(ws), reinterpret_cast<int32_t*>(ws + tk),
+                                  reinterpret_cast<int32_t*>(ws + 2 * tk), dev->sm_count,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_ep_offsets_workspace_size(int64_t S) {
+  if (S < 0) return 0;
+  return align_up(ep_offsets_scratch_ints(S) * sizeof(int32_t), 256);
+}
+
+moe_status moe_ep_route_offsets(const int32_t* ids, int64_t S, int K, int32_t* offsets,
+                                void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (S < 0 || S > (int64_t{1} << 30) || K < 1 || K > 32) return MOE_ERR_INVALID_ARG;
+  if (offsets == nullptr || (S > 0 && ids == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < moe_ep_offsets_workspace_size(S))
+    return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_ep_offsets(ids, S, K, offsets, static_cast<int32_t*>(workspace),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_ep_return(const void* out, int64_t out_rows, const int32_t* src_map,
+                         const int32_t* ids, const int32_t* offsets, int64_t S, int K, int H,
+                         void* ret, int32_t* flag, moe_stream_t stream) {
+  if (S < 0 || S > (int64_t{1} << 30) || K < 1 || K > 32 || !valid_hidden(H) || out_rows < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (S > 0 && (out == nullptr || src_map == nullptr || ids == nullptr || offsets == nullptr ||
+                ret == nullptr || flag == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (S > 0 && (!aligned16(out) || !aligned16(ret))) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_ep_return(out, out_rows, src_map, ids, offsets, S, K, H, ret, flag,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_ep_result_map(const int32_t* route_msg, const int32_t* route_pos,
+                             const int32_t* offsets, const int32_t* flag, int64_t n_ret, int T,
+                             int K, int32_t* result_map, moe_stream_t stream) {
+  if (T < 0 || K < 1 || K > 32 || n_ret < 0) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (route_msg == nullptr || route_pos == nullptr || offsets == nullptr ||
+                result_map == nullptr || (n_ret > 0 && flag == nullptr)))
+    return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  return from_cuda(launch_ep_result(route_msg, route_pos, offsets, flag, n_ret, T, K, result_map,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_combine(const void* out, const int32_t* src_map, const float* topk_w, int T, int H,
                        int K, int E, int R, void* y, moe_stream_t stream) {
   if (T < 0 || !valid_hidden(H) || !valid_experts(E, R) || K < 1 || K > 32 || K > E)
