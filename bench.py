@@ -115,10 +115,22 @@ def measure_fp8_peak(device, n: int = 8192, sustained_s: float = 4.0) -> dict:
                    f"(burst) and {calls} calls back to back over {sustained_s:.0f} s (sustained)"}
 
 
-def kernel_sources_digest() -> str:
-    h = hashlib.sha256()
+# The source files each kernel family is compiled from: a recorded ncu figure
+# stays valid while these are unchanged.
+KERNEL_SOURCES = {
+    "gemm": ("gemm.cu", "common.cuh"),
+    "dispatch": ("dispatch.cu", "common.cuh"),
+    "quant": ("quant.cu", "common.cuh"),
+    "combine": ("combine.cu", "common.cuh"),
+}
+
+
+def kernel_sources_digest(kernel: str) -> str:
+    family = next((f for f in KERNEL_SOURCES if kernel.startswith(f)), None)
     csrc = os.path.join(ROOT, "token_dispatch_grouped_topk_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES[family] if family else sorted(os.listdir(csrc))
+    h = hashlib.sha256()
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -126,7 +138,7 @@ def kernel_sources_digest() -> str:
 
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the kernel's current sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -134,7 +146,7 @@ def recorded_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     item = rec.get(f"{kernel}@{workload}")
-    if not item or item.get("sources") != kernel_sources_digest():
+    if not item or item.get("sources") != kernel_sources_digest(kernel):
         return None
     return item.get("dram_bytes_per_launch")
 

@@ -208,25 +208,30 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   const int v0 = blockIdx.y * vec_per_slice;
   const int v1 = min(nvec, v0 + vec_per_slice);
   const int* wdest = s_dest + warp * 32;
-  if (v1 - v0 <= 32 && tpw <= 8) {
-    // Short slices (few tokens, many column slices, as at decode): one vector
-    // per lane per token, so the loads of all the warp's tokens are issued
-    // before the first store -- one memory round trip instead of one per token.
-    const int v = v0 + lane;
-    uint4 a[8];
+  // When the warp's tokens' slices fit in sixteen 16-byte vectors per lane
+  // (U per token; the slices are short when there are few tokens, as at
+  // decode and prefill), every load is issued before the first store: one
+  // memory round trip per warp instead of one per token (prefill -5 %).
+  const int U = (v1 - v0 + 31) / 32;
+  if (U * tpw <= 16) {
+    uint4 a[16];
 #pragma unroll
-    for (int tt = 0; tt < 8; ++tt) {
+    for (int i = 0; i < 16; ++i) {
+      const int tt = i / U, u = i - (i / U) * U;
       const int t = gw * tpw + tt;
-      if (tt < tpw && t < T && v < v1) a[tt] = ld_stream(x + static_cast<size_t>(t) * nvec + v);
+      const int v = v0 + lane + 32 * u;
+      if (tt < tpw && t < T && v < v1) a[i] = ld_stream(x + static_cast<size_t>(t) * nvec + v);
     }
 #pragma unroll
-    for (int tt = 0; tt < 8; ++tt) {
+    for (int i = 0; i < 16; ++i) {
+      const int tt = i / U, u = i - (i / U) * U;
       const int t = gw * tpw + tt;
+      const int v = v0 + lane + 32 * u;
       if (tt >= tpw || t >= T || v >= v1) continue;
       const int* dq = wdest + tt * K;
       for (int k = 0; k < K; ++k) {
         const int qq = dq[k];
-        if (qq >= 0) recv[static_cast<size_t>(qq) * nvec + v] = a[tt];
+        if (qq >= 0) recv[static_cast<size_t>(qq) * nvec + v] = a[i];
       }
     }
     return;
