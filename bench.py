@@ -431,59 +431,78 @@ def run_ours(args, rank, local, world):
         n_valid.append(st["kept_routes"])
         n_active.append(st["active_experts"])
 
-    # One step = the layer as moe_dispatch, moe_expert_compute and moe_combine
-    # run it: dispatch -> quantisation -> the GEMMs in the library's launch
-    # form for this shape -> combine, with events between the launches (eager
-    # loop) for each kernel's time.
+    # One step = the layer as MoeLayerBuffers.forward runs it: dispatch fused
+    # with the quantisation (moe_dispatch_quant_ex) -> the GEMMs in the
+    # library's launch form for this shape -> combine, with events between
+    # the launches (eager loop) for each kernel's time.  The separate path
+    # (BF16 dispatch, then quantisation) is timed below as a variant.
     gemm_names = ["gemm_gateup_down"] if form == "one" else ["gemm_gateup", "gemm_down"]
-    stage_names = ["dispatch", "quant"] + gemm_names + ["combine"]
 
-    def step(i, evs=None):
-        idx, w = routings[i % N_ROUTINGS]
-        rec = (lambda j: evs[j].record(stream)) if evs else (lambda j: None)
-        rec(0)
-        api.moe_dispatch(x, idx, w, E, R, recv=buf.recv, counts=buf.counts, src_map=buf.src_map,
+    def layer_step(first, stage_names):
+        def step(i, evs=None):
+            idx, w = routings[i % N_ROUTINGS]
+            rec = (lambda j: evs[j].record(stream)) if evs else (lambda j: None)
+            rec(0)
+            k = first(x, idx, w, rec)
+            if form == "one":
+                api.moe_gemm_gateup_down(xq, xs, buf.counts, w13, s13, w2, s2, zq=zq, zs=zs, out=buf.out,
+                                         sync=sync, dev_status=buf.dev_status, gemm_launch="one")
+            else:
+                api.moe_gemm_gateup_silu(xq, xs, buf.counts, w13, s13, zq=zq, zs=zs, dev_status=buf.dev_status)
+                k += 1
+                rec(k)
+                api.moe_gemm_down(zq, zs, buf.counts, w2, s2, out=buf.out, dev_status=buf.dev_status)
+            k += 1
+            rec(k)
+            api.moe_combine(buf.out, buf.src_map, w, y=buf.y)
+            rec(k + 1)
+        return step
+
+    def fused_first(x_, idx, w, rec):
+        api.moe_dispatch_quant(x_, idx, w, E, R, xq=xq, xs=xs, counts=buf.counts, src_map=buf.src_map,
+                               dev_status=buf.dev_status, workspace=buf.ws_dispatch)
+        rec(1)
+        return 1
+
+    def separate_first(x_, idx, w, rec):
+        api.moe_dispatch(x_, idx, w, E, R, recv=buf.recv, counts=buf.counts, src_map=buf.src_map,
                          dev_status=buf.dev_status, workspace=buf.ws_dispatch)
         rec(1)
         api.moe_quantize_fp8(buf.recv, buf.counts, xq=xq, xs=xs)
         rec(2)
-        if form == "one":
-            api.moe_gemm_gateup_down(xq, xs, buf.counts, w13, s13, w2, s2, zq=zq, zs=zs, out=buf.out,
-                                     sync=sync, dev_status=buf.dev_status, gemm_launch="one")
-            k = 3
-        else:
-            api.moe_gemm_gateup_silu(xq, xs, buf.counts, w13, s13, zq=zq, zs=zs, dev_status=buf.dev_status)
-            rec(3)
-            api.moe_gemm_down(zq, zs, buf.counts, w2, s2, out=buf.out, dev_status=buf.dev_status)
-            k = 4
-        rec(k)
-        api.moe_combine(buf.out, buf.src_map, w, y=buf.y)
-        rec(k + 1)
+        return 2
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    graphs = capture(step, N_ROUTINGS)
+    def time_layer(step, stage_names, sampler=None):
+        """Graph-replay ms for args.steps steps, eager ms, per-stage ms."""
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+        graphs = capture(step, N_ROUTINGS)
+        g_ms = graph_ms(graphs, args.steps, stream, args.warmup, world, dev, sampler=sampler,
+                        load_s=0.6 if sampler else 0.0)
+        del graphs
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
+               for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0e.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, evs[i])
+        t1e.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        if buf.dev_status.cpu().tolist()[0] & api.DEV_TIMEOUT:
+            raise RuntimeError("device timeout during the timed region")
+        st_ms = {n: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]))
+                 for j, n in enumerate(stage_names)}
+        return g_ms, t0e.elapsed_time(t1e), st_ms
+
+    stage_names = ["dispatch_quant"] + gemm_names + ["combine"]
     clk = ClockSampler(local)
-    elapsed_ms = graph_ms(graphs, args.steps, stream, args.warmup, world, dev, sampler=clk, load_s=0.6)
-    del graphs
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stage_names) + 1)]
-           for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0e.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i, evs[i])
-    t1e.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    eager_ms = t0e.elapsed_time(t1e)
-    status = buf.dev_status.cpu().tolist()
-    if status[0] & api.DEV_TIMEOUT:
-        raise RuntimeError("device timeout during the timed region")
-    stage_ms = {n: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]))
-                for j, n in enumerate(stage_names)}
+    elapsed_ms, eager_ms, stage_ms = time_layer(layer_step(fused_first, stage_names), stage_names, sampler=clk)
+    sep_names = ["dispatch", "quant"] + gemm_names + ["combine"]
+    sep_ms, _, sep_stage_ms = time_layer(layer_step(separate_first, sep_names), sep_names)
     rows_steps = [n_valid[(args.warmup + i) % N_ROUTINGS] for i in range(args.steps)]
     rows_local = float(sum(rows_steps))
     rows_total = reduce_sum(rows_local, world, dev)
@@ -493,9 +512,8 @@ def run_ours(args, rank, local, world):
     # ---- both launch forms of the GEMMs, same routings, eager with events
     def forms_step(i, fe):
         idx, w = routings[i % N_ROUTINGS]
-        api.moe_dispatch(x, idx, w, E, R, recv=buf.recv, counts=buf.counts, src_map=buf.src_map,
-                         dev_status=buf.dev_status, workspace=buf.ws_dispatch)
-        api.moe_quantize_fp8(buf.recv, buf.counts, xq=xq, xs=xs)
+        api.moe_dispatch_quant(x, idx, w, E, R, xq=xq, xs=xs, counts=buf.counts, src_map=buf.src_map,
+                               dev_status=buf.dev_status, workspace=buf.ws_dispatch)
         fe[0].record(stream)
         api.moe_gemm_gateup_down(xq, xs, buf.counts, w13, s13, w2, s2, zq=zq, zs=zs, out=buf.out,
                                  sync=sync, dev_status=buf.dev_status, gemm_launch="one")
@@ -517,35 +535,8 @@ def run_ours(args, rank, local, world):
             for j, n in enumerate(["one_launch", "gate_up", "down"])}
     f_rows = float(np.mean([n_valid[(args.warmup + i) % N_ROUTINGS] for i in range(form_steps)]))
 
-    # ---- dispatch fused with quantisation (moe_dispatch_quant), graph replay
-    fused_names = ["dispatch_quant", "gemms", "combine"]
-
-    def fused_step(i, fe=None):
-        idx, w = routings[i % N_ROUTINGS]
-        if fe: fe[0].record(stream)
-        api.moe_dispatch_quant(x, idx, w, E, R, xq=xq, xs=xs, counts=buf.counts, src_map=buf.src_map,
-                               dev_status=buf.dev_status, workspace=buf.ws_dispatch)
-        if fe: fe[1].record(stream)
-        api.moe_gemm_gateup_down(xq, xs, buf.counts, w13, s13, w2, s2, zq=zq, zs=zs, out=buf.out,
-                                 sync=sync, dev_status=buf.dev_status)
-        if fe: fe[2].record(stream)
-        api.moe_combine(buf.out, buf.src_map, w, y=buf.y)
-        if fe: fe[3].record(stream)
-
-    for i in range(args.warmup):
-        fused_step(i)
-    torch.cuda.synchronize()
-    fgev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(form_steps)]
-    for i in range(form_steps):
-        fused_step(args.warmup + i, fgev[i])
-    torch.cuda.synchronize()
-    fused_stage_ms = {n: float(np.mean([fgev[i][j].elapsed_time(fgev[i][j + 1]) for i in range(form_steps)]))
-                      for j, n in enumerate(fused_names)}
-    fgraphs = capture(fused_step, N_ROUTINGS)
-    fused_ms = graph_ms(fgraphs, args.steps, stream, args.warmup, world, dev)
-    del fgraphs
-
-    # ---- packed layout (moe_*_packed), graph replay
+    # ---- packed layout (moe_dispatch_quant_ex / moe_gemm_gateup_down / moe_combine_packed
+    # on [rows, ...] buffers), graph replay
     pbuf = api.MoeLayerBuffers(T, E, K, H, I, R, dev, packed=True)
     pgraphs = capture(lambda r: pbuf.forward(x, *routings[r], w13, s13, w2, s2), N_ROUTINGS)
     packed_ms = graph_ms(pgraphs, args.steps, stream, args.warmup, world, dev)
@@ -556,8 +547,10 @@ def run_ours(args, rank, local, world):
 
     packed = {"value": rows_total / (packed_ms / 1e3), "unit": UNIT, "ms_per_step": packed_ms / args.steps,
               "lane_bytes": lane_bytes(pbuf), "padded_lane_bytes": lane_bytes(buf),
-              "note": "moe_dispatch_packed / moe_expert_compute_packed / moe_combine_packed: the "
-                      "receive-side buffers hold min(T*K, E*R) rows instead of E*R (CUDA-graph replay)"}
+              "note": "MoeLayerBuffers(packed=True).forward (moe_dispatch_quant_ex, moe_gemm_gateup_down, "
+                      "moe_combine_packed on the packed layout): the receive-side buffers hold "
+                      "min(T*K, E*R) rows instead of E*R (CUDA-graph replay); lane bytes count every "
+                      "buffer of the lane, the unused BF16 receive buffer included"}
     del pgraphs, pbuf
     torch.cuda.empty_cache()
 
@@ -683,15 +676,20 @@ def run_ours(args, rank, local, world):
              "gemm_gateup_down": acct["gemm_gateup_flops"] + acct["gemm_down_flops"]}
     gbytes = {"gemm_gateup": acct["gemm_gateup_bytes"], "gemm_down": acct["gemm_down_bytes"],
               "gemm_gateup_down": acct["gemm_gateup_bytes"] + acct["gemm_down_bytes"]}
-    kernels = {}
-    for n in ("dispatch", "quant", "combine"):
-        b = acct[f"{n}_bytes"]
-        kernels[n] = {"ms": stage_ms[n], "GB/s": gbs(b, stage_ms[n]), "frac_hbm": gbs(b, stage_ms[n]) / peaks["hbm_gbs"],
-                      "bytes": b}
-    for n in gemm_names:
-        kernels[n] = {"ms": stage_ms[n], "TFLOP/s": tfs(flops[n], stage_ms[n]),
-                      "frac_fp8": tfs(flops[n], stage_ms[n]) / fp8_peak,
-                      "GB/s": gbs(gbytes[n], stage_ms[n]), "frac_hbm": gbs(gbytes[n], stage_ms[n]) / peaks["hbm_gbs"]}
+    def kernel_rates(st_ms):
+        ks = {}
+        for n in st_ms:
+            if n in flops:
+                ks[n] = {"ms": st_ms[n], "TFLOP/s": tfs(flops[n], st_ms[n]),
+                         "frac_fp8": tfs(flops[n], st_ms[n]) / fp8_peak,
+                         "GB/s": gbs(gbytes[n], st_ms[n]), "frac_hbm": gbs(gbytes[n], st_ms[n]) / peaks["hbm_gbs"]}
+            else:
+                b = acct[f"{n}_bytes"]
+                ks[n] = {"ms": st_ms[n], "GB/s": gbs(b, st_ms[n]),
+                         "frac_hbm": gbs(b, st_ms[n]) / peaks["hbm_gbs"], "bytes": b}
+        return ks
+
+    kernels = kernel_rates(stage_ms)
     f_acct = layer_bytes_flops(wl, int(f_rows), na)
     f_fl = f_acct["gemm_gateup_flops"] + f_acct["gemm_down_flops"]
     gemm_forms = {
@@ -705,7 +703,7 @@ def run_ours(args, rank, local, world):
                 "launch then the down launch, on the same routings; moe_expert_compute picks by "
                 "tile count (one launch when the gate/up tiles fill at most 16 waves of SMs)",
     }
-    dom = max(gemm_names + ["dispatch", "quant", "combine"], key=lambda n: stage_ms[n])
+    dom = max(stage_names, key=lambda n: stage_ms[n])
     if dom in flops:
         t_tensor = flops[dom] / (fp8_peak * 1e12)
         t_hbm = gbytes[dom] / (peaks["hbm_gbs"] * 1e9)
@@ -730,17 +728,15 @@ def run_ours(args, rank, local, world):
                 "frac": ach / peaks["hbm_gbs"], "peak_note": f"of {peaks['source']} HBM copy bandwidth",
                 "algorithmic": {"bytes_per_launch": acct[f"{dom}_bytes"]}}
     roof["traffic"] = recorded_traffic(dom, wl.name)
-    fused = {
-        "value": rows_total / (fused_ms / 1e3), "unit": UNIT, "ms_per_step": fused_ms / args.steps,
-        "note": "moe_dispatch_quant (each token row quantised once, FP8 scattered) replaces dispatch + quant",
-        "kernels": {"dispatch_quant": {"ms": fused_stage_ms["dispatch_quant"],
-                                       "GB/s": gbs(acct["dispatch_quant_bytes"], fused_stage_ms["dispatch_quant"]),
-                                       "frac_hbm": gbs(acct["dispatch_quant_bytes"],
-                                                       fused_stage_ms["dispatch_quant"]) / peaks["hbm_gbs"]},
-                    "gemms": {"ms": fused_stage_ms["gemms"]}, "combine": {"ms": fused_stage_ms["combine"]}},
+    separate = {
+        "value": rows_total / (sep_ms / 1e3), "unit": UNIT, "ms_per_step": sep_ms / args.steps,
+        "note": "MoeLayerBuffers.forward(fused=False): moe_dispatch (BF16 rows into the receive buffer), "
+                "then the quantisation kernel, the same GEMMs and combine (CUDA-graph replay; per-kernel "
+                "times from an eager loop)",
+        "kernels": kernel_rates(sep_stage_ms),
     }
     dispatch_kernels = 1 if T * K <= 4096 else 3
-    launches_per_step = dispatch_kernels + 1 + n_gemm + 1
+    launches_per_step = dispatch_kernels + n_gemm + 1
     return {
         "value": value, "ms_per_step": elapsed_ms / args.steps, "eager_ms_per_step": eager_ms / args.steps,
         "kernels": kernels, "gemm_forms": gemm_forms, "roofline": roof,
@@ -753,7 +749,7 @@ def run_ours(args, rank, local, world):
                 "serial_value": e2e_rows / (e2e_serial_ms / 1e3),
                 "serial_note": "copy in, compute, copy out back to back on one stream"},
         "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,
-        "clocks": clk.summary(), "fused": fused, "tbo": tbo_res, "packed": packed,
+        "clocks": clk.summary(), "separate": separate, "tbo": tbo_res, "packed": packed,
         "source_slots": source_slots, "layer_stats": stats,
         "rows_per_step": nv, "wl": wl,
     }
@@ -831,12 +827,14 @@ def main():
                                            "rows_per_step": res["rows_per_step"],
                                            "timing": "CUDA-graph replay of each step (per-kernel "
                                                      "times from an eager loop with events)",
+                                           "path": "MoeLayerBuffers.forward: moe_dispatch_quant_ex -> "
+                                                   "grouped GEMMs -> moe_combine",
                                            "eager_ms_per_step": res["eager_ms_per_step"],
                                            "launches_per_step": res["launches_per_step"]}),
             "kernels": res["kernels"], "gemm_forms": res["gemm_forms"], "roofline": res["roofline"],
             "peaks": res["peaks"], "e2e": res["e2e"], "gpu_launches": res["gpu_launches"],
             "clocks": res["clocks"], "layer_stats": res["layer_stats"],
-            "fused_dispatch_quant": res["fused"], "packed_layout": res["packed"],
+            "separate_dispatch_quant": res["separate"], "packed_layout": res["packed"],
             "source_slots_layout": res["source_slots"], "two_batch_overlap": res["tbo"],
         }
         line["cpu_baseline"] = cpu_baseline(wl)

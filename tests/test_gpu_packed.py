@@ -114,11 +114,12 @@ def test_layer_packed_bit_identical_to_padded(name):
     pad = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
     pk = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev, packed=True)
     args = (d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
-    y_pad = pad.forward(*args).clone()
-    y_pk = pk.forward(*args).clone()
-    torch.cuda.synchronize()
-    assert torch.equal(_bits(y_pk), _bits(y_pad))
-    assert pk.dev_status.cpu().tolist() == pad.dev_status.cpu().tolist()
+    y_pad = pad.forward(*args, fused=False).clone()
+    for fused in (False, True):
+        y_pk = pk.forward(*args, fused=fused).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(y_pk), _bits(y_pad)), f"fused={fused}"
+        assert pk.dev_status.cpu().tolist() == pad.dev_status.cpu().tolist()
     assert pk.recv.shape == (api.packed_rows(wl.T, wl.K, wl.E, wl.R), wl.H)
 
 
@@ -204,7 +205,7 @@ def _unit_scale_weights(E, H, I, seed):
 def test_interleaved_w13_bit_identical_to_standard(packed, shape):
     """Uniform block scales: interleaving W13's rows (2j gate, 2j+1 up) and
     flagging MOE_W13_INTERLEAVED gives the standard layer's bytes, through
-    moe_expert_compute and (padded) through the fused dispatch+quant path."""
+    moe_expert_compute and through the fused dispatch+quant path."""
     T, E, K, H, I, R = shape
     w13, s13, w2, s2 = _unit_scale_weights(E, H, I, seed=41)
     inter = torch.empty_like(w13)
@@ -217,16 +218,15 @@ def test_interleaved_w13_bit_identical_to_standard(packed, shape):
     std = api.MoeLayerBuffers(T, E, K, H, I, R, dev, packed=packed)
     itl = api.MoeLayerBuffers(T, E, K, H, I, R, dev, packed=packed, w13_interleaved=True)
     args = (x, idx, w)
-    y_std = std.forward(*args, w13.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV)).clone()
-    y_itl = itl.forward(*args, inter.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV)).clone()
+    y_std = std.forward(*args, w13.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV), fused=False).clone()
+    y_itl = itl.forward(*args, inter.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV), fused=False).clone()
     torch.cuda.synchronize()
     assert torch.equal(_bits(y_itl), _bits(y_std))
     assert float(y_std.float().abs().max()) > 0
-    if not packed:
-        # the fused dispatch+quant path hands the flag to moe_gemm_gateup_down
-        y_fused = itl.forward_fused(*args, inter.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV))
-        torch.cuda.synchronize()
-        assert torch.equal(_bits(y_fused), _bits(y_std))
+    # the fused dispatch+quant path hands the flag to moe_gemm_gateup_down
+    y_fused = itl.forward(*args, inter.to(DEV), s13.to(DEV), w2.to(DEV), s2.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y_fused), _bits(y_std))
 
 
 def test_interleaved_w13_matches_oracle():
@@ -290,7 +290,7 @@ def test_layer_fused_path_every_variant(name, packed, bits):
     ids = d["topk_idx"].to(torch.int32) if bits == 32 else d["topk_idx"]
     wts = (d["w13"], d["s13"], d["w2"], d["s2"])
     ref = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
-    y_ref = ref.forward(d["x"], d["topk_idx"], d["topk_w"], *wts).clone()
+    y_ref = ref.forward(d["x"], d["topk_idx"], d["topk_w"], *wts, fused=False).clone()
     lane = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev, packed=packed)
     y = lane.forward_fused(d["x"], ids, d["topk_w"], *wts)
     torch.cuda.synchronize()

@@ -29,8 +29,9 @@ def _cuda():
     torch.cuda.synchronize()
 
 
-def check_dispatch(x, idx, E, R, recv, counts, src_map, status):
-    """Bit-exact dispatch check against the oracle's canonical routing."""
+def check_routing(idx, E, R, counts, src_map, status):
+    """Counts, source map and status bit-exact against the oracle's
+    canonical routing."""
     rr = O.route(idx.cpu().numpy(), E, R)
     assert counts.cpu().numpy().tolist() == rr.counts.tolist()
     assert np.array_equal(src_map.cpu().numpy(), rr.src_map)
@@ -38,12 +39,42 @@ def check_dispatch(x, idx, E, R, recv, counts, src_map, status):
     assert int(st[1]) == rr.dropped
     assert bool(st[0] & api.DEV_CAPACITY_DROPPED) == (rr.dropped > 0)
     assert bool(st[0] & api.DEV_BAD_EXPERT_ID) == rr.bad_id
+    return rr
+
+
+def check_dispatch(x, idx, E, R, recv, counts, src_map, status):
+    """Bit-exact dispatch check against the oracle's canonical routing."""
+    rr = check_routing(idx, E, R, counts, src_map, status)
     # payload: every kept route's row equals its token row, bit for bit
     sm = torch.from_numpy(rr.src_map).to(x.device).long()
     tok = torch.arange(x.shape[0], device=x.device)[:, None].expand_as(sm)
     keep = sm >= 0
     rows = recv.view(-1, x.shape[1])[sm[keep]]
     assert torch.equal(rows.view(torch.int16), x[tok[keep]].view(torch.int16))
+    return rr
+
+
+def check_dispatch_fp8(x, idx, E, R, xq, xs, counts, src_map, status, max_tokens=1024, seed=0):
+    """The fused dispatch+quant path's outputs: routing bit-exact against the
+    oracle; every kept route's e4m3 row and scales equal those of the other
+    routes of its token (all K copies identical); and, on all tokens or a
+    sample of max_tokens, the oracle's quantisation of the token row."""
+    rr = check_routing(idx, E, R, counts, src_map, status)
+    H = x.shape[1]
+    q_rows, s_rows = xq.reshape(-1, H), xs.reshape(-1, H // 128)
+    sm = torch.from_numpy(rr.src_map).to(x.device).long()
+    keep = sm >= 0
+    first = torch.where(keep, sm, torch.iinfo(torch.int64).max).min(dim=1).values
+    tok = torch.arange(x.shape[0], device=x.device)[:, None].expand_as(sm)
+    assert torch.equal(q_rows[sm[keep]], q_rows[first[tok[keep]]])
+    assert torch.equal(s_rows[sm[keep]], s_rows[first[tok[keep]]])
+    has = np.nonzero(keep.any(dim=1).cpu().numpy())[0]
+    if len(has) > max_tokens:
+        has = np.sort(np.random.default_rng(seed).choice(has, max_tokens, replace=False))
+    codes, scales = O.quantize_rows(f32(x[torch.from_numpy(has).to(x.device)]))
+    rows = first[torch.from_numpy(has).to(x.device)]
+    assert np.array_equal(q_rows[rows].cpu().numpy(), codes)
+    assert np.array_equal(s_rows[rows].cpu().numpy(), scales)
     return rr
 
 
@@ -174,8 +205,8 @@ def test_layer_fused_path_bit_identical(name):
     wl = d["wl"]
     args = (d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
     buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
-    y1 = buf.forward(*args).clone()
-    y2 = buf.forward_fused(*args)
+    y1 = buf.forward(*args, fused=False).clone()
+    y2 = buf.forward(*args)
     torch.cuda.synchronize()
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     assert buf.dev_status.cpu().tolist()[0] & api.DEV_TIMEOUT == 0
@@ -465,13 +496,21 @@ def test_graph_replay_changes_routes():
 
 def test_layer_decode_config():
     """Decode-shaped layer, full size (T=256, E=64, top-8, H=4096, I=1536,
-    R=256): dispatch bit-exact, every token's output against the oracle."""
+    R=256), both layer paths: dispatch (BF16 rows, or FP8 rows and scales on
+    the fused path) bit-exact, y the same bytes, every fourth token's output
+    against the oracle."""
     d = W.make_layer_inputs("decode", seed=0, device=DEV)
     wl = d["wl"]
     buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
-    y = buf.forward(d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
+    args = (d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
+    y_sep = buf.forward(*args, fused=False).clone()
     torch.cuda.synchronize()
     check_dispatch(d["x"], d["topk_idx"], wl.E, wl.R, buf.recv, buf.counts, buf.src_map, buf.dev_status)
+    y = buf.forward(*args)
+    torch.cuda.synchronize()
+    xq, xs, _, _ = buf.workspace_views()
+    check_dispatch_fp8(d["x"], d["topk_idx"], wl.E, wl.R, xq, xs, buf.counts, buf.src_map, buf.dev_status)
+    assert torch.equal(y.view(torch.int16), y_sep.view(torch.int16))
     toks = np.arange(0, wl.T, 4)
     y_ref, _, _ = _layer_oracle(d, toks)
     assert_rows_close(f32(y)[toks], y_ref, what="decode y")
@@ -537,8 +576,14 @@ def test_layer_prefill_config_and_split():
     args = (d["w13"], d["s13"], d["w2"], d["s2"])
     y = buf.forward(d["x"], d["topk_idx"], d["topk_w"], *args).clone()
     torch.cuda.synchronize()
-    rr = check_dispatch(d["x"], d["topk_idx"], wl.E, wl.R, buf.recv, buf.counts, buf.src_map, buf.dev_status)
+    xq, xs, _, _ = buf.workspace_views()
+    rr = check_dispatch_fp8(d["x"], d["topk_idx"], wl.E, wl.R, xq, xs, buf.counts, buf.src_map,
+                            buf.dev_status, max_tokens=wl.T)
     assert rr.dropped > 0
+    y_sep = buf.forward(d["x"], d["topk_idx"], d["topk_w"], *args, fused=False).clone()
+    torch.cuda.synchronize()
+    check_dispatch(d["x"], d["topk_idx"], wl.E, wl.R, buf.recv, buf.counts, buf.src_map, buf.dev_status)
+    assert torch.equal(y_sep.view(torch.int16), y.view(torch.int16))
     _sampled_out_check(d, buf, 48, seed=1)
     want = O.combine_f32_sequential(f32(buf.out).reshape(-1, wl.H), buf.src_map.cpu().numpy(),
                                     d["topk_w"].cpu().numpy())
@@ -558,14 +603,16 @@ def test_layer_prefill_config_and_split():
     assert torch.equal(y_split[same].view(torch.int16), y[same].view(torch.int16))
 
 
-def test_two_batch_overlap_equals_serial_split():
+@pytest.mark.parametrize("fused", [True, False])
+def test_two_batch_overlap_equals_serial_split(fused):
     """The overlapped two-micro-batch schedule (two lanes, two streams) writes
     exactly what the serial split writes, and equals the unsplit layer on every
-    token whose routes are kept in both."""
+    token whose routes are kept in both; with the fused dispatch+quant stages
+    and with the separate ones."""
     d = W.make_layer_inputs("prefill", seed=4, device=DEV)
     wl = d["wl"]
     args = (d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
-    tbo = api.TwoBatchOverlap(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
+    tbo = api.TwoBatchOverlap(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV), fused=fused)
     y_serial = tbo.forward(*args, overlap=False).clone()
     y_over = tbo.forward(*args, overlap=True).clone()
     full = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
@@ -614,9 +661,12 @@ def test_two_batch_overlap_graph_replay():
 
 def test_layer_large_config_sampled():
     """Large layer (T=16384, E=256, H=7168, I=2048, R=4096, ~11 GB of FP8
-    weights), in the launch configuration the benchmark times: dispatch
-    bit-exact, sampled expert rows against the oracle, combine bit-exact
-    against the fp32 restatement, two graph replays with new routing."""
+    weights), in the launch configuration the benchmark times (the fused
+    dispatch+quant path in a CUDA graph): routing bit-exact, the FP8 rows of
+    512 sampled tokens against the oracle's quantisation (and every copy of a
+    token's row identical), sampled expert rows against the oracle, combine
+    bit-exact against the fp32 restatement, two graph replays with new
+    routing."""
     d = W.make_layer_inputs("large", seed=0, device=DEV)
     wl = d["wl"]
     buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, torch.device(DEV))
@@ -636,7 +686,9 @@ def test_layer_large_config_sampled():
         w.copy_(w2_)
         graph.replay()
         torch.cuda.synchronize()
-        check_dispatch(d["x"], idx, wl.E, wl.R, buf.recv, buf.counts, buf.src_map, buf.dev_status)
+        xq, xs, _, _ = buf.workspace_views()
+        check_dispatch_fp8(d["x"], idx, wl.E, wl.R, xq, xs, buf.counts, buf.src_map, buf.dev_status,
+                           max_tokens=512, seed=seed)
         dd = dict(d, topk_idx=idx, topk_w=w)
         _sampled_out_check(dd, buf, 24, seed=seed)
         toks = np.random.default_rng(seed).choice(wl.T, 512, replace=False)

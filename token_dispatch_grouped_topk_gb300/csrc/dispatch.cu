@@ -164,7 +164,7 @@ __device__ void single_pass_bases(const IdT* __restrict__ topk_idx, int T, int K
   __syncthreads();
 }
 
-template <typename IdT, bool kSingle>
+template <typename IdT, bool kSingle, bool kPreload>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
     route_scatter_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx, int T,
                          int H, int K, int E, RowLayout rl, int nblocks,
@@ -211,9 +211,11 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   // When the warp's tokens' slices fit in sixteen 16-byte vectors per lane
   // (U per token; the slices are short when there are few tokens, as at
   // decode and prefill), every load is issued before the first store: one
-  // memory round trip per warp instead of one per token (prefill -5 %).
-  const int U = (v1 - v0 + 31) / 32;
-  if (U * tpw <= 16) {
+  // memory round trip per warp instead of one per token (prefill -5 %).  It
+  // is a kernel of its own: its registers would halve the resident warps of
+  // the loop below.
+  if constexpr (kPreload) {
+    const int U = (vec_per_slice + 31) / 32;
     uint4 a[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -234,33 +236,72 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
         if (qq >= 0) recv[static_cast<size_t>(qq) * nvec + v] = a[i];
       }
     }
-    return;
-  }
-  for (int tt = 0; tt < tpw; ++tt) {
-    const int t = gw * tpw + tt;
-    if (t >= T) break;
-    const int* dq = wdest + tt * K;
-    bool any = false;
-    for (int k = 0; k < K; ++k) any |= dq[k] >= 0;
-    if (!any) continue;
-    const uint4* src = x + static_cast<size_t>(t) * nvec;
-    // eight 16-byte vectors per lane in flight (four left the large layer's
-    // scatter 6 % slower)
-    for (int v = v0 + lane; v < v1; v += 32 * 8) {
-      uint4 a[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (v + 32 * u < v1) a[u] = ld_stream(src + v + 32 * u);
-      for (int k = 0; k < K; ++k) {
-        const int qq = dq[k];
-        if (qq < 0) continue;
-        uint4* dst = recv + static_cast<size_t>(qq) * nvec;
-#pragma unroll
+  } else {
+    for (int tt = 0; tt < tpw; ++tt) {
+      const int t = gw * tpw + tt;
+      if (t >= T) break;
+      const int* dq = wdest + tt * K;
+      bool any = false;
+      for (int k = 0; k < K; ++k) any |= dq[k] >= 0;
+      if (!any) continue;
+      const uint4* src = x + static_cast<size_t>(t) * nvec;
+      // eight 16-byte vectors per lane in flight (four left the large layer's
+      // scatter 6 % slower)
+      for (int v = v0 + lane; v < v1; v += 32 * 8) {
+        uint4 a[8];
+  #pragma unroll
         for (int u = 0; u < 8; ++u)
-          if (v + 32 * u < v1) dst[v + 32 * u] = a[u];
+          if (v + 32 * u < v1) a[u] = ld_stream(src + v + 32 * u);
+        for (int k = 0; k < K; ++k) {
+          const int qq = dq[k];
+          if (qq < 0) continue;
+          uint4* dst = recv + static_cast<size_t>(qq) * nvec;
+  #pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (v + 32 * u < v1) dst[v + 32 * u] = a[u];
+        }
       }
     }
   }
+}
+
+// One 128-element group per half-warp (8 BF16 per lane): the group amax by a
+// 4-step shuffle, then the lane's 8 e4m3 codes and the group's scale.  Every
+// lane of the warp calls it (the shuffles); `on` marks lanes with a group.
+__device__ __forceinline__ void quantize_group(const uint4& v, bool on, uint2* codes,
+                                               float* scale) {
+  float f[8];
+  float amax = 0.f;
+  if (on) {
+    bf16x8_to_f32(v, f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  }
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  *codes = make_uint2(0u, 0u);
+  *scale = 0.f;
+  if (!on) return;
+  float mult;
+  fp8_group_scale(amax, &mult, scale);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    lo |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[2 * i], mult), __fmul_rn(f[2 * i + 1], mult)))
+          << (16 * i);
+    hi |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[4 + 2 * i], mult), __fmul_rn(f[5 + 2 * i], mult)))
+          << (16 * i);
+  }
+  *codes = make_uint2(lo, hi);
+}
+
+// The FP8 scatter issues all of a warp's loads before its first conversion
+// when each lane needs at most sixteen (one per half-warp group pair and
+// token) and the grid fits on the GPU in one wave.  With more blocks than
+// that, the extra registers cost more resident warps than the loads gain
+// (prefill +14 %); in one wave (decode) it took the kernel from 19 to 15 us.
+__host__ __device__ __forceinline__ bool fp8_preload_fits(int groups_per_slice, int K) {
+  return (groups_per_slice + 1) / 2 * (32 / K) <= 16;
 }
 
 // Dispatch fused with the per-token FP8 quantisation ("SGLang Expert Compute
@@ -270,7 +311,7 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
 // fp32 scales are written to every kept destination row; the BF16 receive
 // buffer is never formed.  Rank derivation is the one of route_scatter_kernel.
 // Each block takes a slice of whole 128-groups of its tokens' rows.
-template <typename IdT, bool kSingle>
+template <typename IdT, bool kSingle, bool kPreload>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
     route_scatter_fp8_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx,
                              int T, int H, int K, int E, RowLayout rl, int nblocks,
@@ -284,7 +325,7 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   int* s_rows = s_dest + kDispatchWarps * 32;                       // [E + 1] packed row bases
   int* s_prev = s_rows + E + 1;                                    // single pass: [E]
   int* s_tot = s_prev + E;                                         //              [E]
-  float* s_sc = reinterpret_cast<float*>(s_tot + E);               // [warps][groups_per_slice]
+  float* s_sc = reinterpret_cast<float*>(s_tot + E);  // [warps][tpw or 1][groups_per_slice]
   for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) s_cnt[i] = 0;
   if (kSingle)
     single_pass_bases(topk_idx, T, K, E, rl, s_prev, s_tot, s_rows, counts, dev_status);
@@ -315,65 +356,91 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   const int g0 = blockIdx.y * groups_per_slice;
   const int g1 = min(G, g0 + groups_per_slice);
   const int* wdest = s_dest + warp * 32;
-  float* wsc = s_sc + warp * groups_per_slice;
-  for (int tt = 0; tt < tpw; ++tt) {
-    const int t = gw * tpw + tt;
-    if (t >= T) break;
-    const int* dq = wdest + tt * K;
-    bool any = false;
-    for (int k = 0; k < K; ++k) any |= dq[k] >= 0;
-    if (!any) continue;
-    const uint4* src = x + static_cast<size_t>(t) * (H / 8);
-    // eight groups per pass: half-warp `half` takes groups gg + 2u + half
-    for (int gg = g0; gg < g1; gg += 8) {
-      uint4 v[4];
+  if constexpr (kPreload) {
+    // Scales staged per token: [tpw][groups_per_slice].  Load i is token
+    // i / U's group pair i % U (U pairs per half-warp per token).
+    float* wsc = s_sc + warp * tpw * groups_per_slice;
+    const int U = (groups_per_slice + 1) / 2;
+    const unsigned kept = __ballot_sync(0xffffffffu, q >= 0);
+    const unsigned kmask = K >= 32 ? 0xffffffffu : ((1u << K) - 1u);
+    uint4 v[16];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int g = gg + 2 * u + half;
-        if (g < g1) v[u] = ld_stream(src + g * 16 + hl);
-      }
+    for (int i = 0; i < 16; ++i) {
+      const int tt = i / U, u = i - (i / U) * U;
+      const int t = gw * tpw + tt;
+      const int g = g0 + 2 * u + half;
+      if (tt < tpw && t < T && g < g1 && ((kept >> (tt * K)) & kmask))
+        v[i] = ld_stream(x + static_cast<size_t>(t) * (H / 8) + g * 16 + hl);
+    }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int g = gg + 2 * u + half;
-        const bool on = g < g1;
-        float f[8];
-        float amax = 0.f;
-        if (on) {
-          bf16x8_to_f32(v[u], f);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    for (int i = 0; i < 16; ++i) {
+      const int tt = i / U, u = i - (i / U) * U;
+      if (tt >= tpw) continue;   // the same for the whole warp
+      const int t = gw * tpw + tt;
+      const int g = g0 + 2 * u + half;
+      const bool on = t < T && g < g1 && ((kept >> (tt * K)) & kmask);
+      uint2 codes;
+      float scale;
+      quantize_group(v[i], on, &codes, &scale);
+      if (on) {
+        const int* dq = wdest + tt * K;
+        for (int k = 0; k < K; ++k) {
+          const int qq = dq[k];
+          if (qq >= 0) xq[static_cast<size_t>(qq) * (H / 8) + g * 16 + hl] = codes;
         }
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (on) {
-          float mult, scale;
-          fp8_group_scale(amax, &mult, &scale);
-          uint32_t lo = 0, hi = 0;
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            lo |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[2 * i], mult),
-                                                    __fmul_rn(f[2 * i + 1], mult)))
-                  << (16 * i);
-            hi |= static_cast<uint32_t>(pack_e4m3x2(__fmul_rn(f[4 + 2 * i], mult),
-                                                    __fmul_rn(f[5 + 2 * i], mult)))
-                  << (16 * i);
-          }
-          const uint2 codes = make_uint2(lo, hi);
-          for (int k = 0; k < K; ++k) {
-            const int qq = dq[k];
-            if (qq >= 0) xq[static_cast<size_t>(qq) * (H / 8) + g * 16 + hl] = codes;
-          }
-          if (hl == 0) wsc[g - g0] = scale;
-        }
+        if (hl == 0) wsc[tt * groups_per_slice + (g - g0)] = scale;
       }
     }
     __syncwarp();
-    for (int k = 0; k < K; ++k) {
-      const int qq = dq[k];
-      if (qq < 0) continue;
-      for (int g = g0 + lane; g < g1; g += 32) xs[static_cast<size_t>(qq) * G + g] = wsc[g - g0];
+    // scales: lane i takes (route, group) pairs i, i + 32, ...
+    const int ng = g1 - g0;
+    for (int i = lane; i < tpw * K * ng; i += 32) {
+      const int rt = i / ng, g = i - (i / ng) * ng;
+      const int qq = wdest[rt];
+      if (qq >= 0) xs[static_cast<size_t>(qq) * G + g0 + g] = wsc[(rt / K) * groups_per_slice + g];
     }
-    __syncwarp();
+  } else {
+    float* wsc = s_sc + warp * groups_per_slice;
+    for (int tt = 0; tt < tpw; ++tt) {
+      const int t = gw * tpw + tt;
+      if (t >= T) break;
+      const int* dq = wdest + tt * K;
+      bool any = false;
+      for (int k = 0; k < K; ++k) any |= dq[k] >= 0;
+      if (!any) continue;
+      const uint4* src = x + static_cast<size_t>(t) * (H / 8);
+      // eight groups per pass: half-warp `half` takes groups gg + 2u + half
+      for (int gg = g0; gg < g1; gg += 8) {
+        uint4 v[4];
+  #pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int g = gg + 2 * u + half;
+          if (g < g1) v[u] = ld_stream(src + g * 16 + hl);
+        }
+  #pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int g = gg + 2 * u + half;
+          const bool on = g < g1;
+          uint2 codes;
+          float scale;
+          quantize_group(v[u], on, &codes, &scale);
+          if (on) {
+            for (int k = 0; k < K; ++k) {
+              const int qq = dq[k];
+              if (qq >= 0) xq[static_cast<size_t>(qq) * (H / 8) + g * 16 + hl] = codes;
+            }
+            if (hl == 0) wsc[g - g0] = scale;
+          }
+        }
+      }
+      __syncwarp();
+      for (int k = 0; k < K; ++k) {
+        const int qq = dq[k];
+        if (qq < 0) continue;
+        for (int g = g0 + lane; g < g1; g += 32) xs[static_cast<size_t>(qq) * G + g] = wsc[g - g0];
+      }
+      __syncwarp();
+    }
   }
 }
 
@@ -533,17 +600,13 @@ cudaError_t dispatch_impl(const void* x, const IdT* topk_idx, int T, int H, int 
   hsplit = (nvec + vec_per_slice - 1) / vec_per_slice;
   const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + 3 * E + 1) * sizeof(int);
   const dim3 grid(nblocks, hsplit);
-  if ((err = allow_smem(one ? route_scatter_kernel<IdT, true> : route_scatter_kernel<IdT, false>,
-                        smem)) != cudaSuccess)
-    return err;
-  if (one)
-    route_scatter_kernel<IdT, true><<<grid, kDispatchWarps * 32, smem, s>>>(
-        static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
-        static_cast<uint4*>(recv), src_map, dev_status, vec_per_slice);
-  else
-    route_scatter_kernel<IdT, false><<<grid, kDispatchWarps * 32, smem, s>>>(
-        static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
-        static_cast<uint4*>(recv), src_map, dev_status, vec_per_slice);
+  const bool pre = (vec_per_slice + 31) / 32 * (32 / K) <= 16;
+  auto kernel = one ? (pre ? route_scatter_kernel<IdT, true, true> : route_scatter_kernel<IdT, true, false>)
+                    : (pre ? route_scatter_kernel<IdT, false, true> : route_scatter_kernel<IdT, false, false>);
+  if ((err = allow_smem(kernel, smem)) != cudaSuccess) return err;
+  kernel<<<grid, kDispatchWarps * 32, smem, s>>>(static_cast<const uint4*>(x), topk_idx, T, H, K, E,
+                                                 rl, nblocks, hist, counts, static_cast<uint4*>(recv),
+                                                 src_map, dev_status, vec_per_slice);
   return cudaGetLastError();
 }
 }  // namespace
@@ -619,26 +682,24 @@ cudaError_t dispatch_quant_impl(const void* x, const IdT* topk_idx, int T, int H
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (nblocks == 0) return cudaSuccess;
   }
-  // Slices of whole 128-groups when there are too few tokens to fill the GPU.
+  // Slices of two or more whole 128-groups when there are too few tokens to
+  // fill the GPU (one-group slices would leave a half-warp idle).
   const int G = H / kGroup;
-  int hsplit = row_slices(nblocks, G, 4, sm_count);
+  int hsplit = row_slices(nblocks, G, 2, sm_count);
   const int gps = (G + hsplit - 1) / hsplit;
   hsplit = (G + gps - 1) / gps;
+  const bool pre = fp8_preload_fits(gps, K) && static_cast<long long>(nblocks) * hsplit <= sm_count;
   const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + 3 * E + 1) * sizeof(int) +
-                      kDispatchWarps * gps * sizeof(float);
+                      kDispatchWarps * (pre ? 32 / K : 1) * gps * sizeof(float);
   const dim3 grid(nblocks, hsplit);
-  if ((err = allow_smem(one ? route_scatter_fp8_kernel<IdT, true>
-                            : route_scatter_fp8_kernel<IdT, false>,
-                        smem)) != cudaSuccess)
-    return err;
-  if (one)
-    route_scatter_fp8_kernel<IdT, true><<<grid, kDispatchWarps * 32, smem, s>>>(
-        static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
-        reinterpret_cast<uint2*>(xq), xs, src_map, dev_status, gps);
-  else
-    route_scatter_fp8_kernel<IdT, false><<<grid, kDispatchWarps * 32, smem, s>>>(
-        static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
-        reinterpret_cast<uint2*>(xq), xs, src_map, dev_status, gps);
+  auto kernel = one ? (pre ? route_scatter_fp8_kernel<IdT, true, true>
+                           : route_scatter_fp8_kernel<IdT, true, false>)
+                    : (pre ? route_scatter_fp8_kernel<IdT, false, true>
+                           : route_scatter_fp8_kernel<IdT, false, false>);
+  if ((err = allow_smem(kernel, smem)) != cudaSuccess) return err;
+  kernel<<<grid, kDispatchWarps * 32, smem, s>>>(
+      static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
+      reinterpret_cast<uint2*>(xq), xs, src_map, dev_status, gps);
   return cudaGetLastError();
 }
 }  // namespace
