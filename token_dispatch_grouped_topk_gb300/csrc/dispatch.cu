@@ -164,7 +164,7 @@ __device__ void single_pass_bases(const IdT* __restrict__ topk_idx, int T, int K
   __syncthreads();
 }
 
-template <typename IdT, bool kSingle, bool kPreload>
+template <typename IdT, bool kSingle, int kPreload>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
     route_scatter_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx, int T,
                          int H, int K, int E, RowLayout rl, int nblocks,
@@ -208,24 +208,25 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   const int v0 = blockIdx.y * vec_per_slice;
   const int v1 = min(nvec, v0 + vec_per_slice);
   const int* wdest = s_dest + warp * 32;
-  // When the warp's tokens' slices fit in sixteen 16-byte vectors per lane
-  // (U per token; the slices are short when there are few tokens, as at
-  // decode and prefill), every load is issued before the first store: one
-  // memory round trip per warp instead of one per token (prefill -5 %).  It
-  // is a kernel of its own: its registers would halve the resident warps of
-  // the loop below.
-  if constexpr (kPreload) {
+  // When the warp's tokens' slices fit in kPreload (8 or 16) 16-byte vectors
+  // per lane (U per token; the slices are short when there are few tokens, as
+  // at decode and prefill), every load is issued before the first store: one
+  // memory round trip per warp instead of one per token (prefill -5 %, and
+  // -3 % more with the 8-deep form, which needs 64 registers against 128).
+  // It is a kernel of its own: its registers would cut the resident warps of
+  // the loop below (48 registers).
+  if constexpr (kPreload > 0) {
     const int U = (vec_per_slice + 31) / 32;
-    uint4 a[16];
+    uint4 a[kPreload];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kPreload; ++i) {
       const int tt = i / U, u = i - (i / U) * U;
       const int t = gw * tpw + tt;
       const int v = v0 + lane + 32 * u;
       if (tt < tpw && t < T && v < v1) a[i] = ld_stream(x + static_cast<size_t>(t) * nvec + v);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kPreload; ++i) {
       const int tt = i / U, u = i - (i / U) * U;
       const int t = gw * tpw + tt;
       const int v = v0 + lane + 32 * u;
@@ -296,14 +297,12 @@ __device__ __forceinline__ void quantize_group(const uint4& v, bool on, uint2* c
 }
 
 // The FP8 scatter issues all of a warp's loads before its first conversion
-// when each lane needs at most sixteen (one per half-warp group pair and
-// token) and the grid fits on the GPU in one wave.  With more blocks than
-// that, the extra registers cost more resident warps than the loads gain
-// (prefill +14 %); in one wave (decode) it took the kernel from 19 to 15 us.
-__host__ __device__ __forceinline__ bool fp8_preload_fits(int groups_per_slice, int K) {
-  return (groups_per_slice + 1) / 2 * (32 / K) <= 16;
-}
-
+// (kPreload = 8 or 16 loads per lane, one per half-warp group pair and token)
+// when each lane needs at most eight, or at most sixteen and the grid fits on
+// the GPU in one wave.  The 8-deep form costs no registers over the loop
+// (64): decode 15.0 -> 12.9 us, prefill 52.9 -> 42.7 us.  The 16-deep form
+// takes 127 registers, which with more blocks than one wave cost more
+// resident warps than the loads gain; kPreload = 0 is the loop over tokens.
 // Dispatch fused with the per-token FP8 quantisation ("SGLang Expert Compute
 // Backend", §4.4: quantise while packing instead of materialising BF16 rows).
 // Every route of a token carries the same row, and the quantisation is per row
@@ -311,7 +310,7 @@ __host__ __device__ __forceinline__ bool fp8_preload_fits(int groups_per_slice, 
 // fp32 scales are written to every kept destination row; the BF16 receive
 // buffer is never formed.  Rank derivation is the one of route_scatter_kernel.
 // Each block takes a slice of whole 128-groups of its tokens' rows.
-template <typename IdT, bool kSingle, bool kPreload>
+template <typename IdT, bool kSingle, int kPreload>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
     route_scatter_fp8_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx,
                              int T, int H, int K, int E, RowLayout rl, int nblocks,
@@ -356,16 +355,16 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   const int g0 = blockIdx.y * groups_per_slice;
   const int g1 = min(G, g0 + groups_per_slice);
   const int* wdest = s_dest + warp * 32;
-  if constexpr (kPreload) {
+  if constexpr (kPreload > 0) {
     // Scales staged per token: [tpw][groups_per_slice].  Load i is token
     // i / U's group pair i % U (U pairs per half-warp per token).
     float* wsc = s_sc + warp * tpw * groups_per_slice;
     const int U = (groups_per_slice + 1) / 2;
     const unsigned kept = __ballot_sync(0xffffffffu, q >= 0);
     const unsigned kmask = K >= 32 ? 0xffffffffu : ((1u << K) - 1u);
-    uint4 v[16];
+    uint4 v[kPreload];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kPreload; ++i) {
       const int tt = i / U, u = i - (i / U) * U;
       const int t = gw * tpw + tt;
       const int g = g0 + 2 * u + half;
@@ -373,7 +372,7 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
         v[i] = ld_stream(x + static_cast<size_t>(t) * (H / 8) + g * 16 + hl);
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kPreload; ++i) {
       const int tt = i / U, u = i - (i / U) * U;
       if (tt >= tpw) continue;   // the same for the whole warp
       const int t = gw * tpw + tt;
@@ -600,9 +599,12 @@ cudaError_t dispatch_impl(const void* x, const IdT* topk_idx, int T, int H, int 
   hsplit = (nvec + vec_per_slice - 1) / vec_per_slice;
   const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + 3 * E + 1) * sizeof(int);
   const dim3 grid(nblocks, hsplit);
-  const bool pre = (vec_per_slice + 31) / 32 * (32 / K) <= 16;
-  auto kernel = one ? (pre ? route_scatter_kernel<IdT, true, true> : route_scatter_kernel<IdT, true, false>)
-                    : (pre ? route_scatter_kernel<IdT, false, true> : route_scatter_kernel<IdT, false, false>);
+  const int need = (vec_per_slice + 31) / 32 * (32 / K);
+  const int depth = need <= 8 ? 8 : (need <= 16 ? 16 : 0);
+  auto kernel = one ? (depth == 8 ? route_scatter_kernel<IdT, true, 8>
+                       : depth == 16 ? route_scatter_kernel<IdT, true, 16> : route_scatter_kernel<IdT, true, 0>)
+                    : (depth == 8 ? route_scatter_kernel<IdT, false, 8>
+                       : depth == 16 ? route_scatter_kernel<IdT, false, 16> : route_scatter_kernel<IdT, false, 0>);
   if ((err = allow_smem(kernel, smem)) != cudaSuccess) return err;
   kernel<<<grid, kDispatchWarps * 32, smem, s>>>(static_cast<const uint4*>(x), topk_idx, T, H, K, E,
                                                  rl, nblocks, hist, counts, static_cast<uint4*>(recv),
@@ -688,14 +690,19 @@ cudaError_t dispatch_quant_impl(const void* x, const IdT* topk_idx, int T, int H
   int hsplit = row_slices(nblocks, G, 2, sm_count);
   const int gps = (G + hsplit - 1) / hsplit;
   hsplit = (G + gps - 1) / gps;
-  const bool pre = fp8_preload_fits(gps, K) && static_cast<long long>(nblocks) * hsplit <= sm_count;
+  const int need = (gps + 1) / 2 * (32 / K);   // loads per lane to preload a warp's slices
+  const bool one_wave = static_cast<long long>(nblocks) * hsplit <= sm_count;
+  const int depth = need <= 8 ? 8 : (need <= 16 && one_wave ? 16 : 0);
+  const bool pre = depth > 0;
   const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + 3 * E + 1) * sizeof(int) +
                       kDispatchWarps * (pre ? 32 / K : 1) * gps * sizeof(float);
   const dim3 grid(nblocks, hsplit);
-  auto kernel = one ? (pre ? route_scatter_fp8_kernel<IdT, true, true>
-                           : route_scatter_fp8_kernel<IdT, true, false>)
-                    : (pre ? route_scatter_fp8_kernel<IdT, false, true>
-                           : route_scatter_fp8_kernel<IdT, false, false>);
+  auto kernel = one ? (depth == 16 ? route_scatter_fp8_kernel<IdT, true, 16>
+                       : depth == 8 ? route_scatter_fp8_kernel<IdT, true, 8>
+                                    : route_scatter_fp8_kernel<IdT, true, 0>)
+                    : (depth == 16 ? route_scatter_fp8_kernel<IdT, false, 16>
+                       : depth == 8 ? route_scatter_fp8_kernel<IdT, false, 8>
+                                    : route_scatter_fp8_kernel<IdT, false, 0>);
   if ((err = allow_smem(kernel, smem)) != cudaSuccess) return err;
   kernel<<<grid, kDispatchWarps * 32, smem, s>>>(
       static_cast<const uint4*>(x), topk_idx, T, H, K, E, rl, nblocks, hist, counts,
