@@ -170,11 +170,16 @@ def test_quantize_bit_exact_ragged():
 
 # ------------------------------------------------- fused dispatch + quant
 
-@pytest.mark.parametrize("T,E,K,R,H", [(300, 33, 5, 40, 640), (4, 8, 2, 4, 256), (2000, 64, 8, 200, 1024)])
+@pytest.mark.parametrize("T,E,K,R,H", [(300, 33, 5, 40, 640), (4, 8, 2, 4, 256), (2000, 64, 8, 200, 1024),
+                                       (3000, 16, 2, 500, 256), (2100, 12, 1, 300, 1024),
+                                       (5000, 12, 1, 500, 1024)])
 def test_dispatch_quant_matches_dispatch_then_quant(T, E, K, R, H):
     """moe_dispatch_quant writes exactly the bytes moe_quantize_fp8 writes on
     moe_dispatch's receive rows (and the oracle's quantisation of the token
-    rows), with the same counts, source map and status."""
+    rows), with the same counts, source map and status.  The shapes take every
+    form of the kernel on a 152-SM GB300: single pass with 16 and no preloaded
+    loads per lane (first two, fifth), three launches with 8, 16 and none
+    (third, fourth, sixth)."""
     g = torch.Generator().manual_seed(T + E)
     idx = torch.randint(-1, E, (T, K), generator=g)
     idx[:, 0] = torch.randint(0, 3, (T,), generator=g)     # hot experts: capacity drops
