@@ -640,21 +640,44 @@ def run_ours(args, rank, local, world):
 
     e2e_steps = max(3, min(args.steps, 20))
 
-    def e2e_time(step_fn, first_stream, last_stream):
+    def e2e_time(step_fn, first_stream, last_stream, sampler=None, load_s=0.5):
         for i in range(args.warmup):
             step_fn(i)
         torch.cuda.synchronize()
-        barrier(world)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(first_stream)
-        for i in range(e2e_steps):
-            step_fn(args.warmup + i)
-        b.record(last_stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        return reduce_max(a.elapsed_time(b), world, dev)
 
-    e2e_ms = e2e_time(e2e_step, pipe.s_in, pipe.s_out)
+        def load():
+            t0 = time.perf_counter()
+            i = 0
+            while time.perf_counter() - t0 < load_s:
+                step_fn(i)
+                i += 1
+                if i % 4 == 0:
+                    torch.cuda.synchronize()
+            torch.cuda.synchronize()
+
+        def timed():
+            barrier(world)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(first_stream)
+            for i in range(e2e_steps):
+                step_fn(args.warmup + i)
+            b.record(last_stream)
+            torch.cuda.synchronize()
+            barrier(world)
+            return a.elapsed_time(b)
+
+        if sampler is None:
+            ms = timed()
+        else:
+            with sampler:
+                load()
+                ms = timed()
+                load()
+        return reduce_max(ms, world, dev)
+
+    # clocks sampled around the pipelined run (the copies add to the GPU's power draw)
+    e2e_clk = ClockSampler(local)
+    e2e_ms = e2e_time(e2e_step, pipe.s_in, pipe.s_out, sampler=e2e_clk)
     e2e_serial_ms = e2e_time(e2e_serial_step, stream, stream)
     del pipe
     e2e_rows = reduce_sum(float(sum(n_valid[(args.warmup + i) % N_ROUTINGS] for i in range(e2e_steps))), world, dev)
@@ -746,6 +769,7 @@ def run_ours(args, rank, local, world):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
                 "path": "api.HostPipeline: pinned host in/out every step; step i+1's copy-in and "
                         "step i-1's copy-out run on two copy streams beside step i's compute",
+                "clocks": e2e_clk.summary(),
                 "serial_value": e2e_rows / (e2e_serial_ms / 1e3),
                 "serial_note": "copy in, compute, copy out back to back on one stream"},
         "gpu_launches": launches_per_step * args.steps, "launches_per_step": launches_per_step,

@@ -9,6 +9,10 @@ inputs still exceed L2.
 
     python -m token_dispatch_grouped_topk_gb300.profile_case [--E 32] [--rows 512]
            [--H 7168] [--I 2048] [--reps 3] [--fused]
+
+With --dispatch WORKLOAD it instead runs the dispatch fused with the
+quantisation (moe_dispatch_quant, padded layout) `reps` times on that named
+layer's inputs (seed 0): a capture of the prefill layer holds about 1.1 GB.
 """
 import argparse
 
@@ -26,8 +30,18 @@ def main():
     ap.add_argument("--I", type=int, default=2048)
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--fused", action="store_true")
+    ap.add_argument("--dispatch", default=None, choices=["decode", "prefill", "large"])
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
+    if a.dispatch:
+        d = W.make_layer_inputs(a.dispatch, seed=0, device=dev, weights=False)
+        wl = d["wl"]
+        for _ in range(a.reps):
+            _, _, counts, _, st = api.moe_dispatch_quant(d["x"], d["topk_idx"], None, wl.E, wl.R)
+        torch.cuda.synchronize()
+        print(f"profile case ok: dispatch+quant {a.dispatch} x{a.reps}, kept routes "
+              f"{int(counts.sum())}, status {st.cpu().tolist()}")
+        return
     E, R, H, I = a.E, a.rows, a.H, a.I
     recv = W.activations(E * R, H, 1, dev).view(E, R, H)
     counts = torch.full((E,), R, dtype=torch.int32, device=dev)
