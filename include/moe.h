@@ -26,8 +26,9 @@
  *    FP8 tensors are e4m3 (OCP "float8_e4m3fn") codes, one byte each.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream): no host synchronisation, no allocation, no host reads of
- *    device data.  Every call except moe_dispatch_noalloc can be captured
- *    into a CUDA graph.
+ *    device data.  Every call other than moe_dispatch_noalloc can be
+ *    captured into a CUDA graph; nothing is stated here either way about
+ *    capturing moe_dispatch_noalloc.
  *  - Host-detectable errors (null pointers, bad sizes, workspace too small,
  *    unsupported device) return a negative moe_status before anything is
  *    launched.  MOE_ERR_CUDA means a CUDA runtime call failed; the CUDA error
