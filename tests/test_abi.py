@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from token_dispatch_grouped_topk_gb300 import _lib
 
@@ -214,3 +215,19 @@ def test_header_compiles_as_c(tmp_path):
                     "-I", os.path.join(root, "include"), "-I", cuda_inc,
                     os.path.join(root, "tests", "capi", "layer_main.c"),
                     "-o", str(tmp_path / "layer_main.o")], check=True)
+
+
+def test_layer_forward_path_choice_on_host():
+    """MoeLayerBuffers.forward takes the fused dispatch+quant path unless asked
+    not to, and refuses it on the per-source slot layout before any call (the
+    lane is built in host memory: nothing reaches the library)."""
+    from token_dispatch_grouped_topk_gb300 import api
+    T, E, K, H, I, L, mt = 8, 4, 2, 128, 128, 2, 4
+    lane = api.MoeLayerBuffers(T, E, K, H, I, (E // L) * mt, torch.device("cpu"), source_slots=mt, L=L)
+    x = torch.zeros(T, H, dtype=torch.bfloat16)
+    idx = torch.zeros(T, K, dtype=torch.int64)
+    w = torch.zeros(T, K)
+    with pytest.raises(ValueError):
+        lane.forward(x, idx, w, None, None, None, None, fused=True)
+    with pytest.raises(ValueError):
+        lane.forward_fused(x, idx, w, None, None, None, None)
