@@ -704,3 +704,53 @@ def test_layer_large_config_sampled():
         rows = f32(buf.out.view(-1, wl.H)[torch.from_numpy(uniq).to(DEV).long()])
         want = O.combine_f32_sequential(rows, compact, w.cpu().numpy()[toks])
         assert np.array_equal(f32(buf.y)[toks], want)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_layer_degenerate_routings(fused):
+    """Both layer paths on the degenerate inputs: no tokens (counts reset,
+    nothing launched past the dispatch), every route a padding route (no
+    expert rows, y = 0), and every route to one expert past its capacity
+    (drops counted, kept rows against the oracle)."""
+    E, K, H, I, R = 4, 2, 256, 128, 8
+    dev = torch.device(DEV)
+    w13, s13, w2, s2 = (t.to(DEV) for t in W.expert_weights(E, H, I, 17, "cpu"))
+    # no tokens
+    buf = api.MoeLayerBuffers(0, E, K, H, I, R, dev)
+    buf.counts.fill_(99)
+    y = buf.forward(torch.empty(0, H, dtype=torch.bfloat16, device=DEV),
+                    torch.empty(0, K, dtype=torch.int64, device=DEV),
+                    torch.empty(0, K, device=DEV), w13, s13, w2, s2, fused=fused)
+    torch.cuda.synchronize()
+    assert y.shape == (0, H)
+    assert buf.counts.cpu().tolist() == [0] * E and buf.dev_status.cpu().tolist() == [0, 0]
+    # every route a padding route
+    T = 40
+    g = torch.Generator().manual_seed(19)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16).to(DEV)
+    w = torch.rand(T, K, generator=g).to(DEV)
+    buf = api.MoeLayerBuffers(T, E, K, H, I, R, dev)
+    buf.y.fill_(7.0)
+    y = buf.forward(x, torch.full((T, K), -1, dtype=torch.int64, device=DEV), w, w13, s13, w2, s2,
+                    fused=fused)
+    torch.cuda.synchronize()
+    assert buf.counts.cpu().tolist() == [0] * E and buf.dev_status.cpu().tolist() == [0, 0]
+    assert bool((y.float() == 0).all())
+    assert bool((buf.src_map == -1).all())
+    # every route to expert 2: R of T*K kept, the rest dropped
+    idx = torch.full((T, K), 2, dtype=torch.int64)
+    idx[:, 1] = -1
+    buf = api.MoeLayerBuffers(T, E, K, H, I, R, dev)
+    y = buf.forward(x, idx.to(DEV), w, w13, s13, w2, s2, fused=fused)
+    torch.cuda.synchronize()
+    rr = O.route(idx.numpy(), E, R)
+    assert buf.counts.cpu().tolist() == rr.counts.tolist() == [0, 0, R, 0]
+    assert buf.dev_status.cpu().tolist() == [api.DEV_CAPACITY_DROPPED, T - R]
+    assert np.array_equal(buf.src_map.cpu().numpy(), rr.src_map)
+    kept = np.nonzero(rr.src_map[:, 0] >= 0)[0]
+    wts = host_weights({"w13": w13, "s13": s13, "w2": w2, "s2": s2}, [2])
+    ref = oracle_expert_rows(f32(x[torch.from_numpy(kept).to(DEV)]), wts[2])
+    got = f32(buf.out.view(-1, H)[torch.from_numpy(rr.src_map[kept, 0]).long().to(DEV)])
+    assert_rows_close(got, ref, what="one expert's kept rows")
+    yk = f32(y)
+    assert np.all(yk[np.setdiff1d(np.arange(T), kept)] == 0)
