@@ -521,9 +521,11 @@ def test_layer_decode_config():
     assert_rows_close(f32(y)[toks], y_ref, what="decode y")
 
 
-def test_host_pipeline_matches_forward():
+@pytest.mark.parametrize("graph", [False, True])
+def test_host_pipeline_matches_forward(graph):
     """api.HostPipeline (pinned host in/out, copies of neighbouring steps
-    overlapped with compute, two device slots) returns, for every step, the
+    overlapped with compute, two device slots; eager, or each slot's layer
+    captured once in a CUDA graph and replayed) returns, for every step, the
     bytes a plain forward on device inputs returns; five steps reuse each slot
     at least twice, with a different routing per step."""
     d = W.make_layer_inputs("decode", seed=0, device=DEV)
@@ -539,7 +541,7 @@ def test_host_pipeline_matches_forward():
     for x, idx, w in steps:
         y = buf.forward(x.to(dev), idx.to(dev), w.to(dev), d["w13"], d["s13"], d["w2"], d["s2"])
         want.append(y.cpu())
-    pipe = api.HostPipeline(buf)
+    pipe = api.HostPipeline(buf, graph=graph)
     outs = [torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory() for _ in steps]
     pinned = [(x.pin_memory(), idx.pin_memory(), w.pin_memory()) for x, idx, w in steps]
     for (x, idx, w), y_h in zip(pinned, outs):

@@ -622,10 +622,18 @@ class HostPipeline:
     slot is rewritten only after its copy to the host).  The layer itself runs
     on one buffer lane, in submission order.  Host tensors must be pinned and
     must not be touched until ``synchronize()`` (or a later step's completion)
-    has returned."""
+    has returned.
 
-    def __init__(self, lane: "MoeLayerBuffers"):
+    With ``graph=True`` the layer of each input slot is captured once into a
+    CUDA graph (on the slot's first step, which runs eagerly) and replayed on
+    later steps, so a step costs one graph launch instead of the layer's
+    separate launches.  A graph is kept per slot and set of weight tensors;
+    new weight tensors are captured anew."""
+
+    def __init__(self, lane: "MoeLayerBuffers", graph: bool = False):
         self.lane = lane
+        self.graph = graph
+        self._graphs = {}
         d, T, H, K = lane.device, lane.T, lane.H, lane.K
         self.x = [torch.empty(T, H, dtype=torch.bfloat16, device=d) for _ in range(2)]
         self.idx = [torch.empty(T, K, dtype=torch.int64, device=d) for _ in range(2)]
@@ -655,8 +663,7 @@ class HostPipeline:
         cs.wait_event(self.in_ready[k])
         if self.n >= 2:
             cs.wait_event(self.y_free[k])
-        self.lane.forward(self.x[k], self.idx[k], self.w[k], w13, w13_scale, w2, w2_scale,
-                          stream=cs, y=self.y[k])
+        self._compute(k, (w13, w13_scale, w2, w2_scale), cs)
         self.in_free[k].record(cs)
         self.y_ready[k].record(cs)
         self.s_out.wait_event(self.y_ready[k])
@@ -664,6 +671,30 @@ class HostPipeline:
             y_h.copy_(self.y[k], non_blocking=True)
         self.y_free[k].record(self.s_out)
         self.n += 1
+
+    def _forward(self, k, weights, stream):
+        self.lane.forward(self.x[k], self.idx[k], self.w[k], *weights, stream=stream, y=self.y[k])
+
+    def _compute(self, k, weights, cs):
+        if not self.graph:
+            self._forward(k, weights, cs)
+            return
+        key = (k,) + tuple(t.data_ptr() for t in weights)
+        g = self._graphs.get(key)
+        if g is None:
+            # this step runs eagerly; the capture records the same launches
+            # without running them
+            self._forward(k, weights, cs)
+            side = torch.cuda.Stream(self.lane.device)
+            side.wait_stream(cs)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                self._forward(k, weights, side)
+            cs.wait_stream(side)
+            self._graphs[key] = g
+            return
+        with torch.cuda.stream(cs):
+            g.replay()
 
     def synchronize(self):
         """Wait until every submitted step's output is in host memory."""
