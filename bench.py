@@ -861,7 +861,8 @@ def main():
             "separate_dispatch_quant": res["separate"], "packed_layout": res["packed"],
             "source_slots_layout": res["source_slots"], "two_batch_overlap": res["tbo"],
         }
-        line["cpu_baseline"] = cpu_baseline(wl)
+        # the oracle's CPU baseline: rank 0 of a one-GPU run only
+        line["cpu_baseline"] = cpu_baseline(wl) if world == 1 else None
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
