@@ -487,7 +487,8 @@ class MoeLayerBuffers:
             self.rows = E * R
             shape = (E, R, H)
             ws = expert_compute_workspace_size(E, R, H, I)
-        self.recv = torch.empty(*shape, dtype=torch.bfloat16, device=d)
+        self._recv_shape = shape
+        self._recv = None
         self.out = torch.empty(*shape, dtype=torch.bfloat16, device=d)
         self.counts = torch.zeros(E, dtype=torch.int32, device=d)
         self.src_map = torch.empty(T, K, dtype=torch.int32, device=d)
@@ -495,6 +496,16 @@ class MoeLayerBuffers:
         self.y = torch.empty(T, H, dtype=torch.bfloat16, device=d)
         self.ws_dispatch = _workspace(dispatch_workspace_size(T, K, E), d)
         self.ws_compute = _workspace(ws, d)
+
+    @property
+    def recv(self):
+        """The BF16 receive buffer of the separate path and the per-source slot
+        layout, allocated on first use (the default fused path never forms it:
+        15 GB saved at the large padded layer).  Touch it before capturing a
+        separate-path forward into a CUDA graph."""
+        if self._recv is None:
+            self._recv = torch.empty(*self._recv_shape, dtype=torch.bfloat16, device=self.device)
+        return self._recv
 
     def workspace_layout(self):
         """Byte offsets of the expert compute workspace's parts, from the
