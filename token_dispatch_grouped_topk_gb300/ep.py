@@ -8,7 +8,7 @@ destination rank among its routes, with a header carrying its route list
 experts, and sends every route's output back into that route's result slot at
 the source, which applies the router weight and sums (§3.2, 合对).  Every step of
 a rank's data path is a call of the C library (``include/moe.h``: moe_ep_pack,
-moe_dispatch_ex, moe_expert_compute, moe_ep_route_offsets, moe_ep_return,
+moe_dispatch_quant_ex, moe_gemm_gateup_down, moe_ep_route_offsets, moe_ep_return,
 moe_ep_result_map, moe_combine_packed); the exchanges are the communicator's
 all-to-alls (``TorchDistComm``: torch.distributed, NCCL between GPUs).  The
 split sizes of an all-to-all are host integers, so each layer call reads the
@@ -64,11 +64,12 @@ class CudaEpOps:
                 "route_msg": route_msg, "route_pos": route_pos, "status": status}
 
     def local(self, recv_x, recv_ids, L, R, weights, gemm_launch=None):
-        """The destination's own layer on the received rows: dispatch by the
-        rows' local expert ids, then the expert compute."""
-        recv, counts, src_map, status = api.moe_dispatch(recv_x, recv_ids, None, L, R)
-        out = api.moe_expert_compute(recv, counts, *weights, dev_status=status,
-                                     gemm_launch=gemm_launch)
+        """The destination's own layer on the received rows, on the fused path:
+        dispatch by the rows' local expert ids with the quantisation, then
+        both GEMMs."""
+        xq, xs, counts, src_map, status = api.moe_dispatch_quant(recv_x, recv_ids, None, L, R)
+        out = api.moe_gemm_gateup_down(xq, xs, counts, *weights, dev_status=status,
+                                       gemm_launch=gemm_launch)
         return {"out": out, "src_map": src_map, "counts": counts, "status": status}
 
     def offsets(self, ids):
