@@ -692,7 +692,10 @@ def run_ours(args, rank, local, world):
     nv = float(np.mean(rows_steps))
     na = int(round(np.mean([n_active[(args.warmup + i) % N_ROUTINGS] for i in range(args.steps)])))
     acct = layer_bytes_flops(wl, int(nv), na)
-    fp8_peak = max(fp8["fp8_tflops"], fp8["fp8_tflops_sustained"])
+    # The kernels are timed inside long loops of layer steps, with the GPU at
+    # its power cap, so the FP8 denominator is the sustained cuBLAS rate; the
+    # burst rate and the fraction against it are reported beside it.
+    fp8_peak = fp8["fp8_tflops_sustained"]
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
     tfs = lambda f, ms: f / (ms * 1e-3) / 1e12
     flops = {"gemm_gateup": acct["gemm_gateup_flops"], "gemm_down": acct["gemm_down_flops"],
@@ -733,16 +736,19 @@ def run_ours(args, rank, local, world):
         if t_tensor >= t_hbm:
             ach = kernels[dom]["TFLOP/s"]
             roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
-                    "frac": ach / fp8_peak,
-                    "peak_note": (f"of measured: dense e4m3 cuBLASLt GEMM on this GPU, the larger of burst "
-                                  f"{fp8['fp8_tflops']:.0f} and sustained {fp8['fp8_tflops_sustained']:.0f} "
-                                  f"TFLOP/s; 2 x the measured bf16 burst would be {2 * peaks['bf16_tflops']:.0f}")}
+                    "frac": ach / fp8_peak, "frac_of_burst": ach / fp8["fp8_tflops"],
+                    "peak_note": (f"of measured: dense e4m3 cuBLASLt GEMM on this GPU run back to back "
+                                  f"for 4 s (sustained {fp8['fp8_tflops_sustained']:.0f} TFLOP/s, the "
+                                  f"figure for a kernel timed inside a long loop of steps); its best "
+                                  f"single call (burst) {fp8['fp8_tflops']:.0f}; 2 x the measured bf16 "
+                                  f"burst would be {2 * peaks['bf16_tflops']:.0f}")}
         else:
             ach = kernels[dom]["GB/s"]
             roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": ach / peaks["hbm_gbs"],
                     "peak_note": (f"of {peaks['source']} HBM copy bandwidth; tensor frac "
-                                  f"{kernels[dom]['frac_fp8']:.3f} of the measured fp8 peak {fp8_peak:.0f}")}
+                                  f"{kernels[dom]['frac_fp8']:.3f} of the measured sustained fp8 rate "
+                                  f"{fp8_peak:.0f}")}
         roof["roofline_ms"] = {"tensor": t_tensor * 1e3, "hbm": t_hbm * 1e3}
         roof["algorithmic"] = {"flops_per_launch": flops[dom], "bytes_per_launch": gbytes[dom]}
     else:
