@@ -224,7 +224,9 @@ moe_status moe_combine(const void* out, const int32_t* src_map, const float* top
  *   zq device e4m3 [E, R, I]; zs device fp32 [E, R, I/128].
  * moe_gemm_down -- the same page, §3.6-3.7: out = block-scaled GEMM of zq/zs
  *   with W2, BF16 [E, R, H], rows [0, counts[e]) only.
- * Only rows < counts[e] are read or written in every step.
+ * Only rows < counts[e] are read or written in every step.  Activations must
+ * be finite: a NaN or infinity in a 128-group gives unspecified codes and
+ * scale for that group (never a fault).
  * ------------------------------------------------------------------------- */
 moe_status moe_quantize_fp8(const void* recv, const int32_t* counts, int E, int R, int H,
                             uint8_t* xq, float* xs, moe_stream_t stream);
