@@ -303,6 +303,7 @@ __device__ __forceinline__ void quantize_group(const uint4& v, bool on, uint2* c
 // (64): decode 15.0 -> 12.9 us, prefill 52.9 -> 42.7 us.  The 16-deep form
 // takes 127 registers, which with more blocks than one wave cost more
 // resident warps than the loads gain; kPreload = 0 is the loop over tokens.
+//
 // Dispatch fused with the per-token FP8 quantisation ("SGLang Expert Compute
 // Backend", §4.4: quantise while packing instead of materialising BF16 rows).
 // Every route of a token carries the same row, and the quantisation is per row
