@@ -756,3 +756,35 @@ def test_layer_degenerate_routings(fused):
     assert_rows_close(got, ref, what="one expert's kept rows")
     yk = f32(y)
     assert np.all(yk[np.setdiff1d(np.arange(T), kept)] == 0)
+
+
+@pytest.mark.parametrize("T,E,K,H,I,R", [(50, 1, 1, 384, 128, 64), (90, 40, 32, 640, 256, 80),
+                                         (33, 3, 2, 128, 384, 16)])
+def test_layer_paths_odd_shapes(T, E, K, H, I, R):
+    """The fused and separate layer paths on shapes off the benchmarked grid:
+    one expert with top-1, top-32 of 40 experts, H % 256 = 128 (128-column
+    down tiles), H = 128 (one K group), a single gate/up tile per block; y
+    the same bytes on both paths and every kept route against the oracle."""
+    dev = torch.device(DEV)
+    g = torch.Generator().manual_seed(T + E + K)
+    idx = torch.stack([torch.randperm(E, generator=g)[:K] for _ in range(T)])
+    idx[0, 0] = -1
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16).to(DEV)
+    w = torch.rand(T, K, generator=g).to(DEV)
+    w13, s13, w2, s2 = (t.to(DEV) for t in W.expert_weights(E, H, I, T, "cpu"))
+    buf = api.MoeLayerBuffers(T, E, K, H, I, R, dev)
+    y_sep = buf.forward(x, idx.to(DEV), w, w13, s13, w2, s2, fused=False).clone()
+    y = buf.forward(x, idx.to(DEV), w, w13, s13, w2, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_sep.view(torch.int16))
+    rr = O.route(idx.numpy(), E, R)
+    assert np.array_equal(buf.src_map.cpu().numpy(), rr.src_map)
+    wts = host_weights({"w13": w13, "s13": s13, "w2": w2, "s2": s2}, range(E))
+    src = rr.src_map
+    for e in range(E):
+        tk = np.argwhere((idx.numpy() == e) & (src >= 0))
+        if len(tk) == 0:
+            continue
+        ref = oracle_expert_rows(f32(x[torch.from_numpy(tk[:, 0]).to(DEV)]), wts[e])
+        got = f32(buf.out.view(-1, H)[torch.from_numpy(src[tk[:, 0], tk[:, 1]]).long().to(DEV)])
+        assert_rows_close(got, ref, what=f"expert {e}")
