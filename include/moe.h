@@ -337,8 +337,10 @@ moe_status moe_combine_packed(const void* out, int64_t rows, const int32_t* src_
  * No workspace: each source rank's slots are computed by its own blocks.
  *
  * moe_expert_compute_source_slots -- moe_expert_compute on that layout: the
- *   tiles of expert e cover its rows up to its last valid row, the gaps
- *   between source ranges are skipped by quantisation and never stored.
+ *   quantisation packs expert e's valid rows together (in slot order, inside
+ *   the workspace), so the GEMM tiles cover valid rows only (the page's masked
+ *   expert compute); the down GEMM stores each row at its slot, and the rows
+ *   between source ranges are never written.
  *   recv/out device BF16 [E, W*max_tokens, H]; counts may be NULL (not read);
  *   seg_counts from moe_dispatch_source_slots; workspace of
  *   moe_expert_compute_workspace_size(E, W*max_tokens, H, I) bytes; flags as

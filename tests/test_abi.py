@@ -56,10 +56,11 @@ def test_workspace_sizes(lib):
     assert lib.moe_dispatch_workspace_size(big, 1, 4) == -(-big // 256) * 4 * 4
     ws = lib.moe_expert_compute_workspace_size(2, 128, 256, 128)
     # xq, xs, zq, zs, then the fused GEMM's scratch: a tile ticket and one
-    # count per 128-row block (ceil(rows/128) plus one per possible expert)
+    # count per 128-row block (ceil(rows/128) plus one per possible expert),
+    # then the per-source layout's slot row of every packed row (int32)
     sync = (1 + 2 + 1024) * 4
     assert ws == 2 * 128 * 256 + 2 * 2 * 128 * 4 + 2 * 128 * 128 + 2 * 1 * 128 * 4 + \
-        (sync + 255) // 256 * 256
+        (sync + 255) // 256 * 256 + 2 * 128 * 4
     assert lib.moe_expert_compute_workspace_size(2, 128, 200, 128) == 0   # H % 128 != 0
 
 
@@ -147,11 +148,12 @@ def test_packed_entry_points_reject_on_host(lib):
                                    FAKE, FAKE, 8, None) == -3          # workspace checked next
     assert lib.moe_dispatch_packed(FAKE, FAKE, None, 112, 200, 2, 8, 128, 224, FAKE, FAKE, FAKE,
                                    FAKE, FAKE, ws, None) == -1         # H % 128
-    # packed compute: workspace sized by rows (xq, xs, zq, zs, each 256-byte aligned)
+    # packed compute: workspace sized by rows (xq, xs, zq, zs, the GEMM scratch
+    # and the slot table, each 256-byte aligned)
     al = lambda v: (v + 255) // 256 * 256
     ws82 = lib.moe_expert_compute_packed_workspace_size(82, 256, 128)
-    assert ws82 == al(al(al(al(al(82 * 256) + 82 * 2 * 4) + 82 * 128) + 82 * 1 * 4) +
-                      (1 + 1 + 1024) * 4)
+    assert ws82 == al(al(al(al(al(al(82 * 256) + 82 * 2 * 4) + 82 * 128) + 82 * 1 * 4) +
+                         (1 + 1 + 1024) * 4) + 82 * 4)
     assert lib.moe_expert_compute_packed_workspace_size(2 * 128, 256, 128) == \
         lib.moe_expert_compute_workspace_size(2, 128, 256, 128)
     assert lib.moe_expert_compute_packed_workspace_size(0, 256, 128) == 0

@@ -246,28 +246,19 @@ __device__ __forceinline__ void expert_prefix(const int32_t* counts, int E, int 
   __syncthreads();
 }
 
-// Per-source fixed slots: s_ext[e] = one past expert e's last valid row
-// (segment r holds rows [r*seg, r*seg + seg_counts[e*W + r]) valid), so the
-// rows [0, s_ext[e]) cover every valid row.  Every thread of the block calls
-// it; ends with __syncthreads().
-__device__ __forceinline__ void source_slot_extents(const int32_t* seg_counts, int E, int R,
-                                                    int seg, int* s_ext) {
+// Per-source layout: valid rows of each expert, the sum over its source
+// ranges of min(seg_counts, seg) -- the packed rows its GEMM tiles cover.
+// Every thread of the block calls it; ends with __syncthreads().
+__device__ __forceinline__ void source_slot_totals(const int32_t* seg_counts, int E, int R,
+                                                   int seg, int* s_tot) {
   const int W = R / seg;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int ext = 0;
-    for (int r = 0; r < W; ++r) {
-      const int c = min(max(seg_counts[static_cast<size_t>(e) * W + r], 0), seg);
-      if (c > 0) ext = r * seg + c;
-    }
-    s_ext[e] = ext;
+    int tot = 0;
+    for (int r = 0; r < W; ++r)
+      tot += min(max(seg_counts[static_cast<size_t>(e) * W + r], 0), seg);
+    s_tot[e] = tot;
   }
   __syncthreads();
-}
-
-// Whether row m (within expert e) of a per-source layout holds a route.
-__device__ __forceinline__ bool source_slot_valid(const int32_t* seg_counts, int R, int seg, int e,
-                                                  int m) {
-  return (m % seg) < __ldg(seg_counts + static_cast<size_t>(e) * (R / seg) + m / seg);
 }
 
 // Largest e in [0, E) with s_start[e] <= x (s_start non-decreasing, s_start[0] = 0).

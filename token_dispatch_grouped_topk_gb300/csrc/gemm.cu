@@ -111,6 +111,7 @@ struct GemmArgs {
   long long rows;          // their row count
   int seg;                 // per-source slots: rows per source range (0: none)
   const int32_t* seg_counts;  // [E, R / seg] valid rows per range
+  const int32_t* slot_of;  // per-source slots: slot row of each packed row (down stores)
   int32_t* dev_status;
 };
 
@@ -338,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Block prefix per expert (ends with __syncthreads, which also publishes the
   // barrier initialisation and the TMEM address).
-  // per-source slots: each expert's tiles cover its rows up to its last valid one
-  if (args.seg) source_slot_extents(args.seg_counts, args.E, args.R, args.seg, ctl->cnt);
+  // per-source slots: each expert's tiles cover its packed valid rows
+  if (args.seg) source_slot_totals(args.seg_counts, args.E, args.R, args.seg, ctl->cnt);
   expert_prefix(args.seg ? ctl->cnt : args.counts, args.E, args.R, kBM, 1, ctl->blk_start,
                 ctl->cnt);
   if (args.packed) expert_prefix(args.counts, args.E, args.R, 1, 1, ctl->cnt, nullptr);
@@ -573,11 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         nxt.t = t_next;
         if (t_next >= 0) epi_prepare<BN, kMode>(&nxt, ctl, args, row, ch);
       }
-      // rows stored: inside the tile's valid range and the buffer, and (per-source
-      // slots) a row that holds a route; bit r of vmask is the warp's row r
-      const bool valid = row < tl.rows && grow < args.rows &&
-                         (!args.seg || source_slot_valid(args.seg_counts, args.R, args.seg, tl.e,
-                                                         tl.m_blk * kBM + row));
+      // rows stored: inside the tile's valid range and the buffer; bit r of
+      // vmask is the warp's row r
+      const bool valid = row < tl.rows && grow < args.rows;
       const unsigned vmask = __ballot_sync(0xffffffffu, valid);
       if (kMode != kModeDown && tl.gu) {
         // Z = SiLU(gate) * up on this thread's 64 columns (written over the
@@ -679,6 +678,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t goff = static_cast<uint32_t>((lane >> 2) * args.H + 8 * c);
         const uint32_t sidx = static_cast<uint32_t>((lane >> 2) * kStageRowBytes + 16 * c);
         const uint32_t gstep = static_cast<uint32_t>(8 * args.H);
+        // per-source slots: packed row -> its slot row, as an offset from the
+        // packed row of this lane's store rows 8i + lane/4
+        long long soff[4] = {0, 0, 0, 0};
+        if (args.seg) {
+          const long long mine = valid ? static_cast<long long>(args.slot_of[grow]) -
+                                             (static_cast<long long>(tl.m_blk) * kBM + row)
+                                       : 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            soff[i] = __shfl_sync(0xffffffffu, mine, 8 * i + (lane >> 2)) * args.H;
+        }
 #pragma unroll
         for (int r = 0; r < kCols / 32; ++r) {
           uint4* srow = reinterpret_cast<uint4*>(stage + lane * kStageRowBytes);
@@ -697,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 4; ++i) {
             if ((vmask >> (8 * i + (lane >> 2))) & 1u) {
               const uint4 v = *reinterpret_cast<const uint4*>(stage + sidx + i * 8 * kStageRowBytes);
-              *reinterpret_cast<uint4*>(gbase + goff + i * gstep + 32 * r) = v;
+              *reinterpret_cast<uint4*>(gbase + soff[i] + goff + i * gstep + 32 * r) = v;
             }
           }
           __syncwarp();
@@ -814,6 +824,7 @@ GemmArgs common_args(const int32_t* counts, int E, RowLayout rl, int H, int I,
   a.rows = rl.rows;
   a.seg = rl.seg;
   a.seg_counts = rl.seg_counts;
+  a.slot_of = rl.slot_of;
   a.dev_status = dev_status;
   return a;
 }

@@ -33,10 +33,16 @@ struct RowLayout {
   int64_t rows;
   int seg = 0;                          // rows per source range, 0: not segmented
   const int32_t* seg_counts = nullptr;  // [E, R / seg] valid rows per range
+  // Segmented: the quantisation packs each expert's valid rows to the front
+  // of its range of xq/xs (row j of expert e at e*R + j) and records their
+  // slot rows in slot_of[e*R + j]; the GEMMs run on the packed rows and the
+  // down GEMM stores row j at its slot row e*R + slot_of[e*R + j].
+  int32_t* slot_of = nullptr;
 };
 inline RowLayout padded_rows(int E, int R) { return RowLayout{R, 0, static_cast<int64_t>(E) * R}; }
-inline RowLayout source_slot_rows(int E, int R, int seg, const int32_t* seg_counts) {
-  return RowLayout{R, 0, static_cast<int64_t>(E) * R, seg, seg_counts};
+inline RowLayout source_slot_rows(int E, int R, int seg, const int32_t* seg_counts,
+                                  int32_t* slot_of) {
+  return RowLayout{R, 0, static_cast<int64_t>(E) * R, seg, seg_counts, slot_of};
 }
 
 // ----- dispatch (route validation, histogram, scan, stable scatter)

@@ -59,7 +59,7 @@ bool valid_experts(int E, int R) {
 }
 
 struct ComputeWorkspace {
-  size_t xq, xs, zq, zs, sync, sync_ints, total;
+  size_t xq, xs, zq, zs, sync, sync_ints, slot, total;
 };
 
 bool valid_rows(int64_t rows) { return rows >= 1 && rows <= (int64_t{1} << 30); }
@@ -83,6 +83,9 @@ ComputeWorkspace compute_workspace_rows(int64_t rows_i, int H, int I) {
   w.sync = off;
   w.sync_ints = 1 + (rows + 127) / 128 + 1024;
   off = align_up(off + w.sync_ints * sizeof(int), 256);
+  // Per-source slot layout: the slot row of each packed row (int32 per row).
+  w.slot = off;
+  off = align_up(off + rows * sizeof(int32_t), 256);
   w.total = off;
   return w;
 }
@@ -272,7 +275,9 @@ moe_status moe_expert_compute_source_slots(const void* recv, const int32_t* coun
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
   // the tile list and the stored rows come from seg_counts; counts is not read
-  return expert_compute_impl(recv, seg_counts, E, source_slot_rows(E, R, max_tokens, seg_counts),
+  int32_t* slot_of = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + w.slot);
+  return expert_compute_impl(recv, seg_counts, E,
+                             source_slot_rows(E, R, max_tokens, seg_counts, slot_of),
                              H, I, w13, w13_scale, w2, w2_scale, out, dev_status, workspace, w,
                              dev->sm_count, reinterpret_cast<cudaStream_t>(stream), flags);
 }

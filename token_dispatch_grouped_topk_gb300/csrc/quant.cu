@@ -34,19 +34,43 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
   int* s_start = smem;               // [E + 1] prefix of row blocks
   int* s_cnt = smem + E + 1;         // [E]
   int* s_rows = smem + 2 * E + 1;    // [E + 1] packed row bases
+  const int G = H / kGroup;
   float* s_scale = reinterpret_cast<float*>(smem + 3 * E + 2);  // [G][kRowsPerBlock]
+  int* s_rp = reinterpret_cast<int*>(s_scale + G * kRowsPerBlock);  // per-source: [W + 1]
   const int R = rl.R;
-  // per-source slots: rows up to each expert's last valid row, gaps skipped
-  if (rl.seg) source_slot_extents(rl.seg_counts, E, R, rl.seg, s_cnt);
+  // Per-source slots: expert e's valid rows are packed to rows [0, c_e) of its
+  // range of xq/xs, in slot order; s_rp holds the current expert's prefix of
+  // valid rows over its source ranges.
+  const int W = rl.seg ? R / rl.seg : 0;
+  if (rl.seg) source_slot_totals(rl.seg_counts, E, R, rl.seg, s_cnt);
   expert_prefix(rl.seg ? s_cnt : counts, E, R, kRowsPerBlock, 1, s_start, s_cnt);
   if (rl.packed) expert_prefix(counts, E, R, 1, 1, s_rows, nullptr);
-  const int G = H / kGroup;
   const int nvec = H / 8;
   const int total = s_start[E];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
+  int rp_e = -1;
   for (int b = blockIdx.x; b < total; b += gridDim.x) {
     const int e = find_expert(s_start, E, b);
+    if (rl.seg && e != rp_e) {   // the same for the whole block
+      if (warp == 0) {
+        int carry = 0;
+        if (lane == 0) s_rp[0] = 0;
+        for (int r0 = 0; r0 < W; r0 += 32) {
+          const int r = r0 + lane;
+          int v = r < W ? min(max(rl.seg_counts[static_cast<size_t>(e) * W + r], 0), rl.seg) : 0;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+          }
+          if (r < W) s_rp[r + 1] = carry + v;
+          carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+      }
+      __syncthreads();
+      rp_e = e;
+    }
     const int row0 = (b - s_start[e]) * kRowsPerBlock;
     const int64_t base = (rl.packed ? static_cast<int64_t>(s_rows[e]) : static_cast<int64_t>(e) * R) + row0;
     // rows of the block: valid rows of e, and never past the buffer
@@ -54,9 +78,21 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
         min(static_cast<int64_t>(min(kRowsPerBlock, s_cnt[e] - row0)), rl.rows - base));
     if (nrows <= 0) continue;
     for (int r = warp; r < nrows; r += kQuantWarps) {
-      if (rl.seg && !source_slot_valid(rl.seg_counts, R, rl.seg, e, row0 + r)) continue;
       const size_t row = static_cast<size_t>(base) + r;
-      const uint4* src = recv + row * nvec;
+      size_t src_row = row;
+      if (rl.seg) {
+        // packed row j of e comes from source range q: s_rp[q] <= j < s_rp[q + 1]
+        const int j = row0 + r;
+        int lo = 0, hi = W - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_rp[mid] <= j) lo = mid; else hi = mid - 1;
+        }
+        const int slot = lo * rl.seg + (j - s_rp[lo]);
+        src_row = static_cast<size_t>(e) * R + slot;
+        if (lane == 0) rl.slot_of[row] = slot;
+      }
+      const uint4* src = recv + src_row * nvec;
       uint2* dst = xq + row * (H / 8);
       // Four pairs of groups per pass: every lane has four 16-byte loads in
       // flight before the reductions.  (Sixteen per pass, a 4096-wide row in
@@ -117,7 +153,8 @@ cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, RowL
                             uint8_t* xq, float* xs, int sm_count, cudaStream_t s) {
   const int R = rl.R;
   const int G = H / kGroup;
-  const size_t smem = (3 * E + 2) * sizeof(int) + G * kRowsPerBlock * sizeof(float);
+  const size_t smem = (3 * E + 2) * sizeof(int) + G * kRowsPerBlock * sizeof(float) +
+                      (rl.seg ? (R / rl.seg + 1) * sizeof(int) : 0);
   // Upper bound of row blocks; the kernel walks the true count read from device memory.
   const long long max_blocks = static_cast<long long>(E) * ((R + kRowsPerBlock - 1) / kRowsPerBlock);
   const int grid = static_cast<int>(std::min<long long>(max_blocks, sm_count * 8LL));
