@@ -552,7 +552,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < kCols / 64; ++j) {
           const uint32_t col = j ? cur.col1 : cur.col0;
           const uint64_t sx2 = (tl.gu && j) ? s1x2 : s0x2;
-          tmem_load64_sync(base + col, buf);
+          if constexpr (kMode == kModeDown)
+            tmem_load64_sync_2x32(base + col, buf);
+          else
+            tmem_load64_sync(base + col, buf);
 #pragma unroll
           for (int i = 0; i < 32; ++i) ffma2_acc(acc2[32 * j + i], sx2, buf[2 * i], buf[2 * i + 1]);
         }
