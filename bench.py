@@ -561,18 +561,34 @@ def run_ours(args, rank, local, world):
     if wl.W * mt <= R:
         sbuf = api.MoeLayerBuffers(T, E, K, H, I, wl.W * mt, dev, source_slots=mt, L=wl.L,
                                    rank_offsets=rank_offsets)
+        sbuf.slots_fp8  # formed outside the capture
         sgraphs = capture(lambda r: sbuf.forward(x, *routings[r], w13, s13, w2, s2), N_ROUTINGS)
         ss_ms = graph_ms(sgraphs, args.steps, stream, args.warmup, world, dev)
+        del sgraphs
+        sbuf.recv  # the separate path's BF16 slots, formed before its capture
+        sgraphs = capture(lambda r: sbuf.forward(x, *routings[r], w13, s13, w2, s2, fused=False),
+                          N_ROUTINGS)
+        ss_sep_ms = graph_ms(sgraphs, args.steps, stream, args.warmup, world, dev)
         ss_rows = []
         for r in range(N_ROUTINGS):
             sbuf.forward(x, *routings[r], w13, s13, w2, s2)
             ss_rows.append(int(sbuf.counts.sum().item()))
         ss_total = reduce_sum(float(sum(ss_rows[(args.warmup + i) % N_ROUTINGS] for i in range(args.steps))),
                               world, dev)
+        common = sum(t.numel() * t.element_size() for t in (sbuf.out, sbuf.ws_compute, sbuf.ws_dispatch,
+                                                            sbuf.counts, sbuf.seg_counts, sbuf.src_map,
+                                                            sbuf.y))
         source_slots = {"value": ss_total / (ss_ms / 1e3), "unit": UNIT, "ms_per_step": ss_ms / args.steps,
-                        "max_tokens": mt, "rows_per_expert": wl.W * mt, "lane_bytes": lane_bytes(sbuf),
-                        "note": "moe_dispatch_source_slots / moe_expert_compute_source_slots / moe_combine: "
-                                "each source rank owns max_tokens slots in every expert (CUDA-graph replay)"}
+                        "separate_value": ss_total / (ss_sep_ms / 1e3),
+                        "separate_ms_per_step": ss_sep_ms / args.steps,
+                        "max_tokens": mt, "rows_per_expert": wl.W * mt,
+                        "lane_bytes": int(common + sum(t.numel() * t.element_size() for t in sbuf.slots_fp8)),
+                        "separate_lane_bytes": int(common + sbuf.recv.numel() * sbuf.recv.element_size()),
+                        "note": "MoeLayerBuffers(source_slots).forward: moe_dispatch_quant_source_slots "
+                                "(FP8 slots) / moe_gemm_source_slots / moe_combine; separate_*: "
+                                "forward(fused=False), moe_dispatch_source_slots (BF16 slots) / "
+                                "moe_expert_compute_source_slots / moe_combine. Each source rank owns "
+                                "max_tokens slots in every expert (CUDA-graph replay)"}
         del sgraphs, sbuf
         torch.cuda.empty_cache()
     else:

@@ -347,6 +347,21 @@ moe_status moe_combine_packed(const void* out, int64_t rows, const int32_t* src_
  *   for moe_expert_compute_ex.  Output rows equal those of the padded layout
  *   for the same routes, bit for bit.  Combine with moe_combine(out, src_map,
  *   topk_w, T, H, K, E, W*max_tokens, y).
+ *
+ * The same layout with the quantisation fused into the dispatch ("SGLang
+ * Expert Compute Backend", §4.4), as moe_dispatch_quant_ex does for the padded
+ * and packed layouts:
+ * moe_dispatch_quant_source_slots -- the slots, counts, seg_counts, src_map and
+ *   status of moe_dispatch_source_slots; each token row is quantised once (the
+ *   rule of moe_quantize_fp8) and its codes and scales are written to every
+ *   kept slot: xq device e4m3 [E, W*max_tokens, H] (8-byte aligned), xs device
+ *   fp32 [E, W*max_tokens, H/128]; other rows untouched.
+ * moe_gemm_source_slots -- both GEMMs on those slots: each expert's valid rows
+ *   are packed inside the workspace (no quantisation: the codes and scales are
+ *   copied), then the GEMMs of moe_expert_compute_source_slots run with the
+ *   same workspace size, flags and output.  Outputs equal
+ *   moe_expert_compute_source_slots' on the BF16 slots of the same routes, bit
+ *   for bit.
  * ------------------------------------------------------------------------- */
 moe_status moe_dispatch_source_slots(const void* x, const void* topk_idx, int idx_bits,
                                      const float* topk_w, int T, int H, int K, int E, int L,
@@ -360,6 +375,18 @@ moe_status moe_expert_compute_source_slots(const void* recv, const int32_t* coun
                                            const float* w2_scale, void* out, int32_t* dev_status,
                                            void* workspace, size_t workspace_bytes, int flags,
                                            moe_stream_t stream);
+moe_status moe_dispatch_quant_source_slots(const void* x, const void* topk_idx, int idx_bits,
+                                           const float* topk_w, int T, int H, int K, int E,
+                                           int L, int max_tokens, const int32_t* rank_offsets,
+                                           uint8_t* xq, float* xs, int32_t* counts,
+                                           int32_t* seg_counts, int32_t* src_map,
+                                           int32_t* dev_status, moe_stream_t stream);
+moe_status moe_gemm_source_slots(const uint8_t* xq, const float* xs, const int32_t* seg_counts,
+                                 int E, int L, int max_tokens, int H, int I, const uint8_t* w13,
+                                 const float* w13_scale, const uint8_t* w2,
+                                 const float* w2_scale, void* out, int32_t* dev_status,
+                                 void* workspace, size_t workspace_bytes, int flags,
+                                 moe_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * moe_dispatch_ex -- the general dispatch: moe_dispatch and moe_dispatch_packed

@@ -219,17 +219,49 @@ def test_header_compiles_as_c(tmp_path):
                     "-o", str(tmp_path / "layer_main.o")], check=True)
 
 
-def test_layer_forward_path_choice_on_host():
+def test_layer_forward_path_choice_on_host(monkeypatch):
     """MoeLayerBuffers.forward takes the fused dispatch+quant path unless asked
-    not to, and refuses it on the per-source slot layout before any call (the
-    lane is built in host memory: nothing reaches the library)."""
+    not to, on every layout, and calls the matching entry points in order (the
+    lane is built in host memory and the entry points are recorded, so nothing
+    reaches a GPU)."""
     from token_dispatch_grouped_topk_gb300 import api
+    names = ["moe_dispatch", "moe_expert_compute", "moe_combine", "moe_dispatch_quant",
+             "moe_gemm_gateup_down", "moe_dispatch_packed", "moe_expert_compute_packed",
+             "moe_combine_packed", "moe_dispatch_source_slots",
+             "moe_expert_compute_source_slots", "moe_dispatch_quant_source_slots",
+             "moe_gemm_source_slots"]
+    calls = []
+    for n in names:
+        monkeypatch.setattr(api, n, lambda *a, _n=n, **k: calls.append(_n))
     T, E, K, H, I, L, mt = 8, 4, 2, 128, 128, 2, 4
-    lane = api.MoeLayerBuffers(T, E, K, H, I, (E // L) * mt, torch.device("cpu"), source_slots=mt, L=L)
+    cpu = torch.device("cpu")
     x = torch.zeros(T, H, dtype=torch.bfloat16)
     idx = torch.zeros(T, K, dtype=torch.int64)
     w = torch.zeros(T, K)
-    with pytest.raises(ValueError):
-        lane.forward(x, idx, w, None, None, None, None, fused=True)
-    with pytest.raises(ValueError):
+    lanes = {
+        "padded": (api.MoeLayerBuffers(T, E, K, H, I, 8, cpu),
+                   ["moe_dispatch_quant", "moe_gemm_gateup_down", "moe_combine"],
+                   ["moe_dispatch", "moe_expert_compute", "moe_combine"]),
+        "packed": (api.MoeLayerBuffers(T, E, K, H, I, 8, cpu, packed=True),
+                   ["moe_dispatch_quant", "moe_gemm_gateup_down", "moe_combine_packed"],
+                   ["moe_dispatch_packed", "moe_expert_compute_packed", "moe_combine_packed"]),
+        "source_slots": (api.MoeLayerBuffers(T, E, K, H, I, (E // L) * mt, cpu, source_slots=mt,
+                                             L=L),
+                         ["moe_dispatch_quant_source_slots", "moe_gemm_source_slots",
+                          "moe_combine"],
+                         ["moe_dispatch_source_slots", "moe_expert_compute_source_slots",
+                          "moe_combine"]),
+    }
+    for name, (lane, fused, separate) in lanes.items():
+        for kw, want in (({}, fused), ({"fused": True}, fused), ({"fused": False}, separate)):
+            calls.clear()
+            lane.forward(x, idx, w, None, None, None, None, **kw)
+            assert calls == want, (name, kw, calls)
+        calls.clear()
         lane.forward_fused(x, idx, w, None, None, None, None)
+        assert calls == fused, name
+    # the per-source lane forms its FP8 slots only on the fused path
+    lane = lanes["source_slots"][0]
+    xq, xs = lane.slots_fp8
+    assert xq.shape == (E, (E // L) * mt, H) and xq.dtype == torch.uint8
+    assert xs.shape == (E, (E // L) * mt, H // 128) and xs.dtype == torch.float32

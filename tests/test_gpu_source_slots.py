@@ -1,11 +1,13 @@
 """The per-source fixed-slot receive layout ("DeepEP 架构与实现笔记", §9.5)
-through moe_dispatch_source_slots and moe_expert_compute_source_slots.
+through moe_dispatch_source_slots / moe_expert_compute_source_slots (BF16
+slots) and moe_dispatch_quant_source_slots / moe_gemm_source_slots (FP8 slots).
 
 Dispatch bit-exact against the oracle's route_source_slots (source map,
-per-expert and per-(expert, source) counts, drops, bad ids, payload rows);
-expert outputs and the layer output bit-identical to the padded layout on the
-same routes (a row's arithmetic does not depend on where the row sits); rows
-between the source ranges never written."""
+per-expert and per-(expert, source) counts, drops, bad ids, payload rows), the
+FP8 slots against the oracle's quantisation of each token row; expert outputs
+and the layer output bit-identical to the padded layout on the same routes (a
+row's arithmetic does not depend on where the row sits) and between the BF16
+and FP8 slot paths; rows between the source ranges never written."""
 import numpy as np
 import pytest
 import torch
@@ -65,6 +67,49 @@ def _check_dispatch(x, idx, E, L, mt, offsets=None):
     return res, recv, counts, seg, src
 
 
+def _check_dispatch_fp8(x, idx, E, L, mt, offsets=None, max_tokens=512):
+    """moe_dispatch_quant_source_slots: routing outputs equal to the BF16 slot
+    dispatch's (itself checked against the oracle); each kept slot holds the
+    oracle's e4m3 codes and scales of its token row; other rows untouched."""
+    T, H = x.shape
+    G = H // 128
+    Wr = E // L
+    res, recv, counts, seg, src = _check_dispatch(x, idx, E, L, mt, offsets)
+    off_d = None if offsets is None else torch.tensor(offsets, dtype=torch.int32, device=DEV)
+    xq = torch.full((E, Wr * mt, H), 0x5A, dtype=torch.uint8, device=DEV)
+    xs = torch.full((E, Wr * mt, G), -3.0, dtype=torch.float32, device=DEV)
+    xq, xs, c8, seg8, src8, st8 = api.moe_dispatch_quant_source_slots(
+        x.to(DEV), idx.to(DEV), None, E, L, mt, rank_offsets=off_d, xq=xq, xs=xs)
+    torch.cuda.synchronize()
+    assert torch.equal(c8, counts) and torch.equal(seg8, seg) and torch.equal(src8, src)
+    stv = st8.cpu().tolist()
+    assert stv[1] == res.dropped
+    assert bool(stv[0] & api.DEV_CAPACITY_DROPPED) == (res.dropped > 0)
+    assert bool(stv[0] & api.DEV_BAD_EXPERT_ID) == res.bad_id
+    q_rows, s_rows = xq.view(-1, H), xs.view(-1, G)
+    keep = res.src_map >= 0
+    slots = torch.from_numpy(res.src_map[keep]).long().to(DEV)
+    tok = np.nonzero(keep)[0]
+    written = torch.zeros(q_rows.shape[0], dtype=torch.bool, device=DEV)
+    written[slots] = True
+    assert bool((q_rows[~written] == 0x5A).all()) and bool((s_rows[~written] == -3.0).all())
+    # every slot of a token holds the same codes; the oracle's on a sample of tokens
+    first = {}
+    for t, sl in zip(tok.tolist(), res.src_map[keep].tolist()):
+        first.setdefault(t, sl)
+    firsts = torch.tensor([first[t] for t in tok.tolist()], dtype=torch.long, device=DEV)
+    assert torch.equal(q_rows[slots], q_rows[firsts]) and torch.equal(s_rows[slots], s_rows[firsts])
+    has = np.array(sorted(first))
+    if len(has) > max_tokens:
+        has = np.sort(np.random.default_rng(0).choice(has, max_tokens, replace=False))
+    if len(has):
+        codes, scales = O.quantize_rows(x[torch.from_numpy(has)].float().cpu().numpy())
+        rows = torch.tensor([first[t] for t in has.tolist()], dtype=torch.long, device=DEV)
+        assert np.array_equal(q_rows[rows].cpu().numpy(), codes)
+        assert np.array_equal(s_rows[rows].cpu().numpy(), scales)
+    return res, xq, xs, seg, src, recv
+
+
 @pytest.mark.parametrize("bits", [64, 32])
 def test_dispatch_random_with_drops_and_empty_ranks(bits):
     E, L, K, mt, H = 40, 5, 4, 3, 256
@@ -84,6 +129,32 @@ def test_dispatch_random_with_drops_and_empty_ranks(bits):
     assert res2.dropped > 0
 
 
+@pytest.mark.parametrize("bits", [64, 32])
+@pytest.mark.parametrize("E,L,K,mt,H,T", [(40, 5, 4, 3, 256, 150), (12, 3, 4, 50, 1152, 300),
+                                          (256, 8, 8, 32, 7168, 256), (16, 16, 2, 7, 128, 1),
+                                          (8, 2, 3, 5, 384, 0)])
+def test_dispatch_quant_source_slots(bits, E, L, K, mt, H, T):
+    """FP8 slots: drops, an invalid id, ranks that send nothing, one group per
+    row, a ragged last pass of groups (9 groups), the decode layer's shape, one
+    token and no tokens."""
+    Wr = E // L
+    g = torch.Generator().manual_seed(E + H + T + bits)
+    idx = torch.randint(-1, E, (T, K), generator=g)
+    if T > 1:
+        idx[:, 0] = torch.randint(0, 3, (T,), generator=g)
+        idx[T // 2, K - 1] = E + 5
+    x = (torch.randn(T, H, generator=g) * 3).to(torch.bfloat16)
+    if T > 2:
+        x[1, :128] = 0                                    # an all-zero group
+    offsets = None
+    if T >= Wr:
+        cuts = np.sort(np.random.default_rng(T).integers(0, T + 1, Wr - 1))
+        offsets = [0] + cuts.tolist() + [T]
+    ids = idx.to(torch.int32) if bits == 32 else idx
+    _check_dispatch_fp8(x, ids, E, L, mt, offsets)
+    _check_dispatch_fp8(x, ids, E, L, mt, None)
+
+
 def test_dispatch_traced_scenario_pins():
     """Traced scenario with the pages' per-rank slot count C = 64: E0 gets 16,
     31 and 64 rows in the ranges of source ranks 1, 2 and 3."""
@@ -99,10 +170,11 @@ def test_dispatch_traced_scenario_pins():
 
 @pytest.mark.parametrize("name,mt", [("decode", 32), ("traced", 64)])
 def test_layer_source_slots_equals_padded(name, mt):
-    """Whole layer on the per-source layout: every kept route's expert output
-    and y bit-identical to the padded layout's, out rows between the source
-    ranges untouched.  Decode: 8 ranks x 32 tokens, so W * max_tokens = 256 =
-    the decode capacity and nothing is dropped."""
+    """Whole layer on the per-source layout, on its default path (FP8 slots)
+    and on the BF16 slots: every kept route's expert output and y
+    bit-identical to the padded layout's and between the two paths, out rows
+    between the source ranges untouched.  Decode: 8 ranks x 32 tokens, so
+    W * max_tokens = 256 = the decode capacity and nothing is dropped."""
     d = W.make_layer_inputs(name, seed=1, device=DEV)
     wl = d["wl"]
     dev = torch.device(DEV)
@@ -117,8 +189,14 @@ def test_layer_source_slots_equals_padded(name, mt):
     pad = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, Wr * mt, dev)
     args = (d["x"], d["topk_idx"], d["topk_w"], d["w13"], d["s13"], d["w2"], d["s2"])
     y_ss = ss.forward(*args).clone()
+    out_fused = ss.out.clone()
+    assert ss._recv is None, "the default path formed the BF16 slots"
+    ss.out.fill_(7.0)
+    y_sep = ss.forward(*args, fused=False).clone()
     y_pad = pad.forward(*args).clone()
     torch.cuda.synchronize()
+    assert torch.equal(_bits(y_sep), _bits(y_ss))
+    assert torch.equal(_bits(ss.out), _bits(out_fused))
     assert ss.dev_status.cpu().tolist() == pad.dev_status.cpu().tolist() == [0, 0]
     assert torch.equal(ss.counts, pad.counts)
     sm_ss, sm_pad = ss.src_map.cpu().numpy(), pad.src_map.cpu().numpy()
@@ -136,7 +214,8 @@ def test_layer_source_slots_equals_padded(name, mt):
 
 def test_expert_compute_source_slots_both_launch_forms():
     """The per-source layout's expert compute, one launch and two launches,
-    with blocks that hold only gaps and ranges cut short by drops."""
+    with blocks that hold only gaps and ranges cut short by drops; the GEMMs on
+    the FP8 slots (moe_gemm_source_slots) give the same output, bit for bit."""
     E, L, K, mt, H, I, T = 12, 3, 4, 50, 512, 256, 300
     g = torch.Generator().manual_seed(17)
     idx = torch.randint(-1, E, (T, K), generator=g)
@@ -154,6 +233,16 @@ def test_expert_compute_source_slots_both_launch_forms():
         assert st.cpu().tolist() == [0, 0]
         outs.append(out)
     assert torch.equal(_bits(outs[0]), _bits(outs[1]))
+    _, xq, xs, seg8, _, _ = _check_dispatch_fp8(x, idx, E, L, mt)
+    assert torch.equal(seg8, seg)
+    for form in ("one", "two"):
+        out = torch.full_like(recv, 9.0)
+        st = torch.zeros(2, dtype=torch.int32, device=DEV)
+        api.moe_gemm_source_slots(xq, xs, seg8, L, mt, w13, s13, w2, s2, out=out, dev_status=st,
+                                  gemm_launch=form)
+        torch.cuda.synchronize()
+        assert st.cpu().tolist() == [0, 0]
+        assert torch.equal(_bits(out), _bits(outs[0])), form
     keep = res.src_map >= 0
     flat = outs[0].view(-1, H)
     q = torch.from_numpy(res.src_map[keep]).long().to(DEV)

@@ -38,6 +38,13 @@ SIGNATURES = {
                                                 c_int, c_int, c_void_p, c_void_p, c_void_p,
                                                 c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
                                                 c_int, c_void_p]),
+    "moe_dispatch_quant_source_slots": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int,
+                                                c_int, c_int, c_int, c_int, c_void_p, c_void_p,
+                                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                c_void_p]),
+    "moe_gemm_source_slots": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                      c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                      c_void_p, c_void_p, c_size_t, c_int, c_void_p]),
     "moe_expert_compute_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int]),
     "moe_expert_compute": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p,
                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,

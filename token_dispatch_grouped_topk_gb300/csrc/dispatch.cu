@@ -455,18 +455,24 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
 // dropped.  Each (y = 0) block adds its clamped positions to counts[e] (the
 // per-expert valid rows, zeroed by the launcher) and writes its column of
 // seg_counts [E, W].
-template <typename IdT>
+//
+// kFp8: the same slots, with the quantisation fused as in route_scatter_fp8_kernel:
+// each token row is quantised once (a half-warp per 128-group of the block's
+// column slice of `slice` groups) and its e4m3 codes and scales are written to
+// xq/xs at every kept slot; otherwise `slice` counts 16-byte vectors of BF16.
+template <typename IdT, bool kFp8>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
     route_source_slots_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx,
                               int T, int H, int K, int E, int W, int mt,
                               const int32_t* __restrict__ rank_offsets, uint4* __restrict__ recv,
+                              uint2* __restrict__ xq, float* __restrict__ xs,
                               int32_t* __restrict__ counts, int32_t* __restrict__ seg_counts,
-                              int32_t* __restrict__ src_map, int32_t* dev_status,
-                              int vec_per_slice) {
+                              int32_t* __restrict__ src_map, int32_t* dev_status, int slice) {
   extern __shared__ int smem[];
   int* s_cnt = smem;                        // [kDispatchWarps][E] routes per warp of a chunk
   int* s_dest = smem + kDispatchWarps * E;  // [kDispatchWarps][32]
   int* s_pos = s_dest + kDispatchWarps * 32;  // [E] next position of this source per expert
+  float* s_sc = reinterpret_cast<float*>(s_pos + E);   // FP8: [kDispatchWarps][slice] scales
   const int r = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tpw = 32 / K;
@@ -477,8 +483,12 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
   const int64_t R = static_cast<int64_t>(W) * mt;
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_pos[e] = 0;
   const int nvec = H / 8;
-  const int v0 = blockIdx.y * vec_per_slice;
-  const int v1 = min(nvec, v0 + vec_per_slice);
+  const int v0 = blockIdx.y * slice;
+  const int v1 = min(nvec, v0 + slice);
+  const int G = H / kGroup;
+  const int g0 = blockIdx.y * slice;
+  const int g1 = min(G, g0 + slice);
+  const int half = lane >> 4, hl = lane & 15;
   int bad = 0;
   for (int c0 = t0; c0 < t1; c0 += kDispatchWarps * tpw) {
     for (int i = threadIdx.x; i < kDispatchWarps * E; i += blockDim.x) s_cnt[i] = 0;
@@ -517,18 +527,53 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
       for (int kk = 0; kk < K; ++kk) any |= dq[kk] >= 0;
       if (!any) continue;
       const uint4* src = x + static_cast<size_t>(tok) * nvec;
-      for (int v = v0 + lane; v < v1; v += 32 * 8) {
-        uint4 a[8];
+      if constexpr (kFp8) {
+        float* wsc = s_sc + warp * slice;
+        // eight groups per pass: half-warp `half` takes groups gg + 2u + half
+        for (int gg = g0; gg < g1; gg += 8) {
+          uint4 v[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (v + 32 * u < v1) a[u] = ld_stream(src + v + 32 * u);
+          for (int u = 0; u < 4; ++u) {
+            const int g = gg + 2 * u + half;
+            if (g < g1) v[u] = ld_stream(src + g * 16 + hl);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int g = gg + 2 * u + half;
+            const bool on = g < g1;
+            uint2 codes;
+            float scale;
+            quantize_group(v[u], on, &codes, &scale);
+            if (on) {
+              for (int kk = 0; kk < K; ++kk) {
+                const int qq = dq[kk];
+                if (qq >= 0) xq[static_cast<size_t>(qq) * (H / 8) + g * 16 + hl] = codes;
+              }
+              if (hl == 0) wsc[g - g0] = scale;
+            }
+          }
+        }
+        __syncwarp();
         for (int kk = 0; kk < K; ++kk) {
           const int qq = dq[kk];
           if (qq < 0) continue;
-          uint4* dst = recv + static_cast<size_t>(qq) * nvec;
+          for (int g = g0 + lane; g < g1; g += 32) xs[static_cast<size_t>(qq) * G + g] = wsc[g - g0];
+        }
+        __syncwarp();
+      } else {
+        for (int v = v0 + lane; v < v1; v += 32 * 8) {
+          uint4 a[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            if (v + 32 * u < v1) dst[v + 32 * u] = a[u];
+            if (v + 32 * u < v1) a[u] = ld_stream(src + v + 32 * u);
+          for (int kk = 0; kk < K; ++kk) {
+            const int qq = dq[kk];
+            if (qq < 0) continue;
+            uint4* dst = recv + static_cast<size_t>(qq) * nvec;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (v + 32 * u < v1) dst[v + 32 * u] = a[u];
+          }
         }
       }
     }
@@ -615,39 +660,47 @@ cudaError_t dispatch_impl(const void* x, const IdT* topk_idx, int T, int H, int 
 }  // namespace
 
 namespace {
+// xq == nullptr: BF16 rows into recv; else e4m3 codes and scales into xq/xs.
 template <typename IdT>
 cudaError_t source_slots_impl(const void* x, const IdT* topk_idx, int T, int H, int K, int E,
                               int W, int mt, const int32_t* rank_offsets, void* recv,
-                              int32_t* counts, int32_t* seg_counts, int32_t* src_map,
-                              int32_t* dev_status, int sm_count, cudaStream_t s) {
+                              uint8_t* xq, float* xs, int32_t* counts, int32_t* seg_counts,
+                              int32_t* src_map, int32_t* dev_status, int sm_count,
+                              cudaStream_t s) {
   cudaError_t err = cudaMemsetAsync(dev_status, 0, 2 * sizeof(int32_t), s);
   if (err == cudaSuccess) err = cudaMemsetAsync(counts, 0, E * sizeof(int32_t), s);
   if (err != cudaSuccess) return err;
-  const int nvec = H / 8;
-  int hsplit = row_slices(W, nvec, 32, sm_count);
-  const int vec_per_slice = (nvec + hsplit - 1) / hsplit;
-  hsplit = (nvec + vec_per_slice - 1) / vec_per_slice;
-  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + E) * sizeof(int);
-  if ((err = allow_smem(route_source_slots_kernel<IdT>, smem)) != cudaSuccess) return err;
-  route_source_slots_kernel<IdT><<<dim3(W, hsplit), kDispatchWarps * 32, smem, s>>>(
+  const bool fp8 = xq != nullptr;
+  // column slices: 16-byte BF16 vectors (at least 32), or whole 128-groups (at least two)
+  const int units = fp8 ? H / kGroup : H / 8;
+  int hsplit = row_slices(W, units, fp8 ? 2 : 32, sm_count);
+  const int per_slice = (units + hsplit - 1) / hsplit;
+  hsplit = (units + per_slice - 1) / per_slice;
+  const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + E) * sizeof(int) +
+                      (fp8 ? kDispatchWarps * per_slice * sizeof(float) : 0);
+  auto kernel = fp8 ? route_source_slots_kernel<IdT, true> : route_source_slots_kernel<IdT, false>;
+  if ((err = allow_smem(kernel, smem)) != cudaSuccess) return err;
+  kernel<<<dim3(W, hsplit), kDispatchWarps * 32, smem, s>>>(
       static_cast<const uint4*>(x), topk_idx, T, H, K, E, W, mt, rank_offsets,
-      static_cast<uint4*>(recv), counts, seg_counts, src_map, dev_status, vec_per_slice);
+      static_cast<uint4*>(recv), reinterpret_cast<uint2*>(xq), xs, counts, seg_counts, src_map,
+      dev_status, per_slice);
   return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_dispatch_source_slots(const void* x, const void* topk_idx, int idx_bits, int T,
                                          int H, int K, int E, int W, int mt,
-                                         const int32_t* rank_offsets, void* recv, int32_t* counts,
-                                         int32_t* seg_counts, int32_t* src_map,
-                                         int32_t* dev_status, int sm_count, cudaStream_t s) {
+                                         const int32_t* rank_offsets, void* recv, uint8_t* xq,
+                                         float* xs, int32_t* counts, int32_t* seg_counts,
+                                         int32_t* src_map, int32_t* dev_status, int sm_count,
+                                         cudaStream_t s) {
   if (idx_bits == 32)
     return source_slots_impl(x, static_cast<const int32_t*>(topk_idx), T, H, K, E, W, mt,
-                             rank_offsets, recv, counts, seg_counts, src_map, dev_status,
+                             rank_offsets, recv, xq, xs, counts, seg_counts, src_map, dev_status,
                              sm_count, s);
   return source_slots_impl(x, static_cast<const int64_t*>(topk_idx), T, H, K, E, W, mt,
-                           rank_offsets, recv, counts, seg_counts, src_map, dev_status, sm_count,
-                           s);
+                           rank_offsets, recv, xq, xs, counts, seg_counts, src_map, dev_status,
+                           sm_count, s);
 }
 
 cudaError_t launch_dispatch(const void* x, const void* topk_idx, int idx_bits, int T, int H, int K,

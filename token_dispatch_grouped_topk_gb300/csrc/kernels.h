@@ -65,14 +65,17 @@ cudaError_t launch_dispatch(const void* x, const void* topk_idx, int idx_bits, i
                             int E, RowLayout rl, void* recv, int32_t* counts, int32_t* src_map,
                             int32_t* dev_status, int32_t* hist, int sm_count, cudaStream_t s);
 
-// ----- per-source fixed-slot dispatch: recv [E, W * mt, H]; counts [E] valid
-// rows per expert, seg_counts [E, W] per (expert, source rank); rank_offsets
-// [W + 1] token offsets of the source ranks, or null for ceil(T / W) each
+// ----- per-source fixed-slot dispatch: recv [E, W * mt, H] BF16, or (recv
+// null) the e4m3 codes xq [E, W * mt, H] and scales xs [E, W * mt, H / 128] of
+// each token row quantised once; counts [E] valid rows per expert, seg_counts
+// [E, W] per (expert, source rank); rank_offsets [W + 1] token offsets of the
+// source ranks, or null for ceil(T / W) each
 cudaError_t launch_dispatch_source_slots(const void* x, const void* topk_idx, int idx_bits, int T,
                                          int H, int K, int E, int W, int mt,
-                                         const int32_t* rank_offsets, void* recv, int32_t* counts,
-                                         int32_t* seg_counts, int32_t* src_map,
-                                         int32_t* dev_status, int sm_count, cudaStream_t s);
+                                         const int32_t* rank_offsets, void* recv, uint8_t* xq,
+                                         float* xs, int32_t* counts, int32_t* seg_counts,
+                                         int32_t* src_map, int32_t* dev_status, int sm_count,
+                                         cudaStream_t s);
 
 // ----- dispatch fused with the per-token FP8 quantisation: xq e4m3 and xs
 // (row layout rl, int32 or int64 ids) instead of the BF16 receive buffer
@@ -81,9 +84,12 @@ cudaError_t launch_dispatch_quant(const void* x, const void* topk_idx, int idx_b
                                   int32_t* counts, int32_t* src_map, int32_t* dev_status,
                                   int32_t* hist, int sm_count, cudaStream_t s);
 
-// ----- per-token FP8 quantisation of the valid rows; xs is [E, R, H/128]
+// ----- per-token FP8 quantisation of the valid rows; xs is [E, R, H/128].
+// With pq/ps (per-source slots only) the slot rows already hold e4m3 codes and
+// scales, which are packed instead of quantised.
 cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, RowLayout rl, int H,
-                            uint8_t* xq, float* xs, int sm_count, cudaStream_t s);
+                            uint8_t* xq, float* xs, int sm_count, cudaStream_t s,
+                            const uint8_t* pq = nullptr, const float* ps = nullptr);
 
 // ----- grouped block-scaled FP8 GEMMs on tcgen05
 // w13_interleaved: W13 output rows alternate gate and up (2j gate, 2j+1 up)

@@ -221,12 +221,14 @@ moe_status moe_dispatch_packed(const void* x, const int64_t* topk_idx, const flo
                          dev_status, workspace, workspace_bytes, stream);
 }
 
-moe_status moe_dispatch_source_slots(const void* x, const void* topk_idx, int idx_bits,
-                                     const float* topk_w, int T, int H, int K, int E, int L,
-                                     int max_tokens, const int32_t* rank_offsets, void* recv,
-                                     int32_t* counts, int32_t* seg_counts, int32_t* src_map,
-                                     int32_t* dev_status, moe_stream_t stream) {
-  (void)topk_w;
+namespace {
+// Host checks and launch of the per-source fixed-slot dispatch: BF16 rows into
+// recv, or (fp8) e4m3 codes and scales into xq/xs.
+moe_status source_slots_dispatch(bool fp8, const void* x, const void* topk_idx, int idx_bits,
+                                 int T, int H, int K, int E, int L, int max_tokens,
+                                 const int32_t* rank_offsets, void* recv, uint8_t* xq, float* xs,
+                                 int32_t* counts, int32_t* seg_counts, int32_t* src_map,
+                                 int32_t* dev_status, moe_stream_t stream) {
   if (T < 0 || !valid_hidden(H) || K < 1 || K > 32 || L < 1 || E % L != 0 || K > E ||
       max_tokens < 1)
     return MOE_ERR_INVALID_ARG;
@@ -237,15 +239,92 @@ moe_status moe_dispatch_source_slots(const void* x, const void* topk_idx, int id
   if (idx_bits != 32 && idx_bits != 64) return MOE_ERR_INVALID_ARG;
   if (counts == nullptr || seg_counts == nullptr || dev_status == nullptr)
     return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (x == nullptr || topk_idx == nullptr || recv == nullptr || src_map == nullptr))
+  if (T > 0 && (x == nullptr || topk_idx == nullptr || src_map == nullptr ||
+                (fp8 ? (xq == nullptr || xs == nullptr) : recv == nullptr)))
     return MOE_ERR_INVALID_ARG;
-  if (T > 0 && (!aligned16(x) || !aligned16(recv))) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(x) || (!fp8 && !aligned16(recv)) ||
+                (fp8 && (reinterpret_cast<uintptr_t>(xq) & 7u) != 0)))
+    return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(T) * K > (int64_t{1} << 31) - 1) return MOE_ERR_INVALID_ARG;
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
   return from_cuda(launch_dispatch_source_slots(
-      x, topk_idx, idx_bits, T, H, K, E, W, max_tokens, rank_offsets, recv, counts, seg_counts,
-      src_map, dev_status, dev->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+      x, topk_idx, idx_bits, T, H, K, E, W, max_tokens, rank_offsets, fp8 ? nullptr : recv,
+      fp8 ? xq : nullptr, fp8 ? xs : nullptr, counts, seg_counts, src_map, dev_status,
+      dev->sm_count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Host checks of the per-source expert compute; then the quantisation (recv
+// BF16) or the packing (xq/xs e4m3 slots) and both GEMMs on the packed rows.
+moe_status source_slots_compute(const void* recv, const uint8_t* xq_slots, const float* xs_slots,
+                                const int32_t* seg_counts, int E, int L, int max_tokens, int H,
+                                int I, const uint8_t* w13, const float* w13_scale,
+                                const uint8_t* w2, const float* w2_scale, void* out,
+                                int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                int flags, moe_stream_t stream) {
+  if (L < 1 || E % L != 0 || max_tokens < 1 || !valid_hidden(H) || !valid_hidden(I))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t R64 = int64_t{E / L} * max_tokens;
+  if (R64 > (int64_t{1} << 30) || !valid_experts(E, static_cast<int>(R64)))
+    return MOE_ERR_INVALID_ARG;
+  const int R = static_cast<int>(R64);
+  if (!valid_gemm_flags(flags)) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = recv == nullptr;
+  if ((fp8 && (xq_slots == nullptr || xs_slots == nullptr)) || seg_counts == nullptr ||
+      w13 == nullptr || w13_scale == nullptr || w2 == nullptr || w2_scale == nullptr ||
+      out == nullptr || dev_status == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if ((!fp8 && !aligned16(recv)) || (fp8 && !aligned16(xq_slots)) || !aligned16(w13) ||
+      !aligned16(w2) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  const ComputeWorkspace w = compute_workspace(E, R, H, I);
+  if (workspace == nullptr || workspace_bytes < w.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  const DeviceInfo* dev = nullptr;
+  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
+  // the tile list and the stored rows come from seg_counts
+  auto* ws = static_cast<uint8_t*>(workspace);
+  int32_t* slot_of = reinterpret_cast<int32_t*>(ws + w.slot);
+  const RowLayout rl = source_slot_rows(E, R, max_tokens, seg_counts, slot_of);
+  if (!fp8)
+    return expert_compute_impl(recv, seg_counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, out,
+                               dev_status, workspace, w, dev->sm_count,
+                               reinterpret_cast<cudaStream_t>(stream), flags);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* xq = ws + w.xq;
+  float* xs = reinterpret_cast<float*>(ws + w.xs);
+  cudaError_t err =
+      launch_quantize(nullptr, seg_counts, E, rl, H, xq, xs, dev->sm_count, s, xq_slots, xs_slots);
+  if (err == cudaSuccess)
+    err = run_gemms(xq, xs, seg_counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, ws + w.zq,
+                    reinterpret_cast<float*>(ws + w.zs), out, reinterpret_cast<int*>(ws + w.sync),
+                    w.sync_ints, dev_status, dev->sm_count, s, flags);
+  return from_cuda(err);
+}
+}  // namespace
+
+moe_status moe_dispatch_source_slots(const void* x, const void* topk_idx, int idx_bits,
+                                     const float* topk_w, int T, int H, int K, int E, int L,
+                                     int max_tokens, const int32_t* rank_offsets, void* recv,
+                                     int32_t* counts, int32_t* seg_counts, int32_t* src_map,
+                                     int32_t* dev_status, moe_stream_t stream) {
+  (void)topk_w;
+  return source_slots_dispatch(false, x, topk_idx, idx_bits, T, H, K, E, L, max_tokens,
+                               rank_offsets, recv, nullptr, nullptr, counts, seg_counts, src_map,
+                               dev_status, stream);
+}
+
+moe_status moe_dispatch_quant_source_slots(const void* x, const void* topk_idx, int idx_bits,
+                                           const float* topk_w, int T, int H, int K, int E,
+                                           int L, int max_tokens, const int32_t* rank_offsets,
+                                           uint8_t* xq, float* xs, int32_t* counts,
+                                           int32_t* seg_counts, int32_t* src_map,
+                                           int32_t* dev_status, moe_stream_t stream) {
+  (void)topk_w;
+  return source_slots_dispatch(true, x, topk_idx, idx_bits, T, H, K, E, L, max_tokens,
+                               rank_offsets, nullptr, xq, xs, counts, seg_counts, src_map,
+                               dev_status, stream);
 }
 
 moe_status moe_expert_compute_source_slots(const void* recv, const int32_t* counts,
@@ -256,30 +335,21 @@ moe_status moe_expert_compute_source_slots(const void* recv, const int32_t* coun
                                            void* workspace, size_t workspace_bytes, int flags,
                                            moe_stream_t stream) {
   (void)counts;  // the tile list follows seg_counts
-  if (L < 1 || E % L != 0 || max_tokens < 1 || !valid_hidden(H) || !valid_hidden(I))
-    return MOE_ERR_INVALID_ARG;
-  const int64_t R64 = int64_t{E / L} * max_tokens;
-  if (R64 > (int64_t{1} << 30) || !valid_experts(E, static_cast<int>(R64)))
-    return MOE_ERR_INVALID_ARG;
-  const int R = static_cast<int>(R64);
-  if (!valid_gemm_flags(flags)) return MOE_ERR_INVALID_ARG;
-  if (recv == nullptr || seg_counts == nullptr || w13 == nullptr || w13_scale == nullptr ||
-      w2 == nullptr || w2_scale == nullptr || out == nullptr || dev_status == nullptr)
-    return MOE_ERR_INVALID_ARG;
-  if (!aligned16(recv) || !aligned16(w13) || !aligned16(w2) || !aligned16(out))
-    return MOE_ERR_INVALID_ARG;
-  const ComputeWorkspace w = compute_workspace(E, R, H, I);
-  if (workspace == nullptr || workspace_bytes < w.total ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return MOE_ERR_WORKSPACE;
-  const DeviceInfo* dev = nullptr;
-  if (moe_status st = check_device(&dev); st != MOE_OK) return st;
-  // the tile list and the stored rows come from seg_counts; counts is not read
-  int32_t* slot_of = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + w.slot);
-  return expert_compute_impl(recv, seg_counts, E,
-                             source_slot_rows(E, R, max_tokens, seg_counts, slot_of),
-                             H, I, w13, w13_scale, w2, w2_scale, out, dev_status, workspace, w,
-                             dev->sm_count, reinterpret_cast<cudaStream_t>(stream), flags);
+  if (recv == nullptr) return MOE_ERR_INVALID_ARG;
+  return source_slots_compute(recv, nullptr, nullptr, seg_counts, E, L, max_tokens, H, I, w13,
+                              w13_scale, w2, w2_scale, out, dev_status, workspace,
+                              workspace_bytes, flags, stream);
+}
+
+moe_status moe_gemm_source_slots(const uint8_t* xq, const float* xs, const int32_t* seg_counts,
+                                 int E, int L, int max_tokens, int H, int I, const uint8_t* w13,
+                                 const float* w13_scale, const uint8_t* w2,
+                                 const float* w2_scale, void* out, int32_t* dev_status,
+                                 void* workspace, size_t workspace_bytes, int flags,
+                                 moe_stream_t stream) {
+  return source_slots_compute(nullptr, xq, xs, seg_counts, E, L, max_tokens, H, I, w13, w13_scale,
+                              w2, w2_scale, out, dev_status, workspace, workspace_bytes, flags,
+                              stream);
 }
 
 moe_status moe_dispatch_quant_ex(const void* x, const void* topk_idx, int idx_bits,

@@ -27,9 +27,13 @@ namespace {
 constexpr int kQuantWarps = 8;
 constexpr int kRowsPerBlock = 8;
 
+// kPack (per-source slots only): the slot rows already hold e4m3 codes `pq` and
+// scales `ps` (the dispatch quantised them); each packed row copies its slot's.
+template <bool kPack>
 __global__ void __launch_bounds__(kQuantWarps * 32)
     quantize_kernel(const uint4* __restrict__ recv, const int32_t* __restrict__ counts, int E,
-                    RowLayout rl, int H, uint2* __restrict__ xq, float* __restrict__ xs) {
+                    RowLayout rl, int H, uint2* __restrict__ xq, float* __restrict__ xs,
+                    const uint4* __restrict__ pq, const float* __restrict__ ps) {
   extern __shared__ int smem[];
   int* s_start = smem;               // [E + 1] prefix of row blocks
   int* s_cnt = smem + E + 1;         // [E]
@@ -92,6 +96,13 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
         src_row = static_cast<size_t>(e) * R + slot;
         if (lane == 0) rl.slot_of[row] = slot;
       }
+      if constexpr (kPack) {
+        const uint4* csrc = pq + src_row * (H / 16);
+        uint4* cdst = reinterpret_cast<uint4*>(xq) + row * (H / 16);
+        for (int i = lane; i < H / 16; i += 32) cdst[i] = ld_stream(csrc + i);
+        for (int g = lane; g < G; g += 32) s_scale[g * kRowsPerBlock + r] = ps[src_row * G + g];
+        continue;
+      }
       const uint4* src = recv + src_row * nvec;
       uint2* dst = xq + row * (H / 8);
       // Four pairs of groups per pass: every lane has four 16-byte loads in
@@ -150,7 +161,8 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 }  // namespace
 
 cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, RowLayout rl, int H,
-                            uint8_t* xq, float* xs, int sm_count, cudaStream_t s) {
+                            uint8_t* xq, float* xs, int sm_count, cudaStream_t s,
+                            const uint8_t* pq, const float* ps) {
   const int R = rl.R;
   const int G = H / kGroup;
   const size_t smem = (3 * E + 2) * sizeof(int) + G * kRowsPerBlock * sizeof(float) +
@@ -159,13 +171,15 @@ cudaError_t launch_quantize(const void* recv, const int32_t* counts, int E, RowL
   const long long max_blocks = static_cast<long long>(E) * ((R + kRowsPerBlock - 1) / kRowsPerBlock);
   const int grid = static_cast<int>(std::min<long long>(max_blocks, sm_count * 8LL));
   if (grid <= 0) return cudaSuccess;
+  auto kernel = pq != nullptr ? quantize_kernel<true> : quantize_kernel<false>;
   if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
   }
-  quantize_kernel<<<grid, kQuantWarps * 32, smem, s>>>(static_cast<const uint4*>(recv), counts, E, rl,
-                                                        H, reinterpret_cast<uint2*>(xq), xs);
+  kernel<<<grid, kQuantWarps * 32, smem, s>>>(static_cast<const uint4*>(recv), counts, E, rl, H,
+                                              reinterpret_cast<uint2*>(xq), xs,
+                                              reinterpret_cast<const uint4*>(pq), ps);
   return cudaGetLastError();
 }
 
