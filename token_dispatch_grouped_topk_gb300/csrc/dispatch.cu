@@ -460,7 +460,11 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
 // each token row is quantised once (a half-warp per 128-group of the block's
 // column slice of `slice` groups) and its e4m3 codes and scales are written to
 // xq/xs at every kept slot; otherwise `slice` counts 16-byte vectors of BF16.
-template <typename IdT, bool kFp8>
+// kShort: at most eight tokens per warp and one 16-byte vector per lane and
+// token (a slice of at most two groups, or 32 vectors); every token's load is
+// then issued before the first store.  A separate instantiation: its eight
+// preloaded vectors would double the loop form's registers.
+template <typename IdT, bool kFp8, bool kShort>
 __global__ void __launch_bounds__(kDispatchWarps * 32)
     route_source_slots_kernel(const uint4* __restrict__ x, const IdT* __restrict__ topk_idx,
                               int T, int H, int K, int E, int W, int mt,
@@ -519,60 +523,98 @@ __global__ void __launch_bounds__(kDispatchWarps * 32)
     if (leader) atomicAdd(&s_pos[e], __popc(peers));   // positions for the next chunk
     // payload: this warp's tokens, this block's column slice
     const int* wdest = s_dest + warp * 32;
-    for (int tt = 0; tt < tpw; ++tt) {
-      const int tok = c0 + warp * tpw + tt;
-      if (tok >= t1) break;
-      const int* dq = wdest + tt * K;
-      bool any = false;
-      for (int kk = 0; kk < K; ++kk) any |= dq[kk] >= 0;
-      if (!any) continue;
-      const uint4* src = x + static_cast<size_t>(tok) * nvec;
-      if constexpr (kFp8) {
-        float* wsc = s_sc + warp * slice;
-        // eight groups per pass: half-warp `half` takes groups gg + 2u + half
-        for (int gg = g0; gg < g1; gg += 8) {
-          uint4 v[4];
+    const int tbase = c0 + warp * tpw;
+    if constexpr (kShort) {
+      const unsigned kept = __ballot_sync(0xffffffffu, q >= 0);
+      const unsigned kmask = K >= 32 ? 0xffffffffu : ((1u << K) - 1u);
+      const int unit = kFp8 ? (g0 + half) * 16 + hl : v0 + lane;   // vector of the row
+      const bool has = kFp8 ? g0 + half < g1 : v0 + lane < v1;
+      uint4 a[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int g = gg + 2 * u + half;
-            if (g < g1) v[u] = ld_stream(src + g * 16 + hl);
-          }
+      for (int tt = 0; tt < 8; ++tt)
+        if (tt < tpw && tbase + tt < t1 && has && ((kept >> (tt * K)) & kmask))
+          a[tt] = ld_stream(x + static_cast<size_t>(tbase + tt) * nvec + unit);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int g = gg + 2 * u + half;
-            const bool on = g < g1;
-            uint2 codes;
-            float scale;
-            quantize_group(v[u], on, &codes, &scale);
-            if (on) {
-              for (int kk = 0; kk < K; ++kk) {
-                const int qq = dq[kk];
-                if (qq >= 0) xq[static_cast<size_t>(qq) * (H / 8) + g * 16 + hl] = codes;
-              }
-              if (hl == 0) wsc[g - g0] = scale;
+      for (int tt = 0; tt < 8; ++tt) {
+        if (tt >= tpw || tbase + tt >= t1) break;   // the same for the whole warp
+        if (!((kept >> (tt * K)) & kmask)) continue;
+        const int* dq = wdest + tt * K;
+        if constexpr (kFp8) {
+          uint2 codes;
+          float scale;
+          quantize_group(a[tt], has, &codes, &scale);
+          if (has) {
+            const int g = g0 + half;
+            for (int kk = 0; kk < K; ++kk) {
+              const int qq = dq[kk];
+              if (qq < 0) continue;
+              xq[static_cast<size_t>(qq) * (H / 8) + unit] = codes;
+              if (hl == 0) xs[static_cast<size_t>(qq) * G + g] = scale;
             }
           }
+        } else if (has) {
+          for (int kk = 0; kk < K; ++kk) {
+            const int qq = dq[kk];
+            if (qq >= 0) recv[static_cast<size_t>(qq) * nvec + unit] = a[tt];
+          }
         }
-        __syncwarp();
-        for (int kk = 0; kk < K; ++kk) {
-          const int qq = dq[kk];
-          if (qq < 0) continue;
-          for (int g = g0 + lane; g < g1; g += 32) xs[static_cast<size_t>(qq) * G + g] = wsc[g - g0];
-        }
-        __syncwarp();
-      } else {
-        for (int v = v0 + lane; v < v1; v += 32 * 8) {
-          uint4 a[8];
+      }
+    } else {
+      for (int tt = 0; tt < tpw; ++tt) {
+        const int tok = c0 + warp * tpw + tt;
+        if (tok >= t1) break;
+        const int* dq = wdest + tt * K;
+        bool any = false;
+        for (int kk = 0; kk < K; ++kk) any |= dq[kk] >= 0;
+        if (!any) continue;
+        const uint4* src = x + static_cast<size_t>(tok) * nvec;
+        if constexpr (kFp8) {
+          float* wsc = s_sc + warp * slice;
+          // eight groups per pass: half-warp `half` takes groups gg + 2u + half
+          for (int gg = g0; gg < g1; gg += 8) {
+            uint4 v[4];
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (v + 32 * u < v1) a[u] = ld_stream(src + v + 32 * u);
+            for (int u = 0; u < 4; ++u) {
+              const int g = gg + 2 * u + half;
+              if (g < g1) v[u] = ld_stream(src + g * 16 + hl);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int g = gg + 2 * u + half;
+              const bool on = g < g1;
+              uint2 codes;
+              float scale;
+              quantize_group(v[u], on, &codes, &scale);
+              if (on) {
+                for (int kk = 0; kk < K; ++kk) {
+                  const int qq = dq[kk];
+                  if (qq >= 0) xq[static_cast<size_t>(qq) * (H / 8) + g * 16 + hl] = codes;
+                }
+                if (hl == 0) wsc[g - g0] = scale;
+              }
+            }
+          }
+          __syncwarp();
           for (int kk = 0; kk < K; ++kk) {
             const int qq = dq[kk];
             if (qq < 0) continue;
-            uint4* dst = recv + static_cast<size_t>(qq) * nvec;
+            for (int g = g0 + lane; g < g1; g += 32) xs[static_cast<size_t>(qq) * G + g] = wsc[g - g0];
+          }
+          __syncwarp();
+        } else {
+          for (int v = v0 + lane; v < v1; v += 32 * 8) {
+            uint4 a[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-              if (v + 32 * u < v1) dst[v + 32 * u] = a[u];
+              if (v + 32 * u < v1) a[u] = ld_stream(src + v + 32 * u);
+            for (int kk = 0; kk < K; ++kk) {
+              const int qq = dq[kk];
+              if (qq < 0) continue;
+              uint4* dst = recv + static_cast<size_t>(qq) * nvec;
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                if (v + 32 * u < v1) dst[v + 32 * u] = a[u];
+            }
           }
         }
       }
@@ -678,7 +720,11 @@ cudaError_t source_slots_impl(const void* x, const IdT* topk_idx, int T, int H, 
   hsplit = (units + per_slice - 1) / per_slice;
   const size_t smem = (kDispatchWarps * E + kDispatchWarps * 32 + E) * sizeof(int) +
                       (fp8 ? kDispatchWarps * per_slice * sizeof(float) : 0);
-  auto kernel = fp8 ? route_source_slots_kernel<IdT, true> : route_source_slots_kernel<IdT, false>;
+  const bool short_slice = 32 / K <= 8 && per_slice <= (fp8 ? 2 : 32);
+  auto kernel = fp8 ? (short_slice ? route_source_slots_kernel<IdT, true, true>
+                                   : route_source_slots_kernel<IdT, true, false>)
+                    : (short_slice ? route_source_slots_kernel<IdT, false, true>
+                                   : route_source_slots_kernel<IdT, false, false>);
   if ((err = allow_smem(kernel, smem)) != cudaSuccess) return err;
   kernel<<<dim3(W, hsplit), kDispatchWarps * 32, smem, s>>>(
       static_cast<const uint4*>(x), topk_idx, T, H, K, E, W, mt, rank_offsets,
