@@ -359,7 +359,9 @@ moe_status moe_combine_packed(const void* out, int64_t rows, const int32_t* src_
  * moe_gemm_source_slots -- both GEMMs on those slots: each expert's valid rows
  *   are packed inside the workspace (no quantisation: the codes and scales are
  *   copied), then the GEMMs of moe_expert_compute_source_slots run with the
- *   same workspace size, flags and output.  Outputs equal
+ *   same workspace size, flags and output.  xq 16-byte aligned (else
+ *   MOE_ERR_INVALID_ARG); xs and seg_counts as written by
+ *   moe_dispatch_quant_source_slots.  Outputs equal
  *   moe_expert_compute_source_slots' on the BF16 slots of the same routes, bit
  *   for bit.
  * ------------------------------------------------------------------------- */

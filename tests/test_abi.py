@@ -202,6 +202,49 @@ def test_gemm_gateup_down_sync_size_and_rejections(lib):
     assert f(*args(zq=ctypes.c_void_p(4096 + 8))) == -1   # TMA source must be 16-byte aligned
 
 
+def test_source_slot_entry_points_reject_on_host(lib):
+    """The per-source layout's calls validate before any launch: the BF16 and
+    FP8 slot dispatches and the GEMMs on FP8 slots."""
+    mis4, mis8 = ctypes.c_void_p(4096 + 4), ctypes.c_void_p(4096 + 8)
+
+    def dq(**k):
+        a = dict(x=FAKE, idx=FAKE, bits=64, T=64, H=256, K=2, E=8, L=2, mt=16, off=None, xq=FAKE,
+                 xs=FAKE, counts=FAKE, seg=FAKE, src=FAKE, st=FAKE)
+        a.update(k)
+        return lib.moe_dispatch_quant_source_slots(
+            a["x"], a["idx"], a["bits"], None, a["T"], a["H"], a["K"], a["E"], a["L"], a["mt"],
+            a["off"], a["xq"], a["xs"], a["counts"], a["seg"], a["src"], a["st"], None)
+    assert dq(L=0) == -1
+    assert dq(L=3) == -1                       # E % L != 0
+    assert dq(mt=0) == -1
+    assert dq(bits=16) == -1
+    assert dq(H=200) == -1
+    assert dq(xq=None) == -1 and dq(xs=None) == -1
+    assert dq(xq=mis4) == -1                   # codes are stored 8 bytes at a time
+    assert dq(counts=None) == -1 and dq(seg=None) == -1
+    assert lib.moe_dispatch_source_slots(FAKE, FAKE, 64, None, 64, 256, 2, 8, 2, 16, None, None,
+                                         FAKE, FAKE, FAKE, FAKE, None) == -1   # null recv
+    assert lib.moe_dispatch_source_slots(FAKE, FAKE, 64, None, 64, 256, 2, 8, 2, 16, None, mis8,
+                                         FAKE, FAKE, FAKE, FAKE, None) == -1   # recv alignment
+
+    ws = lib.moe_expert_compute_workspace_size(8, 4 * 16, 256, 128)
+    assert ws > 0
+
+    def gs(**k):
+        a = dict(xq=FAKE, xs=FAKE, seg=FAKE, E=8, L=2, mt=16, H=256, I=128, w13=FAKE, s13=FAKE,
+                 w2=FAKE, s2=FAKE, out=FAKE, st=FAKE, ws=FAKE, ws_bytes=ws, flags=0)
+        a.update(k)
+        return lib.moe_gemm_source_slots(
+            a["xq"], a["xs"], a["seg"], a["E"], a["L"], a["mt"], a["H"], a["I"], a["w13"],
+            a["s13"], a["w2"], a["s2"], a["out"], a["st"], a["ws"], a["ws_bytes"], a["flags"], None)
+    assert gs(xq=mis8) == -1                   # TMA reads the packed rows; the slots 16-byte aligned
+    assert gs(xq=None) == -1 and gs(xs=None) == -1 and gs(seg=None) == -1
+    assert gs(I=100) == -1 and gs(L=3) == -1 and gs(mt=0) == -1
+    assert gs(flags=8) == -1
+    assert gs(ws_bytes=ws - 1) == -3 and gs(ws=None) == -3
+    assert gs(ws=ctypes.c_void_p(4096 + 128)) == -3   # 256-byte aligned workspace
+
+
 def test_header_compiles_as_c(tmp_path):
     """include/moe.h is plain C: the C layer driver compiles against it with
     gcc in C11 mode, warnings as errors (compile only; it runs in the GPU
