@@ -645,9 +645,10 @@ def run_ours(args, rank, local, world):
         y_h.copy_(y, non_blocking=True)
 
     # The public host-memory path: copies of neighbouring steps overlap the
-    # compute of the current one (api.HostPipeline); every step still copies
-    # its inputs in from pinned host memory and its output back.
-    pipe = api.HostPipeline(buf)
+    # compute of the current one (api.HostPipeline, the layer replayed as one
+    # CUDA graph per input slot after the slot's first step); every step still
+    # copies its inputs in from pinned host memory and its output back.
+    pipe = api.HostPipeline(buf, graph=True)
     y_hs = [y_h, torch.empty_like(y_h).pin_memory()]
 
     def e2e_step(i):
@@ -789,8 +790,9 @@ def run_ours(args, rank, local, world):
                   "source": peaks["source"]},
         "e2e": {"value": e2e_rows / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps, "steps": e2e_steps,
-                "path": "api.HostPipeline: pinned host in/out every step; step i+1's copy-in and "
-                        "step i-1's copy-out run on two copy streams beside step i's compute",
+                "path": "api.HostPipeline(graph=True): pinned host in/out every step; step i+1's "
+                        "copy-in and step i-1's copy-out run on two copy streams beside step i's "
+                        "compute, a CUDA-graph replay of the layer",
                 "clocks": e2e_clk.summary(),
                 "serial_value": e2e_rows / (e2e_serial_ms / 1e3),
                 "serial_note": "copy in, compute, copy out back to back on one stream"},
