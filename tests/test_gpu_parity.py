@@ -469,7 +469,7 @@ def test_layer_traced_scenario():
 
 
 def test_graph_replay_changes_routes():
-    """Replay of one captured graph reads this round's routes: switching
+    """Replay of one captured graph reads the routes current at replay: switching
     token 21 from [E1, E6] to [E0, E7] moves counts 111/1/1/111 -> 112/0/0/112
     and the output follows (the pages' replay example)."""
     d = W.make_layer_inputs("traced", seed=0, device=DEV)

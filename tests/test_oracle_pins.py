@@ -517,7 +517,7 @@ def pin_combine_rounding(combine):
 def test_combine_rounding_sequence():
     """"SGLang、NCCL 与 MoE EP", §3.2: each route's output is multiplied by its
     weight once and summed into the token's row; the accumulation is fp32 in
-    ascending k (the reading this build takes where the pages do not fix the
+    ascending k (the reading taken here, as the pages do not fix the
     rounding).  The three readings differ on this case, so the pin tells them
     apart; the fp64 oracle combine agrees with the fp64 reading."""
     _, _, want = _combine_rounding_readings()
