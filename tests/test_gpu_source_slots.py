@@ -132,11 +132,13 @@ def test_dispatch_random_with_drops_and_empty_ranks(bits):
 @pytest.mark.parametrize("bits", [64, 32])
 @pytest.mark.parametrize("E,L,K,mt,H,T", [(40, 5, 4, 3, 256, 150), (12, 3, 4, 50, 1152, 300),
                                           (256, 8, 8, 32, 7168, 256), (16, 16, 2, 7, 128, 1),
-                                          (8, 2, 3, 5, 384, 0)])
+                                          (8, 2, 3, 5, 384, 0), (64, 8, 32, 4, 256, 40),
+                                          (16, 4, 1, 10, 512, 100)])
 def test_dispatch_quant_source_slots(bits, E, L, K, mt, H, T):
     """FP8 slots: drops, an invalid id, ranks that send nothing, one group per
     row, a ragged last pass of groups (9 groups), the decode layer's shape, one
-    token and no tokens."""
+    token and no tokens, top-32 (one token per warp) and top-1 (32 tokens per
+    warp)."""
     Wr = E // L
     g = torch.Generator().manual_seed(E + H + T + bits)
     idx = torch.randint(-1, E, (T, K), generator=g)
