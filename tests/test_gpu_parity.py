@@ -521,17 +521,27 @@ def test_layer_decode_config():
     assert_rows_close(f32(y)[toks], y_ref, what="decode y")
 
 
-@pytest.mark.parametrize("graph", [False, True])
-def test_host_pipeline_matches_forward(graph):
+@pytest.mark.parametrize("graph,layout", [(False, "padded"), (True, "padded"),
+                                          (True, "source_slots")])
+def test_host_pipeline_matches_forward(graph, layout):
     """api.HostPipeline (pinned host in/out, copies of neighbouring steps
     overlapped with compute, two device slots; eager, or each slot's layer
     captured once in a CUDA graph and replayed) returns, for every step, the
     bytes a plain forward on device inputs returns; five steps reuse each slot
-    at least twice, with a different routing per step."""
+    at least twice, with a different routing per step.  The per-source lane
+    forms its FP8 slots in the pipeline's first (eager) step, before the
+    capture."""
     d = W.make_layer_inputs("decode", seed=0, device=DEV)
     wl = d["wl"]
     dev = torch.device(DEV)
-    buf = api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
+
+    def lane():
+        if layout == "padded":
+            return api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.R, dev)
+        mt = wl.T // wl.W
+        return api.MoeLayerBuffers(wl.T, wl.E, wl.K, wl.H, wl.I, wl.W * mt, dev, source_slots=mt,
+                                   L=wl.L)
+    buf = lane()
     steps = []
     for i in range(5):
         idx, w = W.router(wl.T, wl.E, wl.K, W.router_bias(wl, 10 + i, "cpu"), 20 + i, "cpu")
@@ -541,6 +551,7 @@ def test_host_pipeline_matches_forward(graph):
     for x, idx, w in steps:
         y = buf.forward(x.to(dev), idx.to(dev), w.to(dev), d["w13"], d["s13"], d["w2"], d["s2"])
         want.append(y.cpu())
+    buf = lane()
     pipe = api.HostPipeline(buf, graph=graph)
     outs = [torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory() for _ in steps]
     pinned = [(x.pin_memory(), idx.pin_memory(), w.pin_memory()) for x, idx, w in steps]
