@@ -126,20 +126,21 @@ bool valid_gemm_flags(int flags) {
 }
 
 
-// The expert compute on a carved workspace: quantisation, then both GEMMs in
-// one launch.
+// The expert compute on a carved workspace: quantisation (or, with pq/ps, the
+// packing of per-source FP8 slots), then both GEMMs.
 moe_status expert_compute_impl(const void* recv, const int32_t* counts, int E, RowLayout rl, int H,
                                int I, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
                                const float* w2_scale, void* out, int32_t* dev_status, void* workspace,
                                const ComputeWorkspace& w, int sm_count, cudaStream_t s,
-                               int flags = 0) {
+                               int flags = 0, const uint8_t* pq = nullptr,
+                               const float* ps = nullptr) {
   auto* ws = static_cast<uint8_t*>(workspace);
   uint8_t* xq = ws + w.xq;
   float* xs = reinterpret_cast<float*>(ws + w.xs);
   uint8_t* zq = ws + w.zq;
   float* zs = reinterpret_cast<float*>(ws + w.zs);
   int* sync = reinterpret_cast<int*>(ws + w.sync);
-  cudaError_t err = launch_quantize(recv, counts, E, rl, H, xq, xs, sm_count, s);
+  cudaError_t err = launch_quantize(recv, counts, E, rl, H, xq, xs, sm_count, s, pq, ps);
   if (err == cudaSuccess)
     err = run_gemms(xq, xs, counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, zq, zs, out, sync,
                     w.sync_ints, dev_status, sm_count, s, flags);
@@ -284,23 +285,12 @@ moe_status source_slots_compute(const void* recv, const uint8_t* xq_slots, const
   const DeviceInfo* dev = nullptr;
   if (moe_status st = check_device(&dev); st != MOE_OK) return st;
   // the tile list and the stored rows come from seg_counts
-  auto* ws = static_cast<uint8_t*>(workspace);
-  int32_t* slot_of = reinterpret_cast<int32_t*>(ws + w.slot);
-  const RowLayout rl = source_slot_rows(E, R, max_tokens, seg_counts, slot_of);
-  if (!fp8)
-    return expert_compute_impl(recv, seg_counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, out,
-                               dev_status, workspace, w, dev->sm_count,
-                               reinterpret_cast<cudaStream_t>(stream), flags);
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* xq = ws + w.xq;
-  float* xs = reinterpret_cast<float*>(ws + w.xs);
-  cudaError_t err =
-      launch_quantize(nullptr, seg_counts, E, rl, H, xq, xs, dev->sm_count, s, xq_slots, xs_slots);
-  if (err == cudaSuccess)
-    err = run_gemms(xq, xs, seg_counts, E, rl, H, I, w13, w13_scale, w2, w2_scale, ws + w.zq,
-                    reinterpret_cast<float*>(ws + w.zs), out, reinterpret_cast<int*>(ws + w.sync),
-                    w.sync_ints, dev_status, dev->sm_count, s, flags);
-  return from_cuda(err);
+  int32_t* slot_of = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + w.slot);
+  return expert_compute_impl(recv, seg_counts, E,
+                             source_slot_rows(E, R, max_tokens, seg_counts, slot_of), H, I, w13,
+                             w13_scale, w2, w2_scale, out, dev_status, workspace, w,
+                             dev->sm_count, reinterpret_cast<cudaStream_t>(stream), flags,
+                             fp8 ? xq_slots : nullptr, fp8 ? xs_slots : nullptr);
 }
 }  // namespace
 
