@@ -2,14 +2,16 @@
  * One routed-MoE layer through the library's C ABI alone: no Python, no
  * PyTorch, only the CUDA runtime for memory and a stream.
  *
- *   layer_main DIR T H K E R I
+ *   layer_main DIR T H K E R I [fused]
  *
  * reads from DIR the raw little-endian arrays x.bin (BF16 [T,H]), idx.bin
  * (int64 [T,K]), w.bin (fp32 [T,K]), w13.bin (e4m3 [E,2I,H]), s13.bin (fp32
  * [E,2I/128,H/128]), w2.bin (e4m3 [E,H,I]) and s2.bin (fp32 [E,H/128,I/128]),
- * runs moe_dispatch, moe_expert_compute and moe_combine on one stream, and
- * writes y.bin (BF16 [T,H]), counts.bin (int32 [E]), src_map.bin (int32
- * [T,K]) and status.bin (int32 [2]).  Exits non-zero on any error.
+ * runs moe_dispatch, moe_expert_compute and moe_combine on one stream (with
+ * "fused": moe_dispatch_quant, moe_gemm_gateup_down and moe_combine, the
+ * layer's default path), and writes y.bin (BF16 [T,H]), counts.bin (int32
+ * [E]), src_map.bin (int32 [T,K]) and status.bin (int32 [2]).  Exits non-zero
+ * on any error.
  */
 #include <cuda_runtime.h>
 #include <stdio.h>
@@ -75,7 +77,9 @@ static void* dev_alloc(size_t bytes) {
 }
 
 int main(int argc, char** argv) {
-  if (argc != 8) die("usage: layer_main DIR T H K E R I");
+  if (argc != 8 && !(argc == 9 && strcmp(argv[8], "fused") == 0))
+    die("usage: layer_main DIR T H K E R I [fused]");
+  const int fused = argc == 9;
   const char* dir = argv[1];
   const int T = atoi(argv[2]), H = atoi(argv[3]), K = atoi(argv[4]);
   const int E = atoi(argv[5]), R = atoi(argv[6]), I = atoi(argv[7]);
@@ -89,27 +93,46 @@ int main(int argc, char** argv) {
   void* w2 = upload(dir, "w2.bin", (size_t)E * H * I);
   void* s2 = upload(dir, "s2.bin", (size_t)E * (H / 128) * (I / 128) * 4);
 
-  void* recv = dev_alloc(rows * H * 2);
   void* out = dev_alloc(rows * H * 2);
   int32_t* counts = (int32_t*)dev_alloc((size_t)E * 4);
   int32_t* src_map = (int32_t*)dev_alloc((size_t)T * K * 4);
   int32_t* status = (int32_t*)dev_alloc(8);
   void* y = dev_alloc((size_t)T * H * 2);
   const size_t ws_d = moe_dispatch_workspace_size(T, K, E);
-  const size_t ws_c = moe_expert_compute_workspace_size(E, R, H, I);
-  if (ws_c == 0) die("moe_expert_compute_workspace_size rejected the sizes");
   void* wsd = dev_alloc(ws_d);
-  void* wsc = dev_alloc(ws_c);
 
   cudaStream_t stream;
   check_cuda(cudaStreamCreate(&stream), "cudaStreamCreate");
   moe_stream_t s = (moe_stream_t)stream;
-  check_moe(moe_dispatch(x, (const int64_t*)idx, (const float*)w, T, H, K, E, R, recv, counts,
-                         src_map, status, wsd, ws_d, s),
-            "moe_dispatch");
-  check_moe(moe_expert_compute(recv, counts, E, R, H, I, (const uint8_t*)w13, (const float*)s13,
-                               (const uint8_t*)w2, (const float*)s2, out, status, wsc, ws_c, s),
-            "moe_expert_compute");
+  if (fused) {
+    /* FP8 activations and Z, and the fused GEMM launch's scratch, as separate
+       caller-owned buffers */
+    uint8_t* xq = (uint8_t*)dev_alloc(rows * H);
+    float* xs = (float*)dev_alloc(rows * (H / 128) * 4);
+    uint8_t* zq = (uint8_t*)dev_alloc(rows * I);
+    float* zs = (float*)dev_alloc(rows * (I / 128) * 4);
+    const size_t sync_bytes = moe_gemm_gateup_down_sync_size(E, R, 0);
+    if (sync_bytes == 0) die("moe_gemm_gateup_down_sync_size rejected the sizes");
+    void* sync = dev_alloc(sync_bytes);
+    check_moe(moe_dispatch_quant(x, (const int64_t*)idx, (const float*)w, T, H, K, E, R, xq, xs,
+                                 counts, src_map, status, wsd, ws_d, s),
+              "moe_dispatch_quant");
+    check_moe(moe_gemm_gateup_down(xq, xs, counts, E, R, 0, H, I, (const uint8_t*)w13,
+                                   (const float*)s13, (const uint8_t*)w2, (const float*)s2, zq,
+                                   zs, out, status, sync, sync_bytes, 0, s),
+              "moe_gemm_gateup_down");
+  } else {
+    const size_t ws_c = moe_expert_compute_workspace_size(E, R, H, I);
+    if (ws_c == 0) die("moe_expert_compute_workspace_size rejected the sizes");
+    void* wsc = dev_alloc(ws_c);
+    void* recv = dev_alloc(rows * H * 2);
+    check_moe(moe_dispatch(x, (const int64_t*)idx, (const float*)w, T, H, K, E, R, recv, counts,
+                           src_map, status, wsd, ws_d, s),
+              "moe_dispatch");
+    check_moe(moe_expert_compute(recv, counts, E, R, H, I, (const uint8_t*)w13, (const float*)s13,
+                                 (const uint8_t*)w2, (const float*)s2, out, status, wsc, ws_c, s),
+              "moe_expert_compute");
+  }
   check_moe(moe_combine(out, src_map, (const float*)w, T, H, K, E, R, y, s), "moe_combine");
   check_cuda(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
 

@@ -1,8 +1,10 @@
 """The C ABI driven from a plain C program: tests/capi/layer_main.c has no
 Python or PyTorch in its process, only the CUDA runtime for memory and a
 stream.  It is compiled here with gcc against include/moe.h and the library,
-runs one layer on arrays written to files, and its y, counts, source map and
-status must equal the same layer run through the Python binding."""
+runs one layer on arrays written to files (the separate path, or the default
+fused path: moe_dispatch_quant, moe_gemm_gateup_down, moe_combine), and its y,
+counts, source map and status must equal the same layer run through the
+Python binding."""
 import os
 import shutil
 import subprocess
@@ -43,8 +45,9 @@ def _raw(t):
     return t.numpy()
 
 
+@pytest.mark.parametrize("path", ["separate", "fused"])
 @pytest.mark.parametrize("case", ["traced", "ragged"])
-def test_c_program_layer_matches_python_binding(layer_main, tmp_path, case):
+def test_c_program_layer_matches_python_binding(layer_main, tmp_path, case, path):
     if case == "traced":
         d = W.make_layer_inputs("traced", seed=9, device="cpu")
         wl = d["wl"]
@@ -61,8 +64,9 @@ def test_c_program_layer_matches_python_binding(layer_main, tmp_path, case):
     for name, t in (("x", x), ("idx", idx), ("w", w), ("w13", w13), ("s13", s13), ("w2", w2),
                     ("s2", s2)):
         _raw(t).tofile(str(tmp_path / f"{name}.bin"))
-    run = subprocess.run([layer_main, str(tmp_path), str(T), str(H), str(K), str(E), str(R), str(I)],
-                         capture_output=True, text=True, timeout=300)
+    argv = [layer_main, str(tmp_path), str(T), str(H), str(K), str(E), str(R), str(I)]
+    run = subprocess.run(argv + (["fused"] if path == "fused" else []), capture_output=True,
+                         text=True, timeout=300)
     assert run.returncode == 0, run.stderr
     y_c = np.fromfile(str(tmp_path / "y.bin"), dtype=np.int16).reshape(T, H)
     counts_c = np.fromfile(str(tmp_path / "counts.bin"), dtype=np.int32)
