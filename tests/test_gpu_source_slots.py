@@ -261,3 +261,19 @@ def test_expert_compute_source_slots_both_launch_forms():
     a = flat[torch.from_numpy(res.src_map[both]).long().to(DEV)]
     b = outp.view(-1, H)[torch.from_numpy(mp[both]).long().to(DEV)]
     assert torch.equal(_bits(a), _bits(b))
+    # interleaved W13 rows: the BF16 and FP8 slot paths agree with each other
+    inter = []
+    for fp8 in (False, True):
+        out = torch.full_like(recv, 9.0)
+        st = torch.zeros(2, dtype=torch.int32, device=DEV)
+        if fp8:
+            api.moe_gemm_source_slots(xq, xs, seg8, L, mt, w13, s13, w2, s2, out=out,
+                                      dev_status=st, w13_interleaved=True)
+        else:
+            api.moe_expert_compute_source_slots(recv, counts, seg, L, mt, w13, s13, w2, s2,
+                                                out=out, dev_status=st, w13_interleaved=True)
+        torch.cuda.synchronize()
+        assert st.cpu().tolist() == [0, 0]
+        inter.append(out)
+    assert torch.equal(_bits(inter[0]), _bits(inter[1]))
+    assert not torch.equal(_bits(inter[0]), _bits(outs[0]))   # the flag reaches the GEMM
