@@ -799,3 +799,42 @@ def test_layer_paths_odd_shapes(T, E, K, H, I, R):
         ref = oracle_expert_rows(f32(x[torch.from_numpy(tk[:, 0]).to(DEV)]), wts[e])
         got = f32(buf.out.view(-1, H)[torch.from_numpy(src[tk[:, 0], tk[:, 1]]).long().to(DEV)])
         assert_rows_close(got, ref, what=f"expert {e}")
+
+
+def test_layer_max_experts():
+    """The largest expert count the library takes (E = 1024: the per-expert
+    tables in shared memory at their limit), top-8 over 400 tokens with an 8-row
+    capacity (drops): routing bit-exact against the oracle, fused, separate and
+    packed layer paths the same bytes, and the kept routes of every 16th expert
+    against the oracle."""
+    T, E, K, H, I, R = 400, 1024, 8, 256, 128, 8
+    dev = torch.device(DEV)
+    g = torch.Generator().manual_seed(1024)
+    idx = torch.stack([torch.randperm(E, generator=g)[:K] for _ in range(T)])
+    idx[:, 0] = torch.randint(0, 4, (T,), generator=g)     # four hot experts overflow
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16).to(DEV)
+    w = torch.rand(T, K, generator=g).to(DEV)
+    w13, s13, w2, s2 = (t.to(DEV) for t in W.expert_weights(E, H, I, 5, "cpu"))
+    buf = api.MoeLayerBuffers(T, E, K, H, I, R, dev)
+    y_sep = buf.forward(x, idx.to(DEV), w, w13, s13, w2, s2, fused=False).clone()
+    y = buf.forward(x, idx.to(DEV), w, w13, s13, w2, s2).clone()
+    pk = api.MoeLayerBuffers(T, E, K, H, I, R, dev, packed=True)
+    y_pk = pk.forward(x, idx.to(DEV), w, w13, s13, w2, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_sep.view(torch.int16))
+    assert torch.equal(y.view(torch.int16), y_pk.view(torch.int16))
+    rr = O.route(idx.numpy(), E, R)
+    assert np.array_equal(buf.src_map.cpu().numpy(), rr.src_map)
+    assert buf.counts.cpu().numpy().tolist() == rr.counts.tolist()
+    st = buf.dev_status.cpu().tolist()
+    assert st[1] == rr.dropped > 0 and st[0] & api.DEV_CAPACITY_DROPPED
+    experts = list(range(0, E, 16))
+    wts = host_weights({"w13": w13, "s13": s13, "w2": w2, "s2": s2}, experts)
+    src = rr.src_map
+    for e in experts:
+        tk = np.argwhere((idx.numpy() == e) & (src >= 0))
+        if len(tk) == 0:
+            continue
+        ref = oracle_expert_rows(f32(x[torch.from_numpy(tk[:, 0]).to(DEV)]), wts[e])
+        got = f32(buf.out.view(-1, H)[torch.from_numpy(src[tk[:, 0], tk[:, 1]]).long().to(DEV)])
+        assert_rows_close(got, ref, what=f"expert {e}")
