@@ -770,12 +770,15 @@ def test_layer_degenerate_routings(fused):
 
 
 @pytest.mark.parametrize("T,E,K,H,I,R", [(50, 1, 1, 384, 128, 64), (90, 40, 32, 640, 256, 80),
-                                         (33, 3, 2, 128, 384, 16)])
+                                         (33, 3, 2, 128, 384, 16), (64, 4, 2, 16384, 128, 48),
+                                         (48, 4, 2, 128, 16384, 40)])
 def test_layer_paths_odd_shapes(T, E, K, H, I, R):
     """The fused and separate layer paths on shapes off the benchmarked grid:
     one expert with top-1, top-32 of 40 experts, H % 256 = 128 (128-column
-    down tiles), H = 128 (one K group), a single gate/up tile per block; y
-    the same bytes on both paths and every kept route against the oracle."""
+    down tiles), H = 128 (one K group), a single gate/up tile per block, and
+    the largest hidden and intermediate sizes the library takes (16384, with
+    the other side at one 128-group); y the same bytes on both paths and every
+    kept route against the oracle."""
     dev = torch.device(DEV)
     g = torch.Generator().manual_seed(T + E + K)
     idx = torch.stack([torch.randperm(E, generator=g)[:K] for _ in range(T)])
