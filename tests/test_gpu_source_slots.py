@@ -277,3 +277,35 @@ def test_expert_compute_source_slots_both_launch_forms():
         inter.append(out)
     assert torch.equal(_bits(inter[0]), _bits(inter[1]))
     assert not torch.equal(_bits(inter[0]), _bits(outs[0]))   # the flag reaches the GEMM
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_layer_source_slots_degenerate(fused):
+    """The per-source lane on no tokens (counts and seg_counts reset) and on
+    every route a padding route (no slot rows, y = 0), on both paths."""
+    E, L, K, H, I, mt = 8, 2, 2, 256, 128, 6
+    Wr = E // L
+    dev = torch.device(DEV)
+    w13, s13, w2, s2 = (t.to(DEV) for t in W.expert_weights(E, H, I, 3, "cpu"))
+    ss = api.MoeLayerBuffers(0, E, K, H, I, Wr * mt, dev, source_slots=mt, L=L)
+    ss.counts.fill_(99)
+    ss.seg_counts.fill_(99)
+    y = ss.forward(torch.empty(0, H, dtype=torch.bfloat16, device=DEV),
+                   torch.empty(0, K, dtype=torch.int64, device=DEV), torch.empty(0, K, device=DEV),
+                   w13, s13, w2, s2, fused=fused)
+    torch.cuda.synchronize()
+    assert y.shape == (0, H)
+    assert ss.counts.cpu().tolist() == [0] * E
+    assert bool((ss.seg_counts == 0).all()) and ss.dev_status.cpu().tolist() == [0, 0]
+    T = 20
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(T, H, generator=g).to(torch.bfloat16).to(DEV)
+    ss = api.MoeLayerBuffers(T, E, K, H, I, Wr * mt, dev, source_slots=mt, L=L)
+    ss.y.fill_(7.0)
+    ss.out.fill_(9.0)
+    y = ss.forward(x, torch.full((T, K), -1, dtype=torch.int64, device=DEV),
+                   torch.rand(T, K, generator=g).to(DEV), w13, s13, w2, s2, fused=fused)
+    torch.cuda.synchronize()
+    assert ss.counts.cpu().tolist() == [0] * E and bool((ss.seg_counts == 0).all())
+    assert bool((y.float() == 0).all()) and bool((ss.src_map == -1).all())
+    assert bool((ss.out.float() == 9.0).all()), "no slot row may be written"
